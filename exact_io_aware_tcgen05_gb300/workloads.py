@@ -1,0 +1,114 @@
+"""The attention workloads this library is measured and checked on, and their FLOP counts.
+
+Each workload is named by what it is and its sizes.  FLOPs are algorithmic:
+only visible (query, key) pairs count.  The forward pass counts 4*d per pair
+and query head (S = QK^T and O = PV, 2*d each).  The backward pass counts
+10*d: the five products a backward pass needs (S recomputed once, dP, dV, dK
+and dQ), i.e. the customary 2.5x the forward.  Extra products a kernel
+issues beyond those (a second S and dP for a split dQ pass) are not counted,
+nor is masked-out work.  Causal masking therefore halves the count, and a
+sliding window of W keys counts sum_i min(i + 1, W).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+from .inputs import cu_seqlens_of, varlen_lengths
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int                 # sequences in the batch
+    Hq: int                # query heads
+    Hkv: int               # key/value heads (Hq % Hkv == 0)
+    N: int                 # sequence length (packed: the longest sequence)
+    d: int                 # head dimension
+    causal: bool
+    window: int            # 0: none; else keys visible per query, including itself
+    backward: bool         # whether the workload includes the backward pass
+    lengths: Optional[Tuple[int, ...]] = None   # packed batch: per-sequence lengths
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def packed(self) -> bool:
+        return self.lengths is not None
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths)) if self.packed else self.B * self.N
+
+    def cu_seqlens(self):
+        return cu_seqlens_of(self.lengths) if self.packed else None
+
+    @property
+    def q_shape(self):
+        return (self.total_tokens, self.Hq, self.d) if self.packed else (self.B, self.N, self.Hq, self.d)
+
+    @property
+    def kv_shape(self):
+        return (self.total_tokens, self.Hkv, self.d) if self.packed else (self.B, self.N, self.Hkv, self.d)
+
+    @property
+    def lse_shape(self):
+        return (self.Hq, self.total_tokens) if self.packed else (self.B, self.Hq, self.N)
+
+    def seq_lengths(self):
+        return list(self.lengths) if self.packed else [self.N] * self.B
+
+    def visible_pairs_per_head(self) -> int:
+        return sum(visible_pairs(L, self.causal, self.window) for L in self.seq_lengths())
+
+    def fwd_flops(self) -> int:
+        return 4 * self.d * self.Hq * self.visible_pairs_per_head()
+
+    def bwd_flops(self) -> int:
+        return 10 * self.d * self.Hq * self.visible_pairs_per_head()
+
+    def fwd_io_bytes(self) -> int:
+        """Algorithmic HBM bytes of one forward: read Q, K, V; write O and LSE once."""
+        T = self.total_tokens
+        return 2 * T * self.d * (2 * self.Hq + 2 * self.Hkv) + 4 * T * self.Hq
+
+    def bwd_io_bytes(self) -> int:
+        """Algorithmic HBM bytes of one backward: read Q, K, V, O, dO, LSE; write dQ, dK, dV."""
+        T = self.total_tokens
+        return (2 * T * self.d * (3 * self.Hq + 2 * self.Hkv)      # Q, O, dO, K, V
+                + 4 * T * self.Hq                                     # LSE
+                + 2 * T * self.d * (self.Hq + 2 * self.Hkv))          # dQ, dK, dV
+
+
+def visible_pairs(L: int, causal: bool, window: int) -> int:
+    """Number of (query, key) pairs with key visible to query in one sequence of length L."""
+    if not causal:
+        return L * L
+    if window <= 0 or window >= L:
+        return L * (L + 1) // 2
+    return window * (window + 1) // 2 + (L - window) * window
+
+
+def _varlen(d: int) -> Workload:
+    lengths = tuple(int(x) for x in varlen_lengths(0, 16, 256, 8192))
+    return Workload(f"fwdbwd_varlen16_h32kv8_d{d}_causal", B=len(lengths), Hq=32, Hkv=8,
+                    N=max(lengths), d=d, causal=True, window=0, backward=True, lengths=lengths)
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("fwd_b1_h1_n128_d64", 1, 1, 1, 128, 64, False, 0, False),
+        Workload("fwd_b4_h16_n2048_d128_causal", 4, 16, 16, 2048, 128, True, 0, False),
+        Workload("fwdbwd_b2_h16_n8192_d128_causal", 2, 16, 16, 8192, 128, True, 0, True),
+        Workload("fwdbwd_b1_h32kv8_n16384_d128_causal_w4096", 1, 32, 8, 16384, 128, True, 4096,
+                 True),
+        _varlen(128),
+        _varlen(64),
+    ]
+}
+
+#: the workload the benchmark times by default: long causal sequences, d = 128, fwd + bwd
+BENCH_DEFAULT = "fwdbwd_b2_h16_n8192_d128_causal"
