@@ -1,1 +1,169 @@
+"""Exact IO-aware attention for GB300 (sm_103a): Python binding of libfa_gb300.so.
 
+The functions below carry the names of the C ABI in ``include/fa.h`` and only
+marshal arguments: pointers may be given as integers or as objects with a
+``data_ptr()`` method (e.g. torch tensors), streams as integers or objects
+with a ``cuda_stream`` attribute.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.  If the compiled library is
+missing, :func:`load` raises.
+
+:func:`attention_forward` / :func:`attention_backward` are small conveniences
+that allocate the outputs (and the backward workspace) with PyTorch and call
+the C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "FAError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status",
+    "fa_set_wait_limit_cycles", "fa_last_error", "attention_forward", "attention_backward",
+    "library_path",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
+                4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+
+_lib = None
+_vp, _i, _f, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load libfa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or library_path
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} not found: build it with exact_io_aware_tcgen05_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
+    lib.fa_fwd.restype = _i
+    lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.fa_bwd_workspace_size.restype = _sz
+    lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                           _vp, _i, _f, _vp, _sz, _vp]
+    lib.fa_bwd.restype = _i
+    lib.fa_device_status.argtypes = [_vp]
+    lib.fa_device_status.restype = _i
+    lib.fa_set_wait_limit_cycles.argtypes = [_ll]
+    lib.fa_set_wait_limit_cycles.restype = None
+    lib.fa_last_error.argtypes = []
+    lib.fa_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def fa_last_error() -> str:
+    return load().fa_last_error().decode()
+
+
+def _check(st: int):
+    if st != FA_OK:
+        raise FAError(st, fa_last_error())
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale,
+           stream=None, check: bool = True) -> int:
+    st = load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                       int(bool(causal)), int(window), _ptr(cu_seqlens), int(total_tokens),
+                       float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_bwd_workspace_size(B, Hq, Hkv, N, d, total_tokens) -> int:
+    return int(load().fa_bwd_workspace_size(B, Hq, Hkv, N, d, int(total_tokens)))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
+           total_tokens, scale, workspace, workspace_bytes, stream=None, check: bool = True) -> int:
+    st = load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                       _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)), int(window),
+                       _ptr(cu_seqlens), int(total_tokens), float(scale), _ptr(workspace),
+                       int(workspace_bytes), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_device_status(stream=None, check: bool = True) -> int:
+    st = load().fa_device_status(_stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_set_wait_limit_cycles(cycles: int) -> None:
+    load().fa_set_wait_limit_cycles(int(cycles))
+
+
+# ------------------------------------------------------------ conveniences
+
+def _geometry(q, k, cu_seqlens, max_seqlen):
+    if cu_seqlens is None:
+        B, N, Hq, d = q.shape
+        return B, N, Hq, k.shape[2], d, 0
+    T, Hq, d = q.shape
+    B = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        raise ValueError("packed batches need max_seqlen")
+    return B, int(max_seqlen), Hq, k.shape[1], d, T
+
+
+def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens=None,
+                      max_seqlen=None, stream=None):
+    """O, LSE for bf16 CUDA tensors q, k, v in the library's layouts (allocates outputs)."""
+    import torch
+    B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, T) if cu_seqlens is not None else (B, Hq, N), dtype=torch.float32,
+                      device=q.device)
+    stream = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T, scale, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=None,
+                       cu_seqlens=None, max_seqlen=None, stream=None, workspace=None):
+    """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace)."""
+    import torch
+    B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d, T)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    stream = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T,
+           scale, workspace, workspace.numel() * workspace.element_size(), stream)
+    return dq, dk, dv

@@ -1,0 +1,277 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
+// checks, TMA descriptor encoding, the device status word and kernel launches.
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+namespace fa {
+
+__device__ int g_status_word;  // written by kernels when a bounded wait gives up
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+std::atomic<long long> g_wait_limit{kDefaultTimeoutCycles};
+
+fa_status fail(fa_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// [tokens, heads, d] bf16 viewed as a 3-D tensor (d, heads, tokens); the box is
+// 64 elements of d (128 bytes, the swizzle span) x 1 head x 128 tokens.
+fa_status make_token_map(CUtensorMap* map, const void* base, int tokens, int heads, int d,
+                         const char* name) {
+    auto enc = encode_fn();
+    if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(heads) * d * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockM)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                    static_cast<int>(r));
+    return FA_OK;
+}
+
+int* status_word_ptr() {
+    // one address per device; looked up once per device
+    static std::mutex mu;
+    static int* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+struct Geometry {
+    SeqInfo seq;
+    int tokens;  // rows of the token dimension
+};
+
+fa_status check_common(int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                       const int* cu_seqlens, int total_tokens, float scale, Geometry* g) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1)
+        return fail(FA_ERR_INVALID_ARG, "B, Hq, Hkv and N must be >= 1 (got %d, %d, %d, %d)", B,
+                    Hq, Hkv, N);
+    if (Hq % Hkv != 0)
+        return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", d);
+    if (window < 0) return fail(FA_ERR_INVALID_ARG, "window must be >= 0 (got %d)", window);
+    if (window > 0 && !causal)
+        return fail(FA_ERR_INVALID_ARG, "a sliding window requires causal != 0");
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+    long long tokens;
+    if (cu_seqlens) {
+        if (total_tokens < 0)
+            return fail(FA_ERR_INVALID_ARG, "total_tokens must be >= 0 for a packed batch");
+        if (!aligned16(cu_seqlens) && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+            return fail(FA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+        tokens = total_tokens;
+    } else {
+        tokens = static_cast<long long>(B) * N;
+    }
+    if (tokens > INT_MAX / 2)
+        return fail(FA_ERR_UNSUPPORTED, "token count %lld too large", tokens);
+    if (static_cast<long long>(B) * Hq * ((N + 127) / 128) > INT_MAX / 2)
+        return fail(FA_ERR_UNSUPPORTED, "problem too large for one launch");
+    g->seq.cu_seqlens = cu_seqlens;
+    g->seq.B = B;
+    g->seq.N = N;
+    g->seq.total_tokens = static_cast<int>(tokens);
+    g->seq.Hq = Hq;
+    g->seq.Hkv = Hkv;
+    g->seq.group = Hq / Hkv;
+    g->seq.causal = causal ? 1 : 0;
+    g->seq.window = window;
+    g->tokens = static_cast<int>(tokens);
+    return FA_OK;
+}
+
+// CTAs to launch for blocks of `rows` rows per sequence and head: exact for
+// dense batches, an upper bound (sum_b ceil(len_b/rows) <= ceil(T/rows) + B)
+// for packed ones.
+int num_blocks(const Geometry& g, int rows, int heads) {
+    long long per_head;
+    if (g.seq.cu_seqlens) {
+        per_head = (static_cast<long long>(g.tokens) + rows - 1) / rows + g.seq.B;
+        long long dense_bound = static_cast<long long>(g.seq.B) * ((g.seq.N + rows - 1) / rows);
+        if (dense_bound < per_head) per_head = dense_bound;
+    } else {
+        per_head = static_cast<long long>(g.seq.B) * ((g.seq.N + rows - 1) / rows);
+    }
+    return static_cast<int>(per_head * heads);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+int* device_status_word() { return status_word_ptr(); }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_last_error(void) { return t_last_error; }
+
+void fa_set_wait_limit_cycles(long long cycles) {
+    g_wait_limit.store(cycles > 0 ? cycles : kDefaultTimeoutCycles);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N, int d, int causal, int window, const int* cu_seqlens,
+                 int total_tokens, float scale, cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    if (!q || !k || !v || !o || !lse)
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd: q, k, v, o and lse must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd: tensors must be 16-byte aligned");
+    Geometry g;
+    fa_status st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens,
+                                scale, &g);
+    if (st != FA_OK) return st;
+    if (g.tokens == 0) return FA_OK;
+
+    FwdParams p;
+    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, "q")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, "k")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, "v")) != FA_OK) return st;
+    p.seq = g.seq;
+    p.o = o;
+    p.lse = lse;
+    p.scale_log2 = scale * kLog2e;
+    p.num_work = num_blocks(g, kFwdQTiles * kBlockM, Hq);
+    p.timeout_cycles = g_wait_limit.load();
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fa_fwd: cannot resolve the device status word");
+    cudaError_t e = launch_fwd(p, d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+    return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128) || total_tokens < 0)
+        return 0;
+    (void)Hkv;
+    // delta rows: packed [Hq, T] (total_tokens > 0); dense [B, Hq, N]
+    const long long rows = total_tokens > 0 ? total_tokens : static_cast<long long>(B) * N;
+    size_t bytes = static_cast<size_t>(rows) * Hq * sizeof(float);
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, int causal, int window, const int* cu_seqlens, int total_tokens,
+                 float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "fa_bwd: tensor pointers must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(FA_ERR_INVALID_ARG, "fa_bwd: tensors must be 16-byte aligned");
+    Geometry g;
+    fa_status st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens,
+                                scale, &g);
+    if (st != FA_OK) return st;
+    const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, N, d, cu_seqlens ? total_tokens : 0);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace of %zu bytes needed, got %zu%s", need,
+                    workspace_bytes, workspace ? "" : " (null)");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace must be 256-byte aligned");
+    if (g.tokens == 0) return FA_OK;
+
+    BwdParams p;
+    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, "q")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, "k")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, "v")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_do, dout, g.tokens, Hq, d, "dout")) != FA_OK) return st;
+    p.seq = g.seq;
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.delta = static_cast<float*>(workspace);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.num_work_dq = num_blocks(g, kBlockM, Hq);
+    p.num_work_dkdv = num_blocks(g, kBlockN, Hkv);
+    p.timeout_cycles = g_wait_limit.load();
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fa_bwd: cannot resolve the device status word");
+    cudaError_t e = launch_bwd_preprocess(p, d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_bwd preprocess launch");
+    e = launch_bwd_dkdv(p, d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dk/dv launch");
+    e = launch_bwd_dq(p, d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dq launch");
+    return FA_OK;
+}
+
+fa_status fa_device_status(cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: stream synchronisation");
+    int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: reading the status word");
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: clearing the status word");
+        return fail(FA_ERR_TIMEOUT, "a kernel gave up a bounded wait (device status %d)", word);
+    }
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,366 @@
+// fa_fwd.cu -- forward pass of exact attention on sm_103a.
+//
+// Computes, per query row i, O_i = sum_j softmax_j(scale * q_i . k_j) v_j over
+// the visible keys and LSE_i = ln sum_j exp(scale * q_i . k_j), tile by tile,
+// without writing the score matrix anywhere.  The block loop is the online
+// softmax of "FlashAttention: How IO-Aware Tiling and Online Softmax Solved
+// Transformer Memory Bottlenecks" (section "1. IO-Aware Tiling": a query block
+// stays on chip while key/value blocks stream past; section "2. Online Softmax
+// Reduction": running max m, running normaliser l, rescale of the partial
+// output by exp(m_old - m_new), final division by l).  The saved statistic is
+// the logsumexp of "Flash Attention -- Fast Memory-Efficient Exact Attention"
+// ("Architecture Overview").
+//
+// One CTA owns 256 query rows of one (sequence, head) as two 128-row tiles and
+// streams the 128-key K/V tiles they need:
+//   warp 0        TMA producer: both Q tiles once, then K_j, V_j into a ring
+//   warp 1        tcgen05 issuer (one thread); owns the TMEM allocation
+//   warps 4..7    softmax + epilogue of query tile 0 (one TMEM lane = one row)
+//   warps 8..11   softmax + epilogue of query tile 1
+// TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 and O_1 (D columns each)
+// from 256.  P_t (bf16) overwrites the first 64 columns of S_t and feeds the
+// P.V product straight from TMEM.  The issuer interleaves the two tiles so the
+// tensor cores work on one tile while the softmax warps work on the other:
+//   S0=Q0K0 S1=Q1K0 | O0+=P0V0 S0=Q0K1 | O1+=P1V0 S1=Q1K1 | O0+=P0V1 ...
+// Scores are kept in log2 units (scale * log2 e folded in) and exponentiated
+// with ex2.  The running max used for exponentiation is only raised when the
+// block max exceeds it by more than 8 (a factor 256); O and l always share
+// that reference, so the result is exact and most blocks skip the O rescale.
+#include "fa_kernels.h"
+#include "fa_ptx.cuh"
+#include "fa_seq.cuh"
+
+#include <cuda_bf16.h>
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle column blocks
+    static constexpr int kChunkBytes = kBlockM * 128;      // 128 rows x 64 bf16
+    static constexpr int kTileBytes = kBlockM * D * 2;
+    static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring depth
+    static constexpr int kThreads = 384;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kColS = 0;                        // S_t at kColS + 128 t
+    static constexpr int kColO = 256;                      // O_t at kColO + D t
+    static constexpr int kTilesBytes = (kFwdQTiles + kStages) * kTileBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kTilesBytes + kBarBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+};
+
+struct FwdBars {
+    uint64_t q_full;
+    uint64_t s_full[kFwdQTiles];
+    uint64_t p_full[kFwdQTiles];
+    uint64_t o_full;
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(FwdBars) <= 256, "barrier block");
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+__global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using C = FwdCfg<D>;
+    const SeqInfo& s = p.seq;
+
+    int b, h, qblk;
+    if (!map_work(s, blockIdx.x, kFwdQTiles * kBlockM, s.Hq, true, b, h, qblk)) return;
+    int seq_start, len;
+    seq_bounds(s, b, seq_start, len);
+    const int g = h / s.group;
+    const int q0 = qblk * kFwdQTiles * kBlockM;  // first query row of the CTA (in-sequence)
+    const int q_last = min(q0 + kFwdQTiles * kBlockM - 1, len - 1);
+    const int kv_first = max(key_lo(s, q0), 0) / kBlockN;
+    const int kv_last = key_hi(s, q_last, len) / kBlockN;
+    const int nkv = kv_last - kv_first + 1;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;                                   // [2][tile]
+    uint8_t* sKV = smem + kFwdQTiles * C::kTileBytes;     // [stages][tile]
+    FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kTilesBytes);
+    volatile int* abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        bars->abort = 0;
+        mbar_init(smem_addr(&bars->q_full), 1);
+        mbar_init(smem_addr(&bars->o_full), 1);
+        for (int t = 0; t < kFwdQTiles; ++t) {
+            mbar_init(smem_addr(&bars->s_full[t]), 1);
+            mbar_init(smem_addr(&bars->p_full[t]), kBlockM);
+        }
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(smem_addr(&bars->kv_full[i]), 1);
+            mbar_init(smem_addr(&bars->kv_empty[i]), 1);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&bars->tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            const uint64_t keep = make_l2_policy_evict_last();
+            const uint32_t qbar = smem_addr(&bars->q_full);
+            mbar_arrive_expect_tx(qbar, kFwdQTiles * C::kTileBytes);
+            for (int t = 0; t < kFwdQTiles; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem_addr(sQ + t * C::kTileBytes + c * C::kChunkBytes), &p.tm_q,
+                                qbar, c * 64, h, seq_start + q0 + t * kBlockM);
+            int issued = 0;
+            for (int i = 0; i < 2 * nkv; ++i) {
+                const int st = i % C::kStages, use = i / C::kStages;
+                if (use > 0 && !mbar_wait(smem_addr(&bars->kv_empty[st]), (use - 1) & 1,
+                                          abort_flag, p.timeout_cycles, p.status))
+                    break;
+                const uint32_t fb = smem_addr(&bars->kv_full[st]);
+                mbar_arrive_expect_tx(fb, C::kTileBytes);
+                const CUtensorMap* map = (i & 1) ? &p.tm_v : &p.tm_k;
+                const int row = seq_start + (kv_first + i / 2) * kBlockN;
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes), map,
+                                     fb, c * 64, g, row, keep);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA exits
+                mbar_wait_drain(qbar, 0, p.timeout_cycles);
+                for (int i = max(0, issued - C::kStages); i < issued; ++i)
+                    mbar_wait_drain(smem_addr(&bars->kv_full[i % C::kStages]),
+                                    (i / C::kStages) & 1, p.timeout_cycles);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            auto kv_stage = [&](int i) { return i % C::kStages; };
+            auto kv_phase = [&](int i) { return (i / C::kStages) & 1; };
+            auto wait_kv = [&](int i) {
+                return mbar_wait(smem_addr(&bars->kv_full[kv_stage(i)]), kv_phase(i), abort_flag,
+                                 p.timeout_cycles, p.status);
+            };
+            auto issue_qk = [&](int t, int st) {
+                const uint32_t qa = smem_addr(sQ + t * C::kTileBytes);
+                const uint32_t ka = smem_addr(sKV + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                    mma_ss(tmem + C::kColS + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), C::kIdescQK, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int st, bool acc) {
+                const uint32_t va = smem_addr(sKV + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
+                           sdesc_sw128(va + kk * 2048, C::kChunkBytes, 1024), C::kIdescPV,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(smem_addr(&bars->q_full), 0, abort_flag, p.timeout_cycles,
+                                p.status);
+            if (ok) ok = wait_kv(0);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < kFwdQTiles; ++t) {
+                    issue_qk(t, kv_stage(0));
+                    mma_commit(smem_addr(&bars->s_full[t]));
+                }
+                mma_commit(smem_addr(&bars->kv_empty[kv_stage(0)]));
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                if (!(ok = wait_kv(iv))) break;
+                for (int t = 0; t < kFwdQTiles; ++t) {
+                    if (!(ok = mbar_wait(smem_addr(&bars->p_full[t]), j & 1, abort_flag,
+                                         p.timeout_cycles, p.status)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(t, kv_stage(iv), j > 0);
+                    if (j + 1 < nkv) {
+                        if (t == 0 && !(ok = wait_kv(ik))) break;
+                        tc_fence_after();
+                        issue_qk(t, kv_stage(ik));
+                        mma_commit(smem_addr(&bars->s_full[t]));
+                        if (t == kFwdQTiles - 1) mma_commit(smem_addr(&bars->kv_empty[kv_stage(ik)]));
+                    }
+                }
+                if (ok) mma_commit(smem_addr(&bars->kv_empty[kv_stage(iv)]));
+            }
+            // o_full also tells the teardown that no MMA is still running.
+            mma_commit(smem_addr(&bars->o_full));
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------- softmax + epilogue
+        const int t = (warp - 4) / 4;
+        const int quad = warp % 4;
+        const int r = quad * 32 + lane;               // row within the tile = TMEM lane
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + C::kColS + t * kBlockN;
+        const uint32_t tO = tmem + lane_addr + C::kColO + t * D;
+        const int q = q0 + t * kBlockM + r;           // query position in the sequence
+        const int lo_q = key_lo(s, q), hi_q = key_hi(s, q, len);
+        const int tile_q_first = q0 + t * kBlockM, tile_q_last = tile_q_first + kBlockM - 1;
+        const int full_lo = key_lo(s, tile_q_last);            // keys >= this are >= every row's lo
+        const int full_hi = key_hi(s, tile_q_first, len);      // keys <= this are <= every row's hi
+        const float sl2 = p.scale_log2;
+
+        float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full[t]), j & 1, abort_flag,
+                                                   p.timeout_cycles, p.status));
+            if (!ok) break;  // warp-uniform: the TMEM accesses below are warp-collective
+            tc_fence_after();
+            uint32_t sr[kBlockN];
+#pragma unroll
+            for (int c = 0; c < kBlockN / 32; ++c)
+                tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tmem_ld_wait();
+            reg_fence(sr);
+            float sv[kBlockN];
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) sv[c] = __uint_as_float(sr[c]);
+            const int kb = (kv_first + j) * kBlockN;
+            if (!(kb >= full_lo && kb + kBlockN - 1 <= full_hi)) {
+                const int clo = lo_q - kb, chi = hi_q - kb;
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
+                    if (c < clo || c > chi) sv[c] = kNegInf;
+            }
+            float mx = sv[0];
+#pragma unroll
+            for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
+            const float m_blk = mx * sl2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (m_blk > m_ref + kRescaleThreshold) {
+                alpha = ex2_approx(m_ref - m_blk);  // 0 on the first visible block
+                rescale = (j > 0);
+                m_ref = m_blk;
+                l *= alpha;
+            }
+            const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
+            float rs = 0.f;
+            uint32_t pk[kBlockN / 2];
+#pragma unroll
+            for (int c = 0; c < kBlockN / 2; ++c) {
+                const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, neg_ref));
+                const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, neg_ref));
+                rs += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l += rs;
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
+                // signalled; scale it in place before the next product accumulates.
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orow[32];
+                    tmem_ld32(tO + c * 32, orow);
+                    tmem_ld_wait();
+                    reg_fence(orow);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                    tmem_st32(tO + c * 32, orow);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&bars->p_full[t]));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->o_full), 0, abort_flag,
+                                                   p.timeout_cycles, p.status));
+        if (ok) {
+            tc_fence_after();
+            const bool valid = q < len;
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16* orow_g = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                    (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orow[32];
+                tmem_ld32(tO + c * 32, orow);
+                tmem_ld_wait();
+                reg_fence(orow);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                                       __uint_as_float(orow[2 * i + 1]) * inv_l);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (valid)
+                p.lse[row_stat_index(s, b, h, seq_start, q)] =
+                    (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    if (*abort_flag && warp == 1 && lane == 0) {
+        // o_full was committed last: once it fires no tcgen05 op still uses TMEM
+        mbar_wait_drain(smem_addr(&bars->o_full), 0, p.timeout_cycles);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = fa_fwd_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<p.num_work, C::kThreads, C::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+    if (p.num_work <= 0) return cudaSuccess;
+    return d == 128 ? launch_fwd_d<128>(p, stream) : launch_fwd_d<64>(p, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,67 @@
+// fa_kernels.h -- parameter blocks and launchers shared by the host API
+// (fa_api.cu) and the kernels (fa_fwd.cu, fa_bwd.cu).  Internal to the
+// library; the public interface is include/fa.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+constexpr int kBlockM = 128;   // rows of one MMA tile (TMEM lanes)
+constexpr int kBlockN = 128;   // keys per key/value tile
+constexpr int kFwdQTiles = 2;  // query tiles per forward CTA (ping-pong)
+constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// Token / sequence geometry common to all kernels.  Dense batches are the
+// packed case with sequence b starting at token b*N and length N.
+struct SeqInfo {
+    const int* cu_seqlens;  // device int32[B+1], or nullptr for dense
+    int B;                  // sequences
+    int N;                  // dense: length of every sequence; packed: longest
+    int total_tokens;       // rows of the token dimension (dense: B*N)
+    int Hq, Hkv, group;     // group = Hq / Hkv
+    int causal, window;     // window <= 0: none
+};
+
+struct FwdParams {
+    CUtensorMap tm_q;  // [total_tokens, Hq, d] bf16, box 64 x 1 x 128, 128B swizzle
+    CUtensorMap tm_k;  // [total_tokens, Hkv, d]
+    CUtensorMap tm_v;
+    SeqInfo seq;
+    void* o;            // bf16 [tokens, Hq, d]
+    float* lse;         // fp32 dense [B, Hq, N]; packed [Hq, total_tokens]
+    float scale_log2;   // softmax scale * log2(e)
+    int num_work;       // launched CTAs (upper bound on work items)
+    long long timeout_cycles;
+    int* status;        // device status word
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as in FwdParams; dO like Q
+    SeqInfo seq;
+    const void* o;      // bf16 forward output (for the preprocess)
+    const void* dout;   // bf16 dO (for the preprocess)
+    const float* lse;   // forward logsumexp, layout as FwdParams::lse
+    float* delta;       // fp32 D_i = rowsum(dO * O), same layout as lse
+    void* dq;           // bf16 outputs
+    void* dk;
+    void* dv;
+    float scale;        // softmax scale
+    float scale_log2;
+    int num_work_dq, num_work_dkdv;
+    long long timeout_cycles;
+    int* status;
+};
+
+// Launchers (defined in the kernel translation units).  They only enqueue on
+// `stream` and return the launch error.
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
+
+int* device_status_word();  // library-owned device status word (fa_api.cu)
+
+}  // namespace fa

@@ -1,0 +1,148 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library libfa_gb300.so.
+ *
+ * The library computes exact scaled dot-product attention tile by tile with an
+ * online softmax, so the N x N score / probability matrix never reaches HBM,
+ * and the backward pass by recomputation from the saved logsumexp:
+ *
+ *   "FlashAttention: How IO-Aware Tiling and Online Softmax Solved Transformer
+ *    Memory Bottlenecks" -- "Naive Attention Execution Profile" (S = QK^T,
+ *    P = softmax(S), O = PV), "1. IO-Aware Tiling", "2. Online Softmax
+ *    Reduction" (running max / normaliser, rescale, final division) and
+ *    "3. Recomputation in the Backward Pass";
+ *   "Flash Attention -- Fast Memory-Efficient Exact Attention" -- "What Flash
+ *    Attention Does" (causal masking, variable-length sequences, GQA/MQA),
+ *    "Key Features" (sliding window), "Architecture Overview" (backward from
+ *    the saved output and logsumexp statistics), "Self-Hosting &
+ *    Configuration" (BF16).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Pointers marked "device" are CUDA device pointers owned by the caller; the
+ * library never allocates, frees or keeps them, and never synchronises the
+ * stream (fa_device_status excepted).  Every tensor is contiguous, bf16 unless
+ * stated, and 16-byte aligned (TMA requirement).
+ *
+ *   dense batch (cu_seqlens == NULL): B sequences of N tokens each
+ *     q, o, dout, dq   [B, N, Hq, d]      k, v, dk, dv   [B, N, Hkv, d]
+ *     lse, workspace rows  [B, Hq, N] fp32
+ *   packed batch (cu_seqlens != NULL): B sequences concatenated, T tokens
+ *     q, o, dout, dq   [T, Hq, d]         k, v, dk, dv   [T, Hkv, d]
+ *     lse              [Hq, T] fp32
+ *     cu_seqlens       device int32[B + 1], cu_seqlens[0] = 0,
+ *                      cu_seqlens[B] = T, non-decreasing; sequence b holds
+ *                      tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ *     N must be >= the longest sequence and total_tokens must equal T: the
+ *     library cannot read cu_seqlens on the host without a synchronisation,
+ *     and uses them to bound its TMA descriptors and grids.
+ *
+ *   Scores are S_ij = scale * q_i . k_j (the page's S = QK^T with the usual
+ *   softmax scale made explicit; pass scale = 1/sqrt(d) for the standard
+ *   form).  Key j is visible to query i of the same sequence iff
+ *     causal == 0:  always;
+ *     causal != 0:  j <= i, and if window > 0 also i - j < window, i.e. each
+ *                   query sees at most `window` keys including itself.
+ *   window > 0 requires causal != 0.  Query head h reads key/value head
+ *   h / (Hq / Hkv) (consecutive grouping); Hkv == 1 is multi-query attention.
+ *   lse holds the natural-log logsumexp LSE_i = ln sum_{j visible} exp(S_ij).
+ *   A row with no visible key (impossible with the masks above unless a
+ *   sequence is empty) gets O = 0 and LSE = -inf.
+ *
+ * Supported: d in {64, 128}; 1 <= Hkv <= Hq, Hq % Hkv == 0.  Outputs are
+ * written in full (no accumulate mode), rounded to bf16 by round-to-nearest-
+ * even from fp32 accumulators.
+ *
+ * Errors: argument checks run before anything is enqueued and return
+ * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE; a failed launch
+ * returns FA_ERR_CUDA.  fa_last_error() gives a message for the calling
+ * thread's last non-OK status.  Kernels never trap: every wait inside them is
+ * bounded, and a wait that gives up records FA_ERR_TIMEOUT in a library-owned
+ * device status word, read (and cleared) by fa_device_status().
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size or flag          */
+    FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not in {64, 128})  */
+    FA_ERR_WORKSPACE = 3,    /* workspace null or smaller than fa_bwd_workspace_size  */
+    FA_ERR_CUDA = 4,         /* a CUDA call failed; see fa_last_error()               */
+    FA_ERR_TIMEOUT = 5       /* a kernel's bounded wait gave up (fa_device_status)    */
+} fa_status;
+
+/*
+ * Forward pass: O = softmax(scale * Q K^T, masked) V and LSE.
+ *   q, k, v       device, read only (layouts above)
+ *   o             device, written: bf16, layout of q
+ *   lse           device, written: fp32 [B, Hq, N] dense, [Hq, T] packed
+ *   B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens: see above
+ *                 (total_tokens is ignored for dense batches)
+ *   scale         softmax scale, finite and > 0
+ *   stream        CUDA stream the kernel is enqueued on (0: legacy default)
+ * Enqueues one kernel; returns without waiting for it.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N, int d, int causal, int window, const int* cu_seqlens,
+                 int total_tokens, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes (fp32 row
+ * statistics D_i = sum_c dO_ic O_ic, one per query row and head, padded to
+ * 256 bytes).  total_tokens: T for a packed batch, 0 for a dense one (whose
+ * B * N rows are used).  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens);
+
+/*
+ * Backward pass of fa_fwd for the loss gradient dO, recomputing S and P from
+ * the saved logsumexp ("3. Recomputation in the Backward Pass"):
+ *   D_i = dO_i . O_i,  P_ij = exp(S_ij - LSE_i),  dP_ij = dO_i . v_j,
+ *   dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ *   dV_j = sum_i P_ij dO_i,
+ * with dK and dV summed over the query heads that share a key/value head.
+ * (The pages give no backward formulas; these are the calculus of softmax.)
+ *   q, k, v, o, lse, dout   device, read only; o and lse as written by fa_fwd
+ *   dq, dk, dv              device, written (bf16, layouts of q, k, v)
+ *   workspace               device, >= fa_bwd_workspace_size(...) bytes,
+ *                           256-byte aligned, contents on entry ignored; it
+ *                           must not be shared by calls in flight together
+ * dQ, dK and dV are deterministic: the same inputs give the same bits.
+ * Enqueues three kernels on `stream`; returns without waiting.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, int causal, int window, const int* cu_seqlens, int total_tokens,
+                 float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait since the last call (its outputs are then incomplete), or
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_device_status(cudaStream_t stream);
+
+/*
+ * Cycle budget of every bounded wait inside the kernels (default about two
+ * seconds of SM clock).  Values <= 0 restore the default.  Host-side setting,
+ * read at each launch.
+ */
+void fa_set_wait_limit_cycles(long long cycles);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,97 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every symbol
+include/fa.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_tcgen05_gb300 import build as b
+    path = b.build()
+    import exact_io_aware_tcgen05_gb300 as fa
+    return fa, ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    _, raw = lib
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def _fwd(fa, **over):
+    args = dict(q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=1, N=128, d=128, causal=1,
+                window=0, cu_seqlens=None, total_tokens=0, scale=0.125)
+    args.update(over)
+    return fa.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                     args["Hq"], args["Hkv"], args["N"], args["d"], args["causal"],
+                     args["window"], args["cu_seqlens"], args["total_tokens"], args["scale"],
+                     None, check=False)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), 1), (dict(o=8), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(Hkv=3), 1),
+    (dict(B=0), 1), (dict(N=0), 1), (dict(window=-1), 1), (dict(window=4, causal=0), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
+    (dict(cu_seqlens=16, total_tokens=-1), 1),
+])
+def test_forward_rejects_bad_arguments(lib, over, status):
+    fa, _ = lib
+    assert _fwd(fa, **over) == status
+    assert fa.fa_last_error() != ""
+
+
+def test_backward_rejects_small_workspace(lib):
+    fa, _ = lib
+    need = fa.fa_bwd_workspace_size(2, 4, 2, 300, 128, 0)
+    st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 4, 2, 300, 128, 1, 0, None, 0, 0.1,
+                   256, need - 256, None, check=False)
+    assert st == 3 and "workspace" in fa.fa_last_error()
+    st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 4, 2, 300, 128, 1, 0, None, 0, 0.1,
+                   None, need, None, check=False)
+    assert st == 3
+    st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 4, 2, 300, 128, 1, 0, None, 0, 0.1,
+                   16, need, None, check=False)
+    assert st == 3 and "aligned" in fa.fa_last_error()
+
+
+def test_workspace_size(lib):
+    fa, _ = lib
+    # dense: B * Hq * N fp32, padded to 256 bytes
+    assert fa.fa_bwd_workspace_size(2, 16, 16, 8192, 128, 0) == 2 * 16 * 8192 * 4
+    assert fa.fa_bwd_workspace_size(1, 3, 1, 5, 64, 0) == 256
+    # packed: Hq * T
+    assert fa.fa_bwd_workspace_size(16, 32, 8, 7960, 128, 68143) == ((32 * 68143 * 4 + 255) // 256) * 256
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 1, 96, 0) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import exact_io_aware_tcgen05_gb300 as fa
+    saved = fa._lib
+    try:
+        fa._lib = None
+        with pytest.raises(RuntimeError):
+            fa.load(str(tmp_path / "missing.so"))
+    finally:
+        fa._lib = saved
