@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention (forward + backward) on GB300 through the C ABI.
+
+One step = fa_fwd + fa_bwd over one batch of the workload (seeded bf16 N(0,1)
+inputs already resident in HBM).  Prints ONE JSON line on rank 0:
+
+  value        algorithmic TFLOP/s of the whole job (forward 4*d, backward 10*d
+               per visible (query, key) pair and query head; causal halves it)
+  e2e          the same metric through the C ABI with pinned HOST buffers: each
+               step copies Q, K, V, dO in and O, LSE, dQ, dK, dV out
+  roofline     the dominant kernel (largest device time in the timed region):
+               algorithmic FLOPs per launch / its mean launch time (CUDA events
+               recorded by the library around each launch, on the launching
+               stream) against the measured bf16 tensor peak
+  cpu_baseline the fp64 oracle timed on the host cores on a bounded sample
+  clocks       SM clocks and throttle reasons sampled during the timed region
+
+--impl reference runs the fp64 CPU oracle as the reference arm instead.
+Multi-GPU (torchrun): independent replicas, one per GPU ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from exact_io_aware_tcgen05_gb300.inputs import attention_inputs  # noqa: E402
+from exact_io_aware_tcgen05_gb300.workloads import (BENCH_DEFAULT, WORKLOADS,  # noqa: E402
+                                                    visible_pairs)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16, causal-halved) and % of GB300 dense BF16 peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# Algorithmic FLOPs per visible pair and query head, split by kernel: the
+# forward's two products; of the backward's five products (S recomputed, dP,
+# dV, dK, dQ) the dK/dV kernel performs four and the dQ kernel contributes dQ
+# (its second S and dP are recomputation and not counted).
+KERNEL_FLOPS_PER_PAIR_D = {"fa_fwd": 4, "fa_bwd_dkdv": 8, "fa_bwd_dq": 2}
+KERNEL_SOURCES = {"fa_fwd": "fa_fwd.cu", "fa_bwd_dkdv": "fa_bwd.cu", "fa_bwd_dq": "fa_bwd.cu",
+                  "fa_bwd_preprocess": "fa_bwd.cu"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kernel: str) -> str:
+    path = os.path.join(ROOT, "exact_io_aware_tcgen05_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha") != source_sha(kernel):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = tempfile.TemporaryFile(mode="w+")
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- oracle
+
+def oracle_sample(w, x, target_s: float):
+    """Time the fp64 oracle (forward + backward) on a prefix of sequence 0 for the
+    query heads of key/value head 0, growing the prefix until the run takes about
+    target_s seconds.  Returns (TFLOP/s, threads, description, seconds, prefix length)."""
+    import oracle
+    oracle.build()
+    G = w.Hq // w.Hkv
+    L_full = w.seq_lengths()[0]
+    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens())
+    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens())
+    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens())
+    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens())
+
+    def run(L):
+        qg, dg = q[:L, :G].transpose(1, 0, 2), do[:L, :G].transpose(1, 0, 2)
+        t0 = time.perf_counter()
+        oracle.fwd_group(qg, k[:L, 0], v[:L, 0], w.causal, w.window, w.scale)
+        oracle.bwd_group(qg, k[:L, 0], v[:L, 0], dg, w.causal, w.window, w.scale)
+        return time.perf_counter() - t0
+
+    L = min(256, L_full)
+    t = run(L)
+    while L < L_full and t < target_s / 3:
+        L_new = min(L_full, int(L * max(1.25, min(4.0, math.sqrt(target_s / max(t, 1e-3))))))
+        L_new = max(L + 1, L_new)
+        L, t = L_new, run(L_new)
+    flops = 14 * w.d * G * visible_pairs(L, w.causal, w.window)
+    desc = (f"sequence 0, first {L} of {L_full} tokens, query heads 0..{G - 1} (key/value head 0), "
+            f"forward + backward in fp64")
+    return flops / t / 1e12, oracle.threads(), desc, t, L
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, w):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed)
+    total = args.steps + args.warmup
+    per_step = min(10.0, max(0.3, 120.0 / max(total, 1)))   # whole run within a few minutes
+    _, threads, desc, _, L = oracle_sample(w, x, per_step)
+    import oracle
+    G = w.Hq // w.Hkv
+    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens())[:L, :G].transpose(1, 0, 2)
+    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens())[:L, :G].transpose(1, 0, 2)
+    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens())[:L, 0]
+    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens())[:L, 0]
+    times = []
+    for i in range(total):
+        t0 = time.perf_counter()
+        oracle.fwd_group(q, k, v, w.causal, w.window, w.scale)
+        oracle.bwd_group(q, k, v, do, w.causal, w.window, w.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    flops = 14 * w.d * G * visible_pairs(L, w.causal, w.window)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "cpu run; no L2 involved"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, l2_note):
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+           "causal": w.causal, "window": w.window, "packed": w.packed,
+           "total_tokens": w.total_tokens, "scale": "1/sqrt(d)", "inputs": "bf16 iid N(0,1), seed 0",
+           "l2": l2_note}
+    if w.packed:
+        cfg["lengths"] = list(w.lengths)
+    return cfg
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import torch
+    rank, world, local_rank = dist_info()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from exact_io_aware_tcgen05_gb300 import build as libbuild
+    libbuild.build()
+    import exact_io_aware_tcgen05_gb300 as fa
+    fa.load()
+
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed)
+
+    def pinned(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    h_in = {n: pinned(x[n]) for n in ("q", "k", "v", "dout")}
+    d_in = {n: t.to(dev) for n, t in h_in.items()}
+    cu = None if not w.packed else torch.from_numpy(w.cu_seqlens()).to(dev)
+    T = w.total_tokens if w.packed else 0
+    o = torch.empty_like(d_in["q"])
+    lse = torch.empty(w.lse_shape, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(d_in["q"]), torch.empty_like(d_in["k"]),
+                  torch.empty_like(d_in["v"]))
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    geo = (w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, cu, T, w.scale)
+
+    def step(ev_f=None, ev_b=None):
+        if ev_f is not None:
+            fa.fa_set_launch_events(ev_f)
+        fa.fa_fwd(d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
+        if ev_b is not None:
+            fa.fa_set_launch_events(ev_b)
+        fa.fa_bwd(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk, dv, *geo, ws,
+                  ws_bytes, s)
+
+    in_bytes = sum(t.numel() * 2 for t in d_in.values()) + o.numel() * 2
+    flush = in_bytes < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    l2_note = (f"L2 flushed between steps (write of {2 * L2_BYTES >> 20} MiB outside the step events)"
+               if flush else f"inputs larger than L2 ({in_bytes >> 20} MiB per step); no flush")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    fa.fa_device_status(s)
+
+    K = args.steps
+    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in sum(ev_f, []) + sum(ev_b, []):
+        e.record(stream)      # instantiate the CUDA events
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)] if flush else None
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        if flush:
+            scratch.fill_(float(i))
+            step_ev[i][0].record(stream)
+        step(ev_f[i], ev_b[i])
+        if flush:
+            step_ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    fa.fa_device_status(s)
+
+    if flush:
+        elapsed = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        elapsed = t_start.elapsed_time(t_end)
+    kern_ms = {
+        "fa_fwd": [a.elapsed_time(b) for a, b in ev_f],
+        "fa_bwd_preprocess": [e[0].elapsed_time(e[1]) for e in ev_b],
+        "fa_bwd_dkdv": [e[1].elapsed_time(e[2]) for e in ev_b],
+        "fa_bwd_dq": [e[2].elapsed_time(e[3]) for e in ev_b],
+    }
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    ms_per_step = elapsed / K
+    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    value = world * (fwd_flops + bwd_flops) / (ms_per_step / 1e3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers
+    E = max(1, args.e2e_steps)
+    h_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+             "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+             "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
+             "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
+             "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
+    d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(E):
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        step()
+        for n in h_out:
+            h_out[n].copy_(d_out[n], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    fa.fa_device_status(s)
+    e2e_ms = e0.elapsed_time(e1) / E
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * (fwd_flops + bwd_flops) / (e2e_ms / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = measured_peaks()
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    pairs_heads = w.visible_pairs_per_head() * w.Hq
+    kernels = {}
+    for name, times in kern_ms.items():
+        mean = sum(times) / len(times)
+        entry = {"ms_mean": mean, "launches": len(times), "share": None}
+        if name in KERNEL_FLOPS_PER_PAIR_D:
+            fl = KERNEL_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
+            entry["algorithmic_tflop_per_launch"] = fl / 1e12
+            entry["tflops"] = fl / (mean / 1e3) / 1e12
+        else:
+            by = 2 * w.total_tokens * w.Hq * w.d * 2 + 4 * w.total_tokens * w.Hq
+            entry["algorithmic_bytes_per_launch"] = by
+            entry["gbs"] = by / (mean / 1e3) / 1e9
+        kernels[name] = entry
+    tot = sum(k["ms_mean"] for k in kernels.values())
+    for k in kernels.values():
+        k["share"] = k["ms_mean"] / tot
+    dom = max((n for n in kernels if n in KERNEL_FLOPS_PER_PAIR_D), key=lambda n: kernels[n]["ms_mean"])
+    roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": peak_tf,
+            "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_tf,
+            "peak_source": f"{peak_src} bf16_tflops (burst)" + (" of measured" if peak_src == "measured" else " of fallback"),
+            "traffic": recorded_traffic(dom, w.name)}
+    fwd_tf = fwd_flops / (kernels["fa_fwd"]["ms_mean"] / 1e3) / 1e12
+    bwd_ms = sum(kernels[n]["ms_mean"] for n in ("fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq"))
+    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, threads, desc, secs, _ = oracle_sample(w, x, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, l2_note),
+            "pct_of_peak": value / world / peak_tf,
+            "fwd_tflops": fwd_tf, "fwd_pct_of_peak": fwd_tf / peak_tf,
+            "bwd_tflops": bwd_tf, "bwd_pct_of_peak": bwd_tf / peak_tf,
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E},
+            "gpu_launches": world * K * 4, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = WORKLOADS[args.workload]
+    if not w.backward:
+        raise SystemExit(f"{w.name} is a forward-only parity case; bench steps run fwd + bwd")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

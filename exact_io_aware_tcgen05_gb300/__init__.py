@@ -18,7 +18,7 @@ import os
 
 __all__ = [
     "FAError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status",
-    "fa_set_wait_limit_cycles", "fa_last_error", "attention_forward", "attention_backward",
+    "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
     "library_path",
 ]
 
@@ -59,6 +59,8 @@ def load(path: str | None = None):
     lib.fa_device_status.restype = _i
     lib.fa_set_wait_limit_cycles.argtypes = [_ll]
     lib.fa_set_wait_limit_cycles.restype = None
+    lib.fa_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), _i]
+    lib.fa_set_launch_events.restype = None
     lib.fa_last_error.argtypes = []
     lib.fa_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -120,6 +122,25 @@ def fa_device_status(stream=None, check: bool = True) -> int:
     if check:
         _check(st)
     return st
+
+
+_armed_events = None   # keeps the handle array alive until the armed call has used it
+
+
+def fa_set_launch_events(events) -> None:
+    """Arm per-kernel timing for this thread's next fa_fwd / fa_bwd call.
+
+    ``events``: cudaEvent_t handles (ints) or torch.cuda.Event objects that have
+    been recorded at least once; None disarms.
+    """
+    global _armed_events
+    if events is None:
+        _armed_events = None
+        load().fa_set_launch_events(None, 0)
+        return
+    handles = [e if isinstance(e, int) else e.cuda_event for e in events]
+    _armed_events = (ctypes.c_void_p * len(handles))(*handles)
+    load().fa_set_launch_events(_armed_events, len(handles))
 
 
 def fa_set_wait_limit_cycles(cycles: int) -> None:

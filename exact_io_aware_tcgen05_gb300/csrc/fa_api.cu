@@ -22,6 +22,25 @@ __device__ int g_status_word;  // written by kernels when a bounded wait gives u
 namespace {
 
 thread_local char t_last_error[512] = "";
+thread_local const cudaEvent_t* t_events = nullptr;  // armed by fa_set_launch_events
+thread_local int t_event_count = 0;
+
+// Takes (and disarms) the events armed for this call; fails if too few.
+fa_status take_events(int kernels, const cudaEvent_t** out) {
+    *out = t_events;
+    const int count = t_event_count;
+    t_events = nullptr;
+    t_event_count = 0;
+    if (*out && count < kernels + 1) {
+        *out = nullptr;
+        return FA_ERR_INVALID_ARG;
+    }
+    return FA_OK;
+}
+
+cudaError_t record(const cudaEvent_t* ev, int i, cudaStream_t stream) {
+    return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess;
+}
 std::atomic<long long> g_wait_limit{kDefaultTimeoutCycles};
 
 fa_status fail(fa_status st, const char* fmt, ...) {
@@ -162,6 +181,11 @@ extern "C" {
 
 const char* fa_last_error(void) { return t_last_error; }
 
+void fa_set_launch_events(const cudaEvent_t* events, int count) {
+    t_events = (events && count > 0) ? events : nullptr;
+    t_event_count = t_events ? count : 0;
+}
+
 void fa_set_wait_limit_cycles(long long cycles) {
     g_wait_limit.store(cycles > 0 ? cycles : kDefaultTimeoutCycles);
 }
@@ -170,6 +194,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int Hkv, int N, int d, int causal, int window, const int* cu_seqlens,
                  int total_tokens, float scale, cudaStream_t stream) {
     t_last_error[0] = '\0';
+    const cudaEvent_t* ev = nullptr;
+    if (take_events(1, &ev) != FA_OK)
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd: fa_set_launch_events needs >= 2 events");
     if (!q || !k || !v || !o || !lse)
         return fail(FA_ERR_INVALID_ARG, "fa_fwd: q, k, v, o and lse must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -192,7 +219,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();
     if (!p.status) return fail(FA_ERR_CUDA, "fa_fwd: cannot resolve the device status word");
-    cudaError_t e = launch_fwd(p, d, stream);
+    cudaError_t e = record(ev, 0, stream);
+    if (e == cudaSuccess) e = launch_fwd(p, d, stream);
+    if (e == cudaSuccess) e = record(ev, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
     return FA_OK;
 }
@@ -212,6 +241,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int d, int causal, int window, const int* cu_seqlens, int total_tokens,
                  float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     t_last_error[0] = '\0';
+    const cudaEvent_t* ev = nullptr;
+    if (take_events(3, &ev) != FA_OK)
+        return fail(FA_ERR_INVALID_ARG, "fa_bwd: fa_set_launch_events needs >= 4 events");
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: tensor pointers must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -249,11 +281,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();
     if (!p.status) return fail(FA_ERR_CUDA, "fa_bwd: cannot resolve the device status word");
-    cudaError_t e = launch_bwd_preprocess(p, d, stream);
+    cudaError_t e = record(ev, 0, stream);
+    if (e == cudaSuccess) e = launch_bwd_preprocess(p, d, stream);
+    if (e == cudaSuccess) e = record(ev, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd preprocess launch");
     e = launch_bwd_dkdv(p, d, stream);
+    if (e == cudaSuccess) e = record(ev, 2, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dk/dv launch");
     e = launch_bwd_dq(p, d, stream);
+    if (e == cudaSuccess) e = record(ev, 3, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dq launch");
     return FA_OK;
 }

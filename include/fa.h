@@ -138,6 +138,18 @@ fa_status fa_device_status(cudaStream_t stream);
  */
 void fa_set_wait_limit_cycles(long long cycles);
 
+/*
+ * Per-kernel timing hook.  Arms the calling thread's NEXT fa_fwd or fa_bwd
+ * call (one call, then it disarms itself): events[i] is recorded on that
+ * call's stream just before the call enqueues its i-th kernel, and events[L]
+ * just after the last one, L being the number of kernels the call enqueues
+ * (fa_fwd: 1; fa_bwd: 3 -- row statistics D, then dK/dV, then dQ).  The
+ * events are created and owned by the caller (cudaEventCreate); count must be
+ * >= L + 1, otherwise that call fails with FA_ERR_INVALID_ARG before enqueuing
+ * anything.  events == NULL disarms.
+ */
+void fa_set_launch_events(const cudaEvent_t* events, int count);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* fa_last_error(void);
 
