@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FAError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status",
+    "FAError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_static_workspace",
+    "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
     "library_path",
 ]
@@ -55,6 +56,9 @@ def load(path: str | None = None):
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                            _vp, _i, _f, _vp, _sz, _vp]
     lib.fa_bwd.restype = _i
+    lib.fa_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
+                                            _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
+    lib.fa_bwd_static_workspace.restype = _i
     lib.fa_device_status.argtypes = [_vp]
     lib.fa_device_status.restype = _i
     lib.fa_set_wait_limit_cycles.argtypes = [_ll]
@@ -112,6 +116,21 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, 
                        _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)), int(window),
                        _ptr(cu_seqlens), int(total_tokens), float(scale), _ptr(workspace),
                        int(workspace_bytes), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_bwd_static_workspace(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
+                            cu_seqlens, total_tokens, scale, stream=None, check: bool = True) -> int:
+    """fa_bwd without a workspace argument, for callers that cannot allocate device
+    memory: the scratch is a fixed array inside the library (FA_STATIC_WORKSPACE_BYTES,
+    16 MiB per GPU).  Calls on one device share that array, so calls whose work
+    overlaps on the GPU must be serialised."""
+    st = load().fa_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
+                                        int(bool(causal)), int(window), _ptr(cu_seqlens),
+                                        int(total_tokens), float(scale), _stream(stream))
     if check:
         _check(st)
     return st

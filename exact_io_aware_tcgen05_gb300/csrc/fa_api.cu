@@ -173,6 +173,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 int* device_status_word() { return status_word_ptr(); }
 
+fa_status report_error(fa_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 }  // namespace fa
 
 using namespace fa;

@@ -3,6 +3,8 @@
 // library; the public interface is include/fa.h.
 #pragma once
 
+#include "../../include/fa.h"
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -63,5 +65,8 @@ cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
 
 int* device_status_word();  // library-owned device status word (fa_api.cu)
+
+// Records `fmt` as the calling thread's fa_last_error() message; returns st.
+fa_status report_error(fa_status st, const char* fmt, ...);
 
 }  // namespace fa

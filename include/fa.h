@@ -124,6 +124,38 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Backward pass with a built-in workspace, for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point.
+ *
+ * fa_bwd needs fa_bwd_workspace_size() bytes of device scratch, normally
+ * allocated by the caller.  Some callers cannot call cudaMalloc where they
+ * run the backward pass (a framework whose allocator owns all device memory,
+ * a plugin that may not allocate behind its host, code that must not
+ * allocate because allocation synchronises or may fail mid-step).  This
+ * variant takes the same arguments as fa_bwd minus the workspace, and uses a
+ * fixed array of FA_STATIC_WORKSPACE_BYTES bytes that the library image
+ * places in device memory (every GPU that loads the library holds it until
+ * the process exits).  It calls no allocating routine.
+ *
+ *   - Sizes whose workspace exceeds FA_STATIC_WORKSPACE_BYTES (Hq * tokens
+ *     fp32 row statistics, i.e. Hq * T <= 4,194,304 rows) are rejected with
+ *     FA_ERR_WORKSPACE and a message, before anything is enqueued; other
+ *     argument errors are those of fa_bwd.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose work
+ *     overlaps on the GPU race on it: serialise them.
+ */
+#define FA_STATIC_WORKSPACE_BYTES (16 * 1024 * 1024)
+fa_status fa_bwd_static_workspace(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk,
+                                  void* dv, int B, int Hq, int Hkv, int N, int d, int causal,
+                                  int window, const int* cu_seqlens, int total_tokens,
+                                  float scale, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel gave up a
  * bounded wait since the last call (its outputs are then incomplete), or
