@@ -162,10 +162,10 @@ def oracle_sample(w, x, target_s: float):
     oracle.build()
     G = w.Hq // w.Hkv
     L_full = w.seq_lengths()[0]
-    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens())
-    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens())
-    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens())
-    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens())
+    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))
+    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), slice(0, 1))
+    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), slice(0, 1))
+    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))
 
     def run(L):
         qg, dg = q[:L, :G].transpose(1, 0, 2), do[:L, :G].transpose(1, 0, 2)
@@ -198,10 +198,10 @@ def run_reference(args, w):
     _, threads, desc, _, L = oracle_sample(w, x, per_step)
     import oracle
     G = w.Hq // w.Hkv
-    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens())[:L, :G].transpose(1, 0, 2)
-    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens())[:L, :G].transpose(1, 0, 2)
-    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens())[:L, 0]
-    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens())[:L, 0]
+    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
+    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
+    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), 0)[:L]
+    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), 0)[:L]
     times = []
     for i in range(total):
         t0 = time.perf_counter()

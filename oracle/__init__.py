@@ -240,13 +240,17 @@ def attention_bwd(q, k, v, dout, *, causal: bool = False, window: int = 0, scale
     return dq, dk, dv
 
 
-def sequence_views(x, b, cu_seqlens):
-    """[L, H, d] view of sequence b in either layout (float64)."""
-    x = to_f64(x)
+def sequence_views(x, b, cu_seqlens, heads=None):
+    """[L, H, d] array of sequence b in either layout (float64), optionally only the
+    heads in the slice ``heads``.  Only the selected part is decoded."""
     if cu_seqlens is None:
-        return x[b]
-    cu = np.asarray(cu_seqlens, dtype=np.int64)
-    return x[int(cu[b]):int(cu[b + 1])]
+        part = x[b]
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        part = x[int(cu[b]):int(cu[b + 1])]
+    if heads is not None:
+        part = part[:, heads]
+    return to_f64(part)
 
 
 def fwd_rows(q, k, v, b: int, h: int, rows, *, causal: bool, window: int, scale: float,
@@ -255,9 +259,9 @@ def fwd_rows(q, k, v, b: int, h: int, rows, *, causal: bool, window: int, scale:
     Hq, Hkv = q.shape[-2], k.shape[-2]
     G = Hq // Hkv
     g = h // G
-    qs = sequence_views(q, b, cu_seqlens)[:, h:h + 1].transpose(1, 0, 2)
-    ks = sequence_views(k, b, cu_seqlens)[:, g]
-    vs = sequence_views(v, b, cu_seqlens)[:, g]
+    qs = sequence_views(q, b, cu_seqlens, slice(h, h + 1)).transpose(1, 0, 2)
+    ks = sequence_views(k, b, cu_seqlens, g)
+    vs = sequence_views(v, b, cu_seqlens, g)
     o, lse = fwd_group(qs, ks, vs, causal, window, scale, rows=rows)
     return o[0], lse[0]
 
@@ -268,8 +272,8 @@ def bwd_rows(q, k, v, dout, b: int, g: int, qrows, krows, *, causal: bool, windo
     Hq, Hkv = q.shape[-2], k.shape[-2]
     G = Hq // Hkv
     hs = slice(g * G, (g + 1) * G)
-    qs = sequence_views(q, b, cu_seqlens)[:, hs].transpose(1, 0, 2)
-    ds = sequence_views(dout, b, cu_seqlens)[:, hs].transpose(1, 0, 2)
-    ks = sequence_views(k, b, cu_seqlens)[:, g]
-    vs = sequence_views(v, b, cu_seqlens)[:, g]
+    qs = sequence_views(q, b, cu_seqlens, hs).transpose(1, 0, 2)
+    ds = sequence_views(dout, b, cu_seqlens, hs).transpose(1, 0, 2)
+    ks = sequence_views(k, b, cu_seqlens, g)
+    vs = sequence_views(v, b, cu_seqlens, g)
     return bwd_group(qs, ks, vs, ds, causal, window, scale, qrows=qrows, krows=krows)

@@ -1,0 +1,112 @@
+"""Every workload at its full size, in the launch configuration bench.py times,
+checked on sampled rows against the fp64 oracle (which computes them one by one).
+
+Rows sampled per (sequence, head): the first and last rows, both sides of the
+128-row tile edges near the start, middle and end, and a few seeded random
+rows; sequences: the first, the last, and for packed batches also the longest
+and the shortest.  The backward pass is checked on whole key/value-head groups:
+dQ for all query heads of the group at the sampled rows, dK and dV at the
+sampled key rows, by relative Frobenius error over the samples.
+"""
+import numpy as np
+import pytest
+
+from exact_io_aware_tcgen05_gb300.inputs import attention_inputs
+from exact_io_aware_tcgen05_gb300.workloads import WORKLOADS
+from helpers import GRAD_REL_FRO, LSE_MAX_ABS, O_MAX_ABS, max_abs, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(L, seed):
+    base = {0, 1, L - 1, L - 2}
+    for c in (128, 256, L // 2 - (L // 2) % 128, L - L % 128 if L % 128 else L - 128):
+        base |= {c - 1, c, c + 1}
+    rng = np.random.default_rng(seed)
+    base |= set(int(r) for r in rng.integers(0, L, size=6))
+    return sorted(r for r in base if 0 <= r < L)
+
+
+def sampled_sequences(w):
+    lens = w.seq_lengths()
+    s = {0, len(lens) - 1}
+    if w.packed:
+        s |= {int(np.argmax(lens)), int(np.argmin(lens))}
+    return sorted(s)
+
+
+def run_workload(fa, w, x):
+    import torch
+    dev = torch.device("cuda", 0)
+
+    def d(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = d(x["q"]), d(x["k"]), d(x["v"])
+    cu = None if not w.packed else torch.from_numpy(w.cu_seqlens()).to(dev)
+    T = w.total_tokens if w.packed else 0
+    o = torch.empty_like(q)
+    lse = torch.empty(w.lse_shape, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    geo = (w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, cu, T, w.scale)
+    fa.fa_fwd(q, k, v, o, lse, *geo, s)
+    out = {"o": o, "lse": lse}
+    if w.backward:
+        do = d(x["dout"])
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *geo, ws, ws_bytes, s)
+        out.update(dq=dq, dk=dk, dv=dv)
+    fa.fa_device_status(s)
+    return {n: t.float().cpu().numpy().astype(np.float64) for n, t in out.items()}
+
+
+def token_index(w, b, rows):
+    """Token indices (packed) or in-sequence rows (dense) of sequence b."""
+    if w.packed:
+        return w.cu_seqlens()[b] + np.asarray(rows)
+    return np.asarray(rows)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_full_size_sampled(fa, oracle_mod, name):
+    w = WORKLOADS[name]
+    x = attention_inputs(w.q_shape, w.kv_shape, 0, with_dout=w.backward)
+    got = run_workload(fa, w, x)
+    cu = w.cu_seqlens()
+    G = w.Hq // w.Hkv
+    for b in sampled_sequences(w):
+        L = w.seq_lengths()[b]
+        rows = sample_rows(L, seed=b)
+        t = token_index(w, b, rows)
+        for h in sorted({0, w.Hq // 2, w.Hq - 1}):
+            o_ref, lse_ref = oracle_mod.fwd_rows(x["q"], x["k"], x["v"], b, h, rows,
+                                                 causal=w.causal, window=w.window, scale=w.scale,
+                                                 cu_seqlens=cu)
+            if w.packed:
+                o_got, lse_got = got["o"][t, h], got["lse"][h, t]
+            else:
+                o_got, lse_got = got["o"][b, t, h], got["lse"][b, h, t]
+            assert max_abs(o_got, o_ref) <= O_MAX_ABS, (b, h)
+            assert max_abs(lse_got, lse_ref) <= LSE_MAX_ABS, (b, h)
+    if not w.backward:
+        return
+    for b in sampled_sequences(w)[:2]:
+        L = w.seq_lengths()[b]
+        rows = sample_rows(L, seed=100 + b)
+        t = token_index(w, b, rows)
+        for g in sorted({0, w.Hkv - 1}):
+            dq_ref, dk_ref, dv_ref = oracle_mod.bwd_rows(
+                x["q"], x["k"], x["v"], x["dout"], b, g, rows, rows, causal=w.causal,
+                window=w.window, scale=w.scale, cu_seqlens=cu)
+            hs = slice(g * G, (g + 1) * G)
+            if w.packed:
+                dq_got = got["dq"][t, hs].transpose(1, 0, 2)
+                dk_got, dv_got = got["dk"][t, g], got["dv"][t, g]
+            else:
+                dq_got = got["dq"][b, t, hs].transpose(1, 0, 2)
+                dk_got, dv_got = got["dk"][b, t, g], got["dv"][b, t, g]
+            for nm, a, r in (("dq", dq_got, dq_ref), ("dk", dk_got, dk_ref), ("dv", dv_got, dv_ref)):
+                err = rel_fro(a, r)
+                assert err <= GRAD_REL_FRO, (nm, b, g, err)
