@@ -313,7 +313,10 @@ fa_status fa_device_status(cudaStream_t stream) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: clearing the status word");
-        return fail(FA_ERR_TIMEOUT, "a kernel gave up a bounded wait (device status %d)", word);
+        if (word == 5)
+            return fail(FA_ERR_TIMEOUT, "a kernel gave up a bounded wait (device status %d)", word);
+        return fail(FA_ERR_CUDA, "a kernel reported device status %d (misaligned shared memory)",
+                    word);
     }
     return FA_OK;
 }

@@ -23,8 +23,8 @@
 //                      over the key tiles; S and dP in TMEM, dS (bf16) back to
 //                      TMEM feeds dQ += dS K
 // Warp roles in both tensor-core kernels: warp 0 TMA producer, warp 1 tcgen05
-// issuer (one thread, owns TMEM), warps 4..7 element-wise work + epilogue
-// (TMEM lane = row).
+// issuer (one thread, owns TMEM), warps 4..11 element-wise work + epilogue as
+// two warpgroups, each owning 64 of the 128 tile columns (TMEM lane = row).
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 #include "fa_seq.cuh"
@@ -81,36 +81,42 @@ struct BwdCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = kBlockM * 128;
     static constexpr int kTileBytes = kBlockM * D * 2;
-    static constexpr int kStages = 2;
-    static constexpr int kThreads = 256;
+    // ring of single-tile slots for the streamed operands (Q/dO, or K/V)
+    static constexpr int kSlots = (D == 128) ? 5 : 8;
+    static constexpr int kThreads = 384;     // warp 0 TMA, warp 1 MMA, warps 4..11 element-wise
+    static constexpr int kEwThreads = 256;   // two warpgroups, 64 tile columns each
     static constexpr int kTmemCols = 512;
     static constexpr int kColS = 0;          // S (or S^T), 128 fp32 columns
     static constexpr int kColDP = 128;       // dP (or dP^T), 128 fp32 columns
     static constexpr int kColAcc = 256;      // accumulators: dQ, or dV then dK (D each)
-    // resident pair (Q,dO or K,V) + kStages streamed pairs + row statistics
-    static constexpr int kTilesBytes = (2 + 2 * kStages) * kTileBytes;
-    static constexpr int kStatBytes = kStages * 2 * kBlockM * 4;
+    // [barriers 256 B][row statistics: 2 warpgroups x 2 buffers x 128 fp32][pad] then
+    // tiles: resident pair (K,V or Q,dO) followed by the slot ring
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kTilesBytes + kStatBytes + kBarBytes + 1024;
+    static constexpr int kStatOffset = kBarBytes;
+    static constexpr int kHeadBytes = 3072;
+    static constexpr int kTilesBytes = (2 + kSlots) * kTileBytes;
+    static constexpr int kSmemBytes = kHeadBytes + kTilesBytes;
     static constexpr uint32_t kIdescSS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
     static constexpr uint32_t kIdescTS = idesc_bf16_f32(kBlockM, D, false, true);
 };
+static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
+static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
 
 struct BwdBars {
-    uint64_t res_full;      // resident pair landed
-    uint64_t s_full;        // S and dP tiles computed
-    uint64_t ds_full;       // element-wise results written back to TMEM
-    uint64_t acc_full;      // all accumulation done
-    uint64_t st_full[2];    // streamed pair landed
-    uint64_t st_empty[2];   // streamed pair consumed
+    uint64_t res_full;        // resident pair landed
+    uint64_t s_full;          // S (S^T) tile computed
+    uint64_t dp_full;         // dP (dP^T) tile computed
+    uint64_t p_full;          // element-wise: S consumed (dK/dV: P^T written back)
+    uint64_t ds_full;         // element-wise: dS written back to TMEM
+    uint64_t acc_full;        // all accumulation done
+    uint64_t slot_full[8];    // streamed tile landed in slot
+    uint64_t slot_empty[8];   // streamed tile consumed
+    uint64_t stat_full[2][2]; // dK/dV: row statistics of a step staged [warpgroup][buffer]
     uint32_t tmem_base;
     int abort;
 };
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
-}
+static_assert(sizeof(BwdBars) <= BwdCfg<128>::kBarBytes, "barrier block");
+static_assert(BwdCfg<128>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<128>::kHeadBytes, "stats");
 
 // a[rows: K-major 128 x D] . b[rows: K-major 128 x D]^T -> tmem (128 x 128 fp32)
 template <int D>
@@ -124,14 +130,18 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a, uint32_t b
     }
 }
 
-// tmem bf16 A (128 x 128, packed at a_tmem) . b[smem rows: 128 x D, MN-major] -> d_tmem (128 x D)
+// A = bf16 operand written back to TMEM by the element-wise warpgroups: the 64
+// tile columns of warpgroup w sit, packed two per 32-bit column, in the first
+// 32 TMEM columns of that warpgroup's own 64-column range (region + 64 w).
+// D (128 x D fp32) (+)= A (128 x 128) . b[smem rows: 128 x D, MN-major].
 template <int D>
-__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b, bool acc) {
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uint32_t b, bool acc) {
     using C = BwdCfg<D>;
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024),
-               C::kIdescTS, (acc || kk > 0) ? 1u : 0u);
+        mma_ts(d_tmem, a_region + (kk / 4) * 64 + (kk % 4) * 8,
+               sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024), C::kIdescTS,
+               (acc || kk > 0) ? 1u : 0u);
 }
 
 // TMEM accumulator row (D fp32 columns) * mul -> bf16 row in global memory.
@@ -156,18 +166,56 @@ __device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, __nv_bf
     }
 }
 
+// Loads this warpgroup's 64 fp32 columns of one TMEM row.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t a[32], b[32];
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+    tmem_ld_wait();
+    reg_fence(a);
+    reg_fence(b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(a[i]);
+        v[32 + i] = __uint_as_float(b[i]);
+    }
+}
+
+// Packs 64 fp32 values to bf16 pairs and stores them in the first 32 columns at taddr.
+__device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const float (&v)[64]) {
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    tmem_st32(taddr, w);
+}
+
+// Returns false (uniformly for the CTA) if the dynamic shared memory base is not
+// 1024-byte aligned, which the 128-byte-swizzled tiles and the exact shared
+// memory budget rely on.
+__device__ __forceinline__ bool smem_base_ok(const uint8_t* base, int* status) {
+    if (smem_addr(base) & 1023u) {
+        if (threadIdx.x == 0) atomicExch(status, kDevBadSmem);
+        return false;
+    }
+    return true;
+}
+
 template <int D>
 __device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
     if (threadIdx.x == 0) {
         bars->abort = 0;
         mbar_init(smem_addr(&bars->res_full), 1);
         mbar_init(smem_addr(&bars->s_full), 1);
-        mbar_init(smem_addr(&bars->ds_full), kBlockM);
+        mbar_init(smem_addr(&bars->dp_full), 1);
+        mbar_init(smem_addr(&bars->p_full), BwdCfg<D>::kEwThreads);
+        mbar_init(smem_addr(&bars->ds_full), BwdCfg<D>::kEwThreads);
         mbar_init(smem_addr(&bars->acc_full), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_addr(&bars->st_full[i]), 1);
-            mbar_init(smem_addr(&bars->st_empty[i]), 1);
+        for (int i = 0; i < BwdCfg<D>::kSlots; ++i) {
+            mbar_init(smem_addr(&bars->slot_full[i]), 1);
+            mbar_init(smem_addr(&bars->slot_empty[i]), 1);
         }
+        for (int w = 0; w < 2; ++w)
+            for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&bars->stat_full[w][i]), kBlockM);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -191,11 +239,64 @@ __device__ __forceinline__ void teardown_bwd_cta(BwdBars* bars, int warp, long l
     }
 }
 
+// Warp-uniform bounded wait (the TMEM accesses that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          long long limit, int* status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit, status));
+}
+
+// Producer loop shared by both kernels: streams `items` tiles through the slot
+// ring (item i from map (i & 1) ? odd : even); `coords(i, head, row)` gives the
+// head and token row of item i.
+template <int D, typename Coords>
+__device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int items,
+                                             const CUtensorMap* even, const CUtensorMap* odd,
+                                             Coords coords, volatile int* abort_flag,
+                                             const BwdParams& p) {
+    using C = BwdCfg<D>;
+    const uint64_t keep = make_l2_policy_evict_last();
+    int issued = 0;
+    for (int i = 0; i < items; ++i) {
+        const int sl = i % C::kSlots, use = i / C::kSlots;
+        if (use > 0 && !mbar_wait(smem_addr(&bars->slot_empty[sl]), (use - 1) & 1, abort_flag,
+                                  p.timeout_cycles, p.status))
+            break;
+        const uint32_t fb = smem_addr(&bars->slot_full[sl]);
+        mbar_arrive_expect_tx(fb, C::kTileBytes);
+        int head, row;
+        coords(i, head, row);
+        const CUtensorMap* map = (i & 1) ? odd : even;
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d_hint(smem_addr(slots + sl * C::kTileBytes + c * C::kChunkBytes), map, fb,
+                             c * 64, head, row, keep);
+        issued = i + 1;
+    }
+    if (*abort_flag) {
+        mbar_wait_drain(smem_addr(&bars->res_full), 0, p.timeout_cycles);
+        for (int i = max(0, issued - C::kSlots); i < issued; ++i)
+            mbar_wait_drain(smem_addr(&bars->slot_full[i % C::kSlots]), (i / C::kSlots) & 1,
+                            p.timeout_cycles);
+    }
+}
+
 // ------------------------------------------------------------------ dK, dV
+//
+// Per step n (one query head of the group, one 128-row query tile) the issuer
+// runs   dV += P^T_n dO_n | S^T_{n+1} = K Q_{n+1}^T | dK += dS^T_n Q_n |
+//        dP^T_{n+1} = V dO_{n+1}^T
+// so the element-wise warps turn S^T_{n+1} into P^T_{n+1} while dK_n and
+// dP^T_{n+1} run, and dP^T_n into dS^T_n while dV_n and S^T_{n+1} run.
+// P^T overwrites S^T and dS^T overwrites dP^T in place; each product that
+// overwrites a region is issued after the product reading it (tcgen05 ops of
+// one thread execute in issue order).  Q_n and dO_n stream through the slot
+// ring as items 2n and 2n+1; the element-wise warps fetch the row statistics
+// (LSE, D) of step n+1 from global memory while they work on step n.
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
     int b, g, kblk;
     if (!map_work(s, blockIdx.x, kBlockN, s.Hkv, false, b, g, kblk)) return;
@@ -208,14 +309,11 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const int nq = qt_last - qt_first + 1;
     const int nsteps = s.group * nq;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    uint8_t* sK = smem;
-    uint8_t* sV = smem + C::kTileBytes;
-    uint8_t* sQ = smem + 2 * C::kTileBytes;                       // [stage][tile]
-    uint8_t* sDO = sQ + C::kStages * C::kTileBytes;                // [stage][tile]
-    float* sStat = reinterpret_cast<float*>(smem + C::kTilesBytes);  // [stage][lse2|delta][128]
-    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kTilesBytes + C::kStatBytes);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
+    float* sStat = reinterpret_cast<float*>(smem_raw + C::kStatOffset);   // [wg][buf][128]
+    uint8_t* sK = smem_raw + C::kHeadBytes;
+    uint8_t* sV = sK + C::kTileBytes;
+    uint8_t* sSlots = sV + C::kTileBytes;
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -224,7 +322,6 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        const uint64_t keep = make_l2_policy_evict_last();
         if (lane == 0) {
             const uint32_t rb = smem_addr(&bars->res_full);
             mbar_arrive_expect_tx(rb, 2 * C::kTileBytes);
@@ -232,152 +329,173 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dkdv_kernel(const __grid_consta
                 tma_load_3d(smem_addr(sK + c * C::kChunkBytes), &p.tm_k, rb, c * 64, g, seq_start + kb);
                 tma_load_3d(smem_addr(sV + c * C::kChunkBytes), &p.tm_v, rb, c * 64, g, seq_start + kb);
             }
-        }
-        int issued = 0;
-        for (int n = 0; n < nsteps; ++n) {
-            const int st = n % C::kStages, use = n / C::kStages;
-            const int h = g * s.group + n / nq;
-            const int q0 = (qt_first + n % nq) * kBlockM;
-            // lane 0 waits for the stage, the warp follows its verdict (uniform exit)
-            int free_ok = 1;
-            if (lane == 0 && use > 0)
-                free_ok = mbar_wait(smem_addr(&bars->st_empty[st]), (use - 1) & 1, abort_flag,
-                                    p.timeout_cycles, p.status);
-            if (!__shfl_sync(0xffffffffu, free_ok, 0)) break;
-            // row statistics of the 128 query rows: LSE in log2 units and D;
-            // rows past the sequence end get +inf / 0 so they contribute nothing
-            float* stat = sStat + st * 2 * kBlockM;
-#pragma unroll
-            for (int i = 0; i < kBlockM / 32; ++i) {
-                const int r = i * 32 + lane, q = q0 + r;
-                float l2 = kPosInf, dl = 0.f;
-                if (q < len) {
-                    const long long idx = row_stat_index(s, b, h, seq_start, q);
-                    l2 = __ldg(p.lse + idx) * kLog2eF;
-                    dl = p.delta[idx];
-                }
-                stat[r] = l2;
-                stat[kBlockM + r] = dl;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t fb = smem_addr(&bars->st_full[st]);
-                mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d_hint(smem_addr(sQ + st * C::kTileBytes + c * C::kChunkBytes), &p.tm_q,
-                                     fb, c * 64, h, seq_start + q0, keep);
-                    tma_load_3d_hint(smem_addr(sDO + st * C::kTileBytes + c * C::kChunkBytes),
-                                     &p.tm_do, fb, c * 64, h, seq_start + q0, keep);
-                }
-            }
-            issued = n + 1;
-        }
-        if (*abort_flag && lane == 0) {
-            mbar_wait_drain(smem_addr(&bars->res_full), 0, p.timeout_cycles);
-            for (int n = max(0, issued - C::kStages); n < issued; ++n)
-                mbar_wait_drain(smem_addr(&bars->st_full[n % C::kStages]), (n / C::kStages) & 1,
-                                p.timeout_cycles);
+            stream_tiles<D>(bars, sSlots, 2 * nsteps, &p.tm_q, &p.tm_do,
+                            [&](int i, int& head, int& row) {
+                                const int n = i / 2;
+                                head = g * s.group + n / nq;
+                                row = seq_start + (qt_first + n % nq) * kBlockM;
+                            },
+                            abort_flag, p);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = mbar_wait(smem_addr(&bars->res_full), 0, abort_flag, p.timeout_cycles, p.status);
+            auto wait = [&](uint64_t& bar, int parity) {
+                return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
+            };
+            auto slot = [&](int i) { return smem_addr(sSlots + (i % C::kSlots) * C::kTileBytes); };
+            auto wait_slot = [&](int i) { return wait(bars->slot_full[i % C::kSlots], (i / C::kSlots) & 1); };
+            auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[i % C::kSlots])); };
             const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
-            for (int n = 0; ok && n < nsteps; ++n) {
-                const int st = n % C::kStages;
-                if (!(ok = mbar_wait(smem_addr(&bars->st_full[st]), (n / C::kStages) & 1, abort_flag,
-                                     p.timeout_cycles, p.status)))
-                    break;
+            bool ok = wait(bars->res_full, 0) && wait_slot(0);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t aQ = smem_addr(sQ + st * C::kTileBytes);
-                const uint32_t aDO = smem_addr(sDO + st * C::kTileBytes);
-                issue_ss<D>(tmem + C::kColS, aK, aQ);     // S^T = K Q^T
-                issue_ss<D>(tmem + C::kColDP, aV, aDO);   // dP^T = V dO^T
+                issue_ss<D>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
                 mma_commit(smem_addr(&bars->s_full));
-                if (!(ok = mbar_wait(smem_addr(&bars->ds_full), n & 1, abort_flag, p.timeout_cycles,
-                                     p.status)))
-                    break;
+                ok = wait_slot(1);
+            }
+            if (ok) {
                 tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColS, aDO, n > 0);       // dV += P^T dO
-                issue_ts<D>(tmem + C::kColAcc + D, tmem + C::kColDP, aQ, n > 0);   // dK += dS^T Q
-                mma_commit(smem_addr(&bars->st_empty[st]));
+                issue_ss<D>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
+                mma_commit(smem_addr(&bars->dp_full));
+            }
+            for (int n = 0; ok && n < nsteps; ++n) {
+                const bool more = n + 1 < nsteps;
+                if (!(ok = wait(bars->p_full, n & 1))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColS, slot(2 * n + 1), n > 0);   // dV += P^T dO
+                free_slot(2 * n + 1);
+                if (more) {
+                    if (!(ok = wait_slot(2 * n + 2))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::kColS, aK, slot(2 * n + 2));                     // S^T_{n+1}
+                    mma_commit(smem_addr(&bars->s_full));
+                }
+                if (!(ok = wait(bars->ds_full, n & 1))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::kColAcc + D, tmem + C::kColDP, slot(2 * n), n > 0);  // dK += dS^T Q
+                free_slot(2 * n);
+                if (more) {
+                    if (!(ok = wait_slot(2 * n + 3))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::kColDP, aV, slot(2 * n + 3));                    // dP^T_{n+1}
+                    mma_commit(smem_addr(&bars->dp_full));
+                }
             }
             mma_commit(smem_addr(&bars->acc_full));
         }
     } else if (warp >= 4) {
         // ------------------------------------------- element-wise + epilogue
+        const int wg = (warp - 4) / 4;      // query columns [64 wg, 64 wg + 64) of each tile
         const int quad = warp % 4;
-        const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
+        const int r = quad * 32 + lane;     // key row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + C::kColS + 64 * wg;
+        const uint32_t tDP = tmem + lane_addr + C::kColDP + 64 * wg;
         const int kpos = kb + r;
         // queries that see this key: [qlo, qhi]; none if the key is past the end
         const int qlo = query_lo(s, kpos);
         const int qhi = (kpos < len) ? query_hi(s, kpos, len) : -1;
         const float sl2 = p.scale_log2;
+        // Row statistics of step m for this warpgroup's 64 query columns: thread r
+        // fetches LSE (in log2 units) of column r (r < 64) or D of column r - 64;
+        // rows past the sequence end get +inf / 0 so they contribute nothing.
+        auto fetch_stat = [&](int m) -> float {
+            const int h = g * s.group + m / nq;
+            const int q = (qt_first + m % nq) * kBlockM + 64 * wg + (r & 63);
+            if (q >= len) return r < 64 ? kPosInf : 0.f;
+            const long long idx = row_stat_index(s, b, h, seq_start, q);
+            return r < 64 ? __ldg(p.lse + idx) * kLog2eF : __ldg(p.delta + idx);
+        };
+        float next_stat = fetch_stat(0);
         bool ok = true;
         for (int n = 0; n < nsteps; ++n) {
-            const int st = n % C::kStages;
-            const int q0 = (qt_first + n % nq) * kBlockM;
-            const float* lse2 = sStat + st * 2 * kBlockM;
-            const float* dlt = lse2 + kBlockM;
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full), n & 1, abort_flag,
-                                                   p.timeout_cycles, p.status));
-            if (!ok) break;  // warp-uniform: the TMEM accesses below are warp-collective
-            tc_fence_after();
-            const bool need_mask = !(q0 >= qlo && q0 + kBlockM - 1 <= qhi);
+            const int buf = n & 1;
+            float* sb = sStat + (wg * 2 + buf) * kBlockM;
+            sb[r] = next_stat;
+            mbar_arrive(smem_addr(&bars->stat_full[wg][buf]));
+            if (n + 1 < nsteps) next_stat = fetch_stat(n + 1);   // in flight during this step
+            const int q0 = (qt_first + n % nq) * kBlockM + 64 * wg;   // first query of my columns
+            const bool need_mask = !(q0 >= qlo && q0 + 63 <= qhi);
             const int clo = qlo - q0, chi = qhi - q0;
+            if (!(ok = warp_wait(smem_addr(&bars->stat_full[wg][buf]), (n >> 1) & 1, abort_flag,
+                                 p.timeout_cycles, p.status)))
+                break;
+            const float4* lse4 = reinterpret_cast<const float4*>(sb);
+            const float4* dlt4 = reinterpret_cast<const float4*>(sb + 64);
+            // P^T = exp(S^T - LSE) (keys x queries), written back as bf16 in place
+            if (!(ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles,
+                                 p.status)))
+                break;
+            tc_fence_after();
+            float pv[64];
+            tmem_ld64(tS, pv);
 #pragma unroll
-            for (int c = 0; c < kBlockM / 32; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_addr + C::kColS + c * 32, sr);
-                tmem_ld32(tmem + lane_addr + C::kColDP + c * 32, dr);
-                tmem_ld_wait();
-                reg_fence(sr);
-                reg_fence(dr);
-                uint32_t pw[16], dw[16];
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 l = lse4[c4];
+                const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float pv[2], dv2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * i + e;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), sl2, -lse2[col]));
-                        if (need_mask && (col < clo || col > chi)) pe = 0.f;
-                        pv[e] = pe;
-                        dv2[e] = pe * (__uint_as_float(dr[2 * i + e]) - dlt[col]);
-                    }
-                    pw[i] = pack_bf16x2(pv[0], pv[1]);
-                    dw[i] = pack_bf16x2(dv2[0], dv2[1]);
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * c4 + e;
+                    float pe = ex2_approx(fmaf(pv[c], sl2, -lv[e]));
+                    if (need_mask && (c < clo || c > chi)) pe = 0.f;
+                    pv[c] = pe;
                 }
-                // P^T and dS^T overwrite columns already consumed (16c .. 16c+15 < 32c+32)
-                tmem_st16(tmem + lane_addr + C::kColS + c * 16, pw);
-                tmem_st16(tmem + lane_addr + C::kColDP + c * 16, dw);
             }
+            tmem_st_bf16x64(tS, pv);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&bars->p_full));
+            // dS^T = P^T (dP^T - D), written back as bf16 in place
+            if (!(ok = warp_wait(smem_addr(&bars->dp_full), n & 1, abort_flag, p.timeout_cycles,
+                                 p.status)))
+                break;
+            tc_fence_after();
+            float dp[64];
+            tmem_ld64(tDP, dp);
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 dl = dlt4[c4];
+                const float dv4[4] = {dl.x, dl.y, dl.z, dl.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dp[4 * c4 + e] = pv[4 * c4 + e] * (dp[4 * c4 + e] - dv4[e]);
+            }
+            tmem_st_bf16x64(tDP, dp);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_addr(&bars->ds_full));
         }
         if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->acc_full), 0, abort_flag,
-                                                   p.timeout_cycles, p.status));
+            ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
         if (ok) {
             tc_fence_after();
+            // warpgroup 0 stores dV, warpgroup 1 stores dK (scaled)
             const bool valid = kpos < len;
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
-            store_acc_row<D>(tmem + lane_addr + C::kColAcc, 1.f,
-                             reinterpret_cast<__nv_bfloat16*>(p.dv) + row, valid);
-            store_acc_row<D>(tmem + lane_addr + C::kColAcc + D, p.scale,
-                             reinterpret_cast<__nv_bfloat16*>(p.dk) + row, valid);
+            if (wg == 0)
+                store_acc_row<D>(tmem + lane_addr + C::kColAcc, 1.f,
+                                 reinterpret_cast<__nv_bfloat16*>(p.dv) + row, valid);
+            else
+                store_acc_row<D>(tmem + lane_addr + C::kColAcc + D, p.scale,
+                                 reinterpret_cast<__nv_bfloat16*>(p.dk) + row, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp, p.timeout_cycles);
 }
 
 // ---------------------------------------------------------------------- dQ
+//
+// Per key tile j the issuer runs S_j, dP_j; as soon as the element-wise warps
+// have read S_j into registers it issues S_{j+1}; when dS_j is back in TMEM
+// (over dP_j) it issues dQ += dS_j K_j and then dP_{j+1}.  K_j and V_j stream
+// through the slot ring as items 2j and 2j+1; V_j's slot is released as soon
+// as dP_j is done, K_j's after dQ_j.
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
     int b, h, qblk;
     if (!map_work(s, blockIdx.x, kBlockM, s.Hq, true, b, h, qblk)) return;
@@ -390,13 +508,10 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
     const int kt_last = key_hi(s, q_last, len) / kBlockN;
     const int nk = kt_last - kt_first + 1;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);
-    uint8_t* sQ = smem;
-    uint8_t* sDO = smem + C::kTileBytes;
-    uint8_t* sK = smem + 2 * C::kTileBytes;          // [stage][tile]
-    uint8_t* sV = sK + C::kStages * C::kTileBytes;   // [stage][tile]
-    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kTilesBytes + C::kStatBytes);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
+    uint8_t* sQ = smem_raw + C::kHeadBytes;
+    uint8_t* sDO = sQ + C::kTileBytes;
+    uint8_t* sSlots = sDO + C::kTileBytes;
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -405,117 +520,116 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t keep = make_l2_policy_evict_last();
             const uint32_t rb = smem_addr(&bars->res_full);
             mbar_arrive_expect_tx(rb, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
                 tma_load_3d(smem_addr(sQ + c * C::kChunkBytes), &p.tm_q, rb, c * 64, h, seq_start + q0);
                 tma_load_3d(smem_addr(sDO + c * C::kChunkBytes), &p.tm_do, rb, c * 64, h, seq_start + q0);
             }
-            int issued = 0;
-            for (int j = 0; j < nk; ++j) {
-                const int st = j % C::kStages, use = j / C::kStages;
-                if (use > 0 && !mbar_wait(smem_addr(&bars->st_empty[st]), (use - 1) & 1, abort_flag,
-                                          p.timeout_cycles, p.status))
-                    break;
-                const uint32_t fb = smem_addr(&bars->st_full[st]);
-                mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
-                const int row = seq_start + (kt_first + j) * kBlockN;
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d_hint(smem_addr(sK + st * C::kTileBytes + c * C::kChunkBytes), &p.tm_k,
-                                     fb, c * 64, g, row, keep);
-                    tma_load_3d_hint(smem_addr(sV + st * C::kTileBytes + c * C::kChunkBytes), &p.tm_v,
-                                     fb, c * 64, g, row, keep);
-                }
-                issued = j + 1;
-            }
-            if (*abort_flag) {
-                mbar_wait_drain(rb, 0, p.timeout_cycles);
-                for (int j = max(0, issued - C::kStages); j < issued; ++j)
-                    mbar_wait_drain(smem_addr(&bars->st_full[j % C::kStages]), (j / C::kStages) & 1,
-                                    p.timeout_cycles);
-            }
+            stream_tiles<D>(bars, sSlots, 2 * nk, &p.tm_k, &p.tm_v,
+                            [&](int i, int& head, int& row) {
+                                head = g;
+                                row = seq_start + (kt_first + i / 2) * kBlockN;
+                            },
+                            abort_flag, p);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(smem_addr(&bars->res_full), 0, abort_flag, p.timeout_cycles, p.status);
+            auto wait = [&](uint64_t& bar, int parity) {
+                return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
+            };
+            auto slot = [&](int i) { return smem_addr(sSlots + (i % C::kSlots) * C::kTileBytes); };
+            auto wait_slot = [&](int i) { return wait(bars->slot_full[i % C::kSlots], (i / C::kSlots) & 1); };
+            auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[i % C::kSlots])); };
             const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO);
-            for (int j = 0; ok && j < nk; ++j) {
-                const int st = j % C::kStages;
-                if (!(ok = mbar_wait(smem_addr(&bars->st_full[st]), (j / C::kStages) & 1, abort_flag,
-                                     p.timeout_cycles, p.status)))
-                    break;
+            bool ok = wait(bars->res_full, 0) && wait_slot(0);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t aK = smem_addr(sK + st * C::kTileBytes);
-                const uint32_t aV = smem_addr(sV + st * C::kTileBytes);
-                issue_ss<D>(tmem + C::kColS, aQ, aK);     // S = Q K^T
-                issue_ss<D>(tmem + C::kColDP, aDO, aV);   // dP = dO V^T
+                issue_ss<D>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
                 mma_commit(smem_addr(&bars->s_full));
-                if (!(ok = mbar_wait(smem_addr(&bars->ds_full), j & 1, abort_flag, p.timeout_cycles,
-                                     p.status)))
-                    break;
+                ok = wait_slot(1);
+            }
+            if (ok) {
                 tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColS, aK, j > 0);   // dQ += dS K
-                mma_commit(smem_addr(&bars->st_empty[st]));
+                issue_ss<D>(tmem + C::kColDP, aDO, slot(1));     // dP_0 = dO V_0^T
+                mma_commit(smem_addr(&bars->dp_full));
+                free_slot(1);
+            }
+            for (int j = 0; ok && j < nk; ++j) {
+                const bool more = j + 1 < nk;
+                if (more) {
+                    if (!(ok = wait(bars->p_full, j & 1))) break;     // S_j is in registers
+                    if (!(ok = wait_slot(2 * j + 2))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::kColS, aQ, slot(2 * j + 2));
+                    mma_commit(smem_addr(&bars->s_full));
+                }
+                if (!(ok = wait(bars->ds_full, j & 1))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColDP, slot(2 * j), j > 0);   // dQ += dS K
+                free_slot(2 * j);
+                if (more) {
+                    if (!(ok = wait_slot(2 * j + 3))) break;
+                    tc_fence_after();
+                    issue_ss<D>(tmem + C::kColDP, aDO, slot(2 * j + 3));
+                    mma_commit(smem_addr(&bars->dp_full));
+                    free_slot(2 * j + 3);
+                }
             }
             mma_commit(smem_addr(&bars->acc_full));
         }
     } else if (warp >= 4) {
+        const int wg = (warp - 4) / 4;      // key columns [64 wg, 64 wg + 64) of each tile
         const int quad = warp % 4;
-        const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
+        const int r = quad * 32 + lane;     // query row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + C::kColS + 64 * wg;
+        const uint32_t tDP = tmem + lane_addr + C::kColDP + 64 * wg;
         const int q = q0 + r;
         const bool valid = q < len;
         float lse2 = kPosInf, dlt = 0.f;
         if (valid) {
             const long long idx = row_stat_index(s, b, h, seq_start, q);
             lse2 = __ldg(p.lse + idx) * kLog2eF;
-            dlt = p.delta[idx];
+            dlt = __ldg(p.delta + idx);
         }
         const int lo_q = key_lo(s, q), hi_q = valid ? key_hi(s, q, len) : -1;
-        const int full_lo = key_lo(s, q0 + kBlockM - 1);
-        const int full_hi = key_hi(s, q0, len);
         const float sl2 = p.scale_log2;
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full), j & 1, abort_flag,
-                                                   p.timeout_cycles, p.status));
-            if (!ok) break;  // warp-uniform: the TMEM accesses below are warp-collective
+            const int kc = (kt_first + j) * kBlockN + 64 * wg;   // first key of my columns
+            const bool need_mask = !(kc >= lo_q && kc + 63 <= hi_q);
+            const int clo = lo_q - kc, chi = hi_q - kc;
+            if (!(ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles,
+                                 p.status)))
+                break;
             tc_fence_after();
-            const int kb = (kt_first + j) * kBlockN;
-            const bool need_mask = !(kb >= full_lo && kb + kBlockN - 1 <= full_hi) || !valid;
-            const int clo = lo_q - kb, chi = hi_q - kb;
+            float pv[64];
+            tmem_ld64(tS, pv);
+            tc_fence_before();
+            mbar_arrive(smem_addr(&bars->p_full));   // S_j consumed: the next S may be issued
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_addr + C::kColS + c * 32, sr);
-                tmem_ld32(tmem + lane_addr + C::kColDP + c * 32, dr);
-                tmem_ld_wait();
-                reg_fence(sr);
-                reg_fence(dr);
-                uint32_t dw[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float ds[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * i + e;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), sl2, -lse2));
-                        if (need_mask && (col < clo || col > chi)) pe = 0.f;
-                        ds[e] = pe * (__uint_as_float(dr[2 * i + e]) - dlt);
-                    }
-                    dw[i] = pack_bf16x2(ds[0], ds[1]);
-                }
-                tmem_st16(tmem + lane_addr + C::kColS + c * 16, dw);
+            for (int c = 0; c < 64; ++c) {
+                float pe = ex2_approx(fmaf(pv[c], sl2, -lse2));
+                if (need_mask && (c < clo || c > chi)) pe = 0.f;
+                pv[c] = pe;
             }
+            if (!(ok = warp_wait(smem_addr(&bars->dp_full), j & 1, abort_flag, p.timeout_cycles,
+                                 p.status)))
+                break;
+            tc_fence_after();
+            float dp[64];
+            tmem_ld64(tDP, dp);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) dp[c] = pv[c] * (dp[c] - dlt);
+            tmem_st_bf16x64(tDP, dp);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_addr(&bars->ds_full));
         }
         if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->acc_full), 0, abort_flag,
-                                                   p.timeout_cycles, p.status));
-        if (ok) {
+            ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
+        if (ok && wg == 0) {
             tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
             store_acc_row<D>(tmem + lane_addr + C::kColAcc, p.scale,
@@ -529,7 +643,7 @@ template <typename K>
 cudaError_t launch_tc(K kern, int grid, int smem, const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 256, smem, stream>>>(p);
+    kern<<<grid, 384, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -20,8 +20,9 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 __device__ __forceinline__ bool elect_lane0() { return lane_id() == 0; }
 
 // Device-wide status word, written (never read) by kernels when a bounded wait
-// gives up.  Host code reads it with fa_device_status().
-enum : int { kDevOk = 0, kDevTimeout = 5 };
+// gives up (kDevTimeout) or a launch finds its shared memory misaligned
+// (kDevBadSmem).  Host code reads it with fa_device_status().
+enum : int { kDevOk = 0, kDevTimeout = 5, kDevBadSmem = 6 };
 
 // ---------------------------------------------------------------- mbarrier
 

@@ -45,63 +45,39 @@ __device__ __forceinline__ long long row_stat_index(const SeqInfo& s, int b, int
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Number of work items of "level" below V: sum_b min(nblk_b, V), where
-// nblk_b = ceil(len_b / rows).
-__device__ __forceinline__ int items_below_level(const SeqInfo& s, int rows, int V) {
-    int c = 0;
-    for (int b = 0; b < s.B; ++b) {
-        int st, len;
-        seq_bounds(s, b, st, len);
-        c += min(ceil_div(len, rows), V);
-    }
-    return c;
-}
-
 // Maps CTA index w to (sequence b, head h, block index blk of `rows` rows).
-// Heads vary fastest.  Blocks are ordered by level: level 0 holds the most
-// expensive block of every sequence, level 1 the next, and so on, so the
-// heaviest work items start first.  `from_end` selects whether the most
-// expensive block of a sequence is its last (query blocks under a causal
-// mask) or its first (key blocks under a causal mask).  Returns false for
-// CTAs beyond the real work (packed batches launch an upper bound).
+// The work items of one (sequence, head) are consecutive, so the CTAs in
+// flight at any moment touch few heads and the tiles they share stay in L2;
+// within a (sequence, head) the most expensive block comes first: its last
+// block for query blocks under a causal mask (`from_end`), its first for key
+// blocks.  Returns false for CTAs beyond the real work (packed batches launch
+// an upper bound).
 __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int heads,
                                          bool from_end, int& b, int& h, int& blk) {
-    h = w % heads;
-    int r = w / heads;
     if (!s.cu_seqlens) {
-        int nblk = ceil_div(s.N, rows);
-        if (r >= nblk * s.B) return false;
-        b = r % s.B;
-        int v = r / s.B;
-        blk = from_end ? nblk - 1 - v : v;
+        const int nblk = ceil_div(s.N, rows);
+        if (w >= nblk * heads * s.B) return false;
+        const int t = w % nblk, bh = w / nblk;
+        h = bh % heads;
+        b = bh / heads;
+        blk = from_end ? nblk - 1 - t : t;
         return true;
     }
-    const int max_level = ceil_div(s.N, rows);
-    if (r >= items_below_level(s, rows, max_level)) return false;
-    // largest v with items_below_level(v) <= r
-    int lo = 0, hi = max_level;  // invariant: below(lo) <= r < below(hi)
-    while (hi - lo > 1) {
-        int mid = (lo + hi) / 2;
-        if (items_below_level(s, rows, mid) <= r) lo = mid;
-        else hi = mid;
-    }
-    const int v = lo;
-    int idx = r - items_below_level(s, rows, v);
+    int base = 0;
     for (b = 0; b < s.B; ++b) {
         int st, len;
         seq_bounds(s, b, st, len);
-        int n = ceil_div(len, rows);
-        if (n > v) {
-            if (idx == 0) break;
-            --idx;
+        const int n = ceil_div(len, rows);
+        if (w < base + n * heads) {
+            const int r = w - base;
+            h = r / n;
+            const int t = r % n;
+            blk = from_end ? n - 1 - t : t;
+            return true;
         }
+        base += n * heads;
     }
-    if (b >= s.B) return false;
-    int st, len;
-    seq_bounds(s, b, st, len);
-    int n = ceil_div(len, rows);
-    blk = from_end ? n - 1 - v : v;
-    return true;
+    return false;
 }
 
 }  // namespace fa
