@@ -45,39 +45,52 @@ __device__ __forceinline__ long long row_stat_index(const SeqInfo& s, int b, int
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Heads per scheduling chunk (see map_work).
+constexpr int kHeadChunk = 8;
+
 // Maps CTA index w to (sequence b, head h, block index blk of `rows` rows).
-// The work items of one (sequence, head) are consecutive, so the CTAs in
-// flight at any moment touch few heads and the tiles they share stay in L2;
-// within a (sequence, head) the most expensive block comes first: its last
-// block for query blocks under a causal mask (`from_end`), its first for key
-// blocks.  Returns false for CTAs beyond the real work (packed batches launch
-// an upper bound).
+// Heads are taken in chunks of kHeadChunk: all work items of a chunk are
+// launched before the next chunk's, so the CTAs in flight touch few heads and
+// the tiles they share stay in L2.  Within a chunk the order is by "level":
+// level 0 is the most expensive block of every head of the chunk, level 1 the
+// next, and so on (longest first); the most expensive block is the last one
+// for query blocks under a causal mask (`from_end`), the first for key blocks.
+// Returns false for CTAs beyond the real work (packed batches launch an upper
+// bound).
 __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int heads,
                                          bool from_end, int& b, int& h, int& blk) {
+    int n, first_bh, nbh, r;   // blocks per head, first (seq, head) pair of the range, pairs, index
     if (!s.cu_seqlens) {
-        const int nblk = ceil_div(s.N, rows);
-        if (w >= nblk * heads * s.B) return false;
-        const int t = w % nblk, bh = w / nblk;
-        h = bh % heads;
-        b = bh / heads;
-        blk = from_end ? nblk - 1 - t : t;
-        return true;
-    }
-    int base = 0;
-    for (b = 0; b < s.B; ++b) {
-        int st, len;
-        seq_bounds(s, b, st, len);
-        const int n = ceil_div(len, rows);
-        if (w < base + n * heads) {
-            const int r = w - base;
-            h = r / n;
-            const int t = r % n;
-            blk = from_end ? n - 1 - t : t;
-            return true;
+        n = ceil_div(s.N, rows);
+        const int pairs = s.B * heads;
+        if (w >= n * pairs) return false;
+        const int chunk = w / (n * kHeadChunk);
+        first_bh = chunk * kHeadChunk;
+        nbh = min(kHeadChunk, pairs - first_bh);
+        r = w - first_bh * n;
+    } else {
+        // sequences in order; within a sequence its heads in chunks
+        int base = 0;
+        for (b = 0; b < s.B; ++b) {
+            int st, len;
+            seq_bounds(s, b, st, len);
+            n = ceil_div(len, rows);
+            if (w < base + n * heads) break;
+            base += n * heads;
         }
-        base += n * heads;
+        if (b >= s.B) return false;
+        const int idx = w - base;
+        const int chunk = idx / (n * kHeadChunk);
+        first_bh = b * heads + chunk * kHeadChunk;
+        nbh = min(kHeadChunk, heads - chunk * kHeadChunk);
+        r = idx - chunk * kHeadChunk * n;
     }
-    return false;
+    const int level = r / nbh;
+    const int bh = first_bh + r % nbh;
+    b = bh / heads;
+    h = bh % heads;
+    blk = from_end ? n - 1 - level : level;
+    return true;
 }
 
 }  // namespace fa
