@@ -89,6 +89,7 @@ struct BwdCfg {
     static constexpr int kColS = 0;          // S (or S^T), 128 fp32 columns
     static constexpr int kColDP = 128;       // dP (or dP^T), 128 fp32 columns
     static constexpr int kColAcc = 256;      // accumulators: dQ, or dV then dK (D each)
+    static constexpr int kColDP1 = 384;      // dQ kernel only: second dP buffer
     // [barriers 256 B][row statistics: 2 warpgroups x 2 buffers x 128 fp32][pad] then
     // tiles: resident pair (K,V or Q,dO) followed by the slot ring
     static constexpr int kBarBytes = 256;
@@ -105,9 +106,9 @@ static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
 struct BwdBars {
     uint64_t res_full;        // resident pair landed
     uint64_t s_full;          // S (S^T) tile computed
-    uint64_t dp_full;         // dP (dP^T) tile computed
+    uint64_t dp_full[2];      // dP (dP^T) tile computed, per dP buffer
     uint64_t p_full;          // element-wise: S consumed (dK/dV: P^T written back)
-    uint64_t ds_full;         // element-wise: dS written back to TMEM
+    uint64_t ds_full[2];      // element-wise: dS written back to TMEM, per dP buffer
     uint64_t acc_full;        // all accumulation done
     uint64_t slot_full[8];    // streamed tile landed in slot
     uint64_t slot_empty[8];   // streamed tile consumed
@@ -206,9 +207,11 @@ __device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
         bars->abort = 0;
         mbar_init(smem_addr(&bars->res_full), 1);
         mbar_init(smem_addr(&bars->s_full), 1);
-        mbar_init(smem_addr(&bars->dp_full), 1);
         mbar_init(smem_addr(&bars->p_full), BwdCfg<D>::kEwThreads);
-        mbar_init(smem_addr(&bars->ds_full), BwdCfg<D>::kEwThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&bars->dp_full[i]), 1);
+            mbar_init(smem_addr(&bars->ds_full[i]), BwdCfg<D>::kEwThreads);
+        }
         mbar_init(smem_addr(&bars->acc_full), 1);
         for (int i = 0; i < BwdCfg<D>::kSlots; ++i) {
             mbar_init(smem_addr(&bars->slot_full[i]), 1);
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
             if (ok) {
                 tc_fence_after();
                 issue_ss<D>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
-                mma_commit(smem_addr(&bars->dp_full));
+                mma_commit(smem_addr(&bars->dp_full[0]));
             }
             for (int n = 0; ok && n < nsteps; ++n) {
                 const bool more = n + 1 < nsteps;
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
                     issue_ss<D>(tmem + C::kColS, aK, slot(2 * n + 2));                     // S^T_{n+1}
                     mma_commit(smem_addr(&bars->s_full));
                 }
-                if (!(ok = wait(bars->ds_full, n & 1))) break;
+                if (!(ok = wait(bars->ds_full[0], n & 1))) break;
                 tc_fence_after();
                 issue_ts<D>(tmem + C::kColAcc + D, tmem + C::kColDP, slot(2 * n), n > 0);  // dK += dS^T Q
                 free_slot(2 * n);
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
                     if (!(ok = wait_slot(2 * n + 3))) break;
                     tc_fence_after();
                     issue_ss<D>(tmem + C::kColDP, aV, slot(2 * n + 3));                    // dP^T_{n+1}
-                    mma_commit(smem_addr(&bars->dp_full));
+                    mma_commit(smem_addr(&bars->dp_full[0]));
                 }
             }
             mma_commit(smem_addr(&bars->acc_full));
@@ -397,15 +400,17 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
         const int qlo = query_lo(s, kpos);
         const int qhi = (kpos < len) ? query_hi(s, kpos, len) : -1;
         const float sl2 = p.scale_log2;
-        // Row statistics of step m for this warpgroup's 64 query columns: thread r
-        // fetches LSE (in log2 units) of column r (r < 64) or D of column r - 64;
-        // rows past the sequence end get +inf / 0 so they contribute nothing.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        // Row statistics of step m for this warpgroup's 64 query columns, negated:
+        // thread r fetches -LSE (in log2 units) of column r (r < 64) or -D of
+        // column r - 64; rows past the sequence end get -inf / 0 so they
+        // contribute nothing.
         auto fetch_stat = [&](int m) -> float {
             const int h = g * s.group + m / nq;
             const int q = (qt_first + m % nq) * kBlockM + 64 * wg + (r & 63);
-            if (q >= len) return r < 64 ? kPosInf : 0.f;
+            if (q >= len) return r < 64 ? -kPosInf : 0.f;
             const long long idx = row_stat_index(s, b, h, seq_start, q);
-            return r < 64 ? __ldg(p.lse + idx) * kLog2eF : __ldg(p.delta + idx);
+            return r < 64 ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
         };
         float next_stat = fetch_stat(0);
         bool ok = true;
@@ -421,8 +426,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
             if (!(ok = warp_wait(smem_addr(&bars->stat_full[wg][buf]), (n >> 1) & 1, abort_flag,
                                  p.timeout_cycles, p.status)))
                 break;
-            const float4* lse4 = reinterpret_cast<const float4*>(sb);
-            const float4* dlt4 = reinterpret_cast<const float4*>(sb + 64);
+            const float4* nlse4 = reinterpret_cast<const float4*>(sb);
+            const float4* ndlt4 = reinterpret_cast<const float4*>(sb + 64);
             // P^T = exp(S^T - LSE) (keys x queries), written back as bf16 in place
             if (!(ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles,
                                  p.status)))
@@ -432,38 +437,50 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
             tmem_ld64(tS, pv);
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
-                const float4 l = lse4[c4];
-                const float lv[4] = {l.x, l.y, l.z, l.w};
+                const float4 nl = nlse4[c4];
+                const float2 a = f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2x2,
+                                                  f2_pack(nl.x, nl.y)));
+                const float2 e = f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2,
+                                                  f2_pack(nl.z, nl.w)));
+                pv[4 * c4] = ex2_approx(a.x);
+                pv[4 * c4 + 1] = ex2_approx(a.y);
+                pv[4 * c4 + 2] = ex2_approx(e.x);
+                pv[4 * c4 + 3] = ex2_approx(e.y);
+            }
+            if (need_mask) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 4 * c4 + e;
-                    float pe = ex2_approx(fmaf(pv[c], sl2, -lv[e]));
-                    if (need_mask && (c < clo || c > chi)) pe = 0.f;
-                    pv[c] = pe;
-                }
+                for (int c = 0; c < 64; ++c)
+                    if (c < clo || c > chi) pv[c] = 0.f;
             }
             tmem_st_bf16x64(tS, pv);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_addr(&bars->p_full));
             // dS^T = P^T (dP^T - D), written back as bf16 in place
-            if (!(ok = warp_wait(smem_addr(&bars->dp_full), n & 1, abort_flag, p.timeout_cycles,
-                                 p.status)))
+            if (!(ok = warp_wait(smem_addr(&bars->dp_full[0]), n & 1, abort_flag,
+                                 p.timeout_cycles, p.status)))
                 break;
             tc_fence_after();
             float dp[64];
             tmem_ld64(tDP, dp);
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
-                const float4 dl = dlt4[c4];
-                const float dv4[4] = {dl.x, dl.y, dl.z, dl.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dp[4 * c4 + e] = pv[4 * c4 + e] * (dp[4 * c4 + e] - dv4[e]);
+                const float4 nd = ndlt4[c4];
+                const float2 a = f2_unpack(f2_mul(f2_pack(pv[4 * c4], pv[4 * c4 + 1]),
+                                                  f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]),
+                                                         f2_pack(nd.x, nd.y))));
+                const float2 e = f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
+                                                  f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]),
+                                                         f2_pack(nd.z, nd.w))));
+                dp[4 * c4] = a.x;
+                dp[4 * c4 + 1] = a.y;
+                dp[4 * c4 + 2] = e.x;
+                dp[4 * c4 + 3] = e.y;
             }
             tmem_st_bf16x64(tDP, dp);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_addr(&bars->ds_full));
+            mbar_arrive(smem_addr(&bars->ds_full[0]));
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
@@ -485,11 +502,15 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
 // ---------------------------------------------------------------------- dQ
 //
-// Per key tile j the issuer runs S_j, dP_j; as soon as the element-wise warps
-// have read S_j into registers it issues S_{j+1}; when dS_j is back in TMEM
-// (over dP_j) it issues dQ += dS_j K_j and then dP_{j+1}.  K_j and V_j stream
-// through the slot ring as items 2j and 2j+1; V_j's slot is released as soon
-// as dP_j is done, K_j's after dQ_j.
+// Per key tile j the issuer runs S_j and dP_j; as soon as the element-wise
+// warps have read S_j into registers it issues S_{j+1} and dP_{j+1} (dP
+// alternates between two TMEM buffers), and when dS_j is back in TMEM (over
+// dP_j) it issues dQ += dS_j K_j.  The tensor cores thus compute the next
+// tile's S and dP while the element-wise warps turn dP_j into dS_j.  K_j and
+// V_j stream through the slot ring as items 2j and 2j+1; V_j's slot is
+// released as soon as dP_j is done, K_j's after dQ_j.  dP_full / ds_full have
+// one barrier per dP buffer, so neither can run two phases ahead of its
+// waiter.
 
 template <int D>
 __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -541,6 +562,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
             auto slot = [&](int i) { return smem_addr(sSlots + (i % C::kSlots) * C::kTileBytes); };
             auto wait_slot = [&](int i) { return wait(bars->slot_full[i % C::kSlots], (i / C::kSlots) & 1); };
             auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[i % C::kSlots])); };
+            auto dp_col = [&](int j) { return tmem + ((j & 1) ? C::kColDP1 : C::kColDP); };
             const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO);
             bool ok = wait(bars->res_full, 0) && wait_slot(0);
             if (ok) {
@@ -551,30 +573,29 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
             }
             if (ok) {
                 tc_fence_after();
-                issue_ss<D>(tmem + C::kColDP, aDO, slot(1));     // dP_0 = dO V_0^T
-                mma_commit(smem_addr(&bars->dp_full));
+                issue_ss<D>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
+                mma_commit(smem_addr(&bars->dp_full[0]));
                 free_slot(1);
             }
             for (int j = 0; ok && j < nk; ++j) {
-                const bool more = j + 1 < nk;
-                if (more) {
-                    if (!(ok = wait(bars->p_full, j & 1))) break;     // S_j is in registers
+                if (j + 1 < nk) {
+                    // S_{j+1} once S_j is in registers; dP_{j+1} into the other buffer,
+                    // whose dS_{j-1} the already issued dQ_{j-1} reads first
+                    if (!(ok = wait(bars->p_full, j & 1))) break;
                     if (!(ok = wait_slot(2 * j + 2))) break;
                     tc_fence_after();
                     issue_ss<D>(tmem + C::kColS, aQ, slot(2 * j + 2));
                     mma_commit(smem_addr(&bars->s_full));
-                }
-                if (!(ok = wait(bars->ds_full, j & 1))) break;
-                tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColDP, slot(2 * j), j > 0);   // dQ += dS K
-                free_slot(2 * j);
-                if (more) {
                     if (!(ok = wait_slot(2 * j + 3))) break;
                     tc_fence_after();
-                    issue_ss<D>(tmem + C::kColDP, aDO, slot(2 * j + 3));
-                    mma_commit(smem_addr(&bars->dp_full));
+                    issue_ss<D>(dp_col(j + 1), aDO, slot(2 * j + 3));
+                    mma_commit(smem_addr(&bars->dp_full[(j + 1) & 1]));
                     free_slot(2 * j + 3);
                 }
+                if (!(ok = wait(bars->ds_full[j & 1], (j >> 1) & 1))) break;
+                tc_fence_after();
+                issue_ts<D>(tmem + C::kColAcc, dp_col(j), slot(2 * j), j > 0);   // dQ += dS K
+                free_slot(2 * j);
             }
             mma_commit(smem_addr(&bars->acc_full));
         }
@@ -584,7 +605,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
         const int r = quad * 32 + lane;     // query row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_addr + C::kColS + 64 * wg;
-        const uint32_t tDP = tmem + lane_addr + C::kColDP + 64 * wg;
+        const uint32_t tDP0 = tmem + lane_addr + C::kColDP + 64 * wg;
+        const uint32_t tDP1 = tmem + lane_addr + C::kColDP1 + 64 * wg;
         const int q = q0 + r;
         const bool valid = q < len;
         float lse2 = kPosInf, dlt = 0.f;
@@ -593,8 +615,9 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
             lse2 = __ldg(p.lse + idx) * kLog2eF;
             dlt = __ldg(p.delta + idx);
         }
+        const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndlt2 = f2_pack(-dlt, -dlt);
         const int lo_q = key_lo(s, q), hi_q = valid ? key_hi(s, q, len) : -1;
-        const float sl2 = p.scale_log2;
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
             const int kc = (kt_first + j) * kBlockN + 64 * wg;   // first key of my columns
@@ -609,23 +632,34 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
             tc_fence_before();
             mbar_arrive(smem_addr(&bars->p_full));   // S_j consumed: the next S may be issued
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float pe = ex2_approx(fmaf(pv[c], sl2, -lse2));
-                if (need_mask && (c < clo || c > chi)) pe = 0.f;
-                pv[c] = pe;
+            for (int i = 0; i < 32; ++i) {
+                const float2 a = f2_unpack(f2_fma(f2_pack(pv[2 * i], pv[2 * i + 1]), sl2x2, nlse2));
+                pv[2 * i] = ex2_approx(a.x);
+                pv[2 * i + 1] = ex2_approx(a.y);
             }
-            if (!(ok = warp_wait(smem_addr(&bars->dp_full), j & 1, abort_flag, p.timeout_cycles,
-                                 p.status)))
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < clo || c > chi) pv[c] = 0.f;
+            }
+            if (!(ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
+                                 p.timeout_cycles, p.status)))
                 break;
             tc_fence_after();
+            const uint32_t tDP = (j & 1) ? tDP1 : tDP0;
             float dp[64];
             tmem_ld64(tDP, dp);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) dp[c] = pv[c] * (dp[c] - dlt);
+            for (int i = 0; i < 32; ++i) {
+                const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]),
+                                                  f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2)));
+                dp[2 * i] = a.x;
+                dp[2 * i + 1] = a.y;
+            }
             tmem_st_bf16x64(tDP, dp);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_addr(&bars->ds_full));
+            mbar_arrive(smem_addr(&bars->ds_full[j & 1]));
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);

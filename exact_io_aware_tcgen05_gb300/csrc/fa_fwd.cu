@@ -267,18 +267,25 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 l *= alpha;
             }
             const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
-            float rs = 0.f;
-            uint32_t pk[kBlockN / 2];
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
+            uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+            // P (bf16 pairs) goes to the first 64 columns of S_t in two halves; every
+            // S value is already in registers, so the overwrite is safe.
 #pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, neg_ref));
-                const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, neg_ref));
-                rs += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int k = 64 * half + 2 * c;
+                    const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
+                    const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                    rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 32 * half, pk);
             }
-            l += rs;
-            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            const float2 rsum = f2_unpack(f2_add(rs2[0], rs2[1]));
+            l += rsum.x + rsum.y;
             if (__any_sync(0xffffffffu, rescale)) {
                 // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
                 // signalled; scale it in place before the next product accumulates.
