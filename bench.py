@@ -155,7 +155,7 @@ class ClockSampler:
 # ---------------------------------------------------------------- oracle
 
 def oracle_sample(w, x, target_s: float):
-    """Time the fp64 oracle (forward + backward) on a prefix of sequence 0 for the
+    """Time the fp64 oracle (forward, and backward if the workload has one) on a prefix of sequence 0 for the
     query heads of key/value head 0, growing the prefix until the run takes about
     target_s seconds.  Returns (TFLOP/s, threads, description, seconds, prefix length)."""
     import oracle
@@ -165,13 +165,15 @@ def oracle_sample(w, x, target_s: float):
     q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))
     k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), slice(0, 1))
     v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), slice(0, 1))
-    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))
+    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G)) if w.backward else None
 
     def run(L):
-        qg, dg = q[:L, :G].transpose(1, 0, 2), do[:L, :G].transpose(1, 0, 2)
+        qg = q[:L, :G].transpose(1, 0, 2)
         t0 = time.perf_counter()
         oracle.fwd_group(qg, k[:L, 0], v[:L, 0], w.causal, w.window, w.scale)
-        oracle.bwd_group(qg, k[:L, 0], v[:L, 0], dg, w.causal, w.window, w.scale)
+        if w.backward:
+            oracle.bwd_group(qg, k[:L, 0], v[:L, 0], do[:L, :G].transpose(1, 0, 2), w.causal,
+                             w.window, w.scale)
         return time.perf_counter() - t0
 
     L = min(256, L_full)
@@ -180,9 +182,9 @@ def oracle_sample(w, x, target_s: float):
         L_new = min(L_full, int(L * max(1.25, min(4.0, math.sqrt(target_s / max(t, 1e-3))))))
         L_new = max(L + 1, L_new)
         L, t = L_new, run(L_new)
-    flops = 14 * w.d * G * visible_pairs(L, w.causal, w.window)
+    flops = (14 if w.backward else 4) * w.d * G * visible_pairs(L, w.causal, w.window)
     desc = (f"sequence 0, first {L} of {L_full} tokens, query heads 0..{G - 1} (key/value head 0), "
-            f"forward + backward in fp64")
+            f"{'forward + backward' if w.backward else 'forward'} in fp64")
     return flops / t / 1e12, oracle.threads(), desc, t, L
 
 
@@ -192,24 +194,26 @@ def run_reference(args, w):
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    x = attention_inputs(w.q_shape, w.kv_shape, args.seed)
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=w.backward)
     total = args.steps + args.warmup
     per_step = min(10.0, max(0.3, 120.0 / max(total, 1)))   # whole run within a few minutes
     _, threads, desc, _, L = oracle_sample(w, x, per_step)
     import oracle
     G = w.Hq // w.Hkv
     q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
-    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
+    do = (oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
+          if w.backward else None)
     k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), 0)[:L]
     v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), 0)[:L]
     times = []
     for i in range(total):
         t0 = time.perf_counter()
         oracle.fwd_group(q, k, v, w.causal, w.window, w.scale)
-        oracle.bwd_group(q, k, v, do, w.causal, w.window, w.scale)
+        if w.backward:
+            oracle.bwd_group(q, k, v, do, w.causal, w.window, w.scale)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    flops = 14 * w.d * G * visible_pairs(L, w.causal, w.window)
+    flops = (14 if w.backward else 4) * w.d * G * visible_pairs(L, w.causal, w.window)
     ms = 1e3 * sum(times) / len(times)
     value = flops / (ms / 1e3) / 1e12
     line = {
@@ -251,12 +255,13 @@ def run_ours(args, w):
     import exact_io_aware_tcgen05_gb300 as fa
     fa.load()
 
-    x = attention_inputs(w.q_shape, w.kv_shape, args.seed)
+    bwd = w.backward          # forward-only workloads time fa_fwd alone
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=bwd)
 
     def pinned(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
 
-    h_in = {n: pinned(x[n]) for n in ("q", "k", "v", "dout")}
+    h_in = {n: pinned(x[n]) for n in (("q", "k", "v", "dout") if bwd else ("q", "k", "v"))}
     d_in = {n: t.to(dev) for n, t in h_in.items()}
     cu = None if not w.packed else torch.from_numpy(w.cu_seqlens()).to(dev)
     T = w.total_tokens if w.packed else 0
@@ -274,6 +279,8 @@ def run_ours(args, w):
         if ev_f is not None:
             fa.fa_set_launch_events(ev_f)
         fa.fa_fwd(d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
+        if not bwd:
+            return
         if ev_b is not None:
             fa.fa_set_launch_events(ev_b)
         fa.fa_bwd(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk, dv, *geo, ws,
@@ -292,8 +299,8 @@ def run_ours(args, w):
 
     K = args.steps
     ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for e in sum(ev_f, []) + sum(ev_b, []):
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)] if bwd else [None] * K
+    for e in sum(ev_f, []) + (sum(ev_b, []) if bwd else []):
         e.record(stream)      # instantiate the CUDA events
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)] if flush else None
@@ -329,28 +336,25 @@ def run_ours(args, w):
         elapsed = sum(a.elapsed_time(b) for a, b in step_ev)
     else:
         elapsed = t_start.elapsed_time(t_end)
-    kern_ms = {
-        "fa_fwd": [a.elapsed_time(b) for a, b in ev_f],
-        "fa_bwd_preprocess": [e[0].elapsed_time(e[1]) for e in ev_b],
-        "fa_bwd_dkdv": [e[1].elapsed_time(e[2]) for e in ev_b],
-        "fa_bwd_dq": [e[2].elapsed_time(e[3]) for e in ev_b],
-    }
+    kern_ms = {"fa_fwd": [a.elapsed_time(b) for a, b in ev_f]}
+    if bwd:
+        kern_ms["fa_bwd_preprocess"] = [e[0].elapsed_time(e[1]) for e in ev_b]
+        kern_ms["fa_bwd_dkdv"] = [e[1].elapsed_time(e[2]) for e in ev_b]
+        kern_ms["fa_bwd_dq"] = [e[2].elapsed_time(e[3]) for e in ev_b]
     if world > 1:
         t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed = float(t.item())
     ms_per_step = elapsed / K
-    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    fwd_flops, bwd_flops = w.fwd_flops(), (w.bwd_flops() if bwd else 0)
     value = world * (fwd_flops + bwd_flops) / (ms_per_step / 1e3) / 1e12
 
     # ---- end to end through the C ABI with host buffers
     E = max(1, args.e2e_steps)
-    h_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-             "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
-             "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
-             "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
-             "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
-    d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    d_out = {"o": o, "lse": lse}
+    if bwd:
+        d_out.update(dq=dq, dk=dk, dv=dv)
+    h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d_out.items()}
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,6 +390,9 @@ def run_ours(args, w):
             fl = KERNEL_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
             entry["algorithmic_tflop_per_launch"] = fl / 1e12
             entry["tflops"] = fl / (mean / 1e3) / 1e12
+            if name == "fa_fwd":
+                entry["algorithmic_bytes_per_launch"] = w.fwd_io_bytes()
+                entry["gbs"] = w.fwd_io_bytes() / (mean / 1e3) / 1e9
         else:
             by = 2 * w.total_tokens * w.Hq * w.d * 2 + 4 * w.total_tokens * w.Hq
             entry["algorithmic_bytes_per_launch"] = by
@@ -400,8 +407,10 @@ def run_ours(args, w):
             "peak_source": f"{peak_src} bf16_tflops (burst)" + (" of measured" if peak_src == "measured" else " of fallback"),
             "traffic": recorded_traffic(dom, w.name)}
     fwd_tf = fwd_flops / (kernels["fa_fwd"]["ms_mean"] / 1e3) / 1e12
-    bwd_ms = sum(kernels[n]["ms_mean"] for n in ("fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq"))
-    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
+    bwd_tf = None
+    if bwd:
+        bwd_ms = sum(kernels[n]["ms_mean"] for n in ("fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq"))
+        bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -417,11 +426,11 @@ def run_ours(args, w):
             "config": workload_config(w, l2_note),
             "pct_of_peak": value / world / peak_tf,
             "fwd_tflops": fwd_tf, "fwd_pct_of_peak": fwd_tf / peak_tf,
-            "bwd_tflops": bwd_tf, "bwd_pct_of_peak": bwd_tf / peak_tf,
+            "bwd_tflops": bwd_tf, "bwd_pct_of_peak": (bwd_tf / peak_tf) if bwd else None,
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E},
-            "gpu_launches": world * K * 4, "clocks": clocks,
+            "gpu_launches": world * K * (4 if bwd else 1), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -431,8 +440,6 @@ def run_ours(args, w):
 def main():
     args = parse_args()
     w = WORKLOADS[args.workload]
-    if not w.backward:
-        raise SystemExit(f"{w.name} is a forward-only parity case; bench steps run fwd + bwd")
     if args.impl == "reference":
         run_reference(args, w)
     else:
