@@ -73,6 +73,24 @@ def dist_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over all ranks of the default process group (identity
+    when there is none or it has one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput of `world` replicas, each doing flops_per_rank_step per step,
+    when the slowest rank takes ms_per_step per step."""
+    return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -341,13 +359,10 @@ def run_ours(args, w):
         kern_ms["fa_bwd_preprocess"] = [e[0].elapsed_time(e[1]) for e in ev_b]
         kern_ms["fa_bwd_dkdv"] = [e[1].elapsed_time(e[2]) for e in ev_b]
         kern_ms["fa_bwd_dq"] = [e[2].elapsed_time(e[3]) for e in ev_b]
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dev)
     ms_per_step = elapsed / K
     fwd_flops, bwd_flops = w.fwd_flops(), (w.bwd_flops() if bwd else 0)
-    value = world * (fwd_flops + bwd_flops) / (ms_per_step / 1e3) / 1e12
+    value = job_tflops(fwd_flops + bwd_flops, world, ms_per_step)
 
     # ---- end to end through the C ABI with host buffers
     E = max(1, args.e2e_steps)
@@ -371,12 +386,8 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     fa.fa_device_status(s)
-    e2e_ms = e0.elapsed_time(e1) / E
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * (fwd_flops + bwd_flops) / (e2e_ms / 1e3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
+    e2e_value = job_tflops(fwd_flops + bwd_flops, world, e2e_ms)
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = measured_peaks()
