@@ -123,11 +123,12 @@ static_assert(BwdCfg<128>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<128>::kHe
 template <int D>
 __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a, uint32_t b) {
     using C = BwdCfg<D>;
+    // descriptor of the tile base; a k-step adds its byte offset >> 4
+    const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-        mma_ss(d_tmem, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), C::kIdescSS,
-               kk > 0);
+        const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+        mma_ss(d_tmem, ad + off, bd + off, C::kIdescSS, kk > 0);
     }
 }
 
@@ -138,11 +139,11 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a, uint32_t b
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uint32_t b, bool acc) {
     using C = BwdCfg<D>;
+    const uint64_t bd = sdesc_sw128(b, C::kChunkBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_ts(d_tmem, a_region + (kk / 4) * 64 + (kk % 4) * 8,
-               sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024), C::kIdescTS,
-               (acc || kk > 0) ? 1u : 0u);
+        mma_ts(d_tmem, a_region + (kk / 4) * 64 + (kk % 4) * 8, bd + ((kk * 2048) >> 4),
+               C::kIdescTS, (acc || kk > 0) ? 1u : 0u);
 }
 
 // TMEM accumulator row (D fp32 columns) * mul -> bf16 row in global memory.

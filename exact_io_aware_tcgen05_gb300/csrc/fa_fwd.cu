@@ -164,22 +164,22 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                                  p.timeout_cycles, p.status);
             };
             auto issue_qk = [&](int t, int st) {
-                const uint32_t qa = smem_addr(sQ + t * C::kTileBytes);
-                const uint32_t ka = smem_addr(sKV + st * C::kTileBytes);
+                // descriptor of the tile base; a k-step adds its byte offset >> 4
+                const uint64_t qd = sdesc_sw128(smem_addr(sQ + t * C::kTileBytes), 16, 1024);
+                const uint64_t kd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                    mma_ss(tmem + C::kColS + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), C::kIdescQK, kk > 0);
+                    const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+                    mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, C::kIdescQK, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, int st, bool acc) {
-                const uint32_t va = smem_addr(sKV + st * C::kTileBytes);
+                const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes),
+                                                C::kChunkBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
-                           sdesc_sw128(va + kk * 2048, C::kChunkBytes, 1024), C::kIdescPV,
-                           (acc || kk > 0) ? 1u : 0u);
+                           vd + ((kk * 2048) >> 4), C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
             };
             bool ok = mbar_wait(smem_addr(&bars->q_full), 0, abort_flag, p.timeout_cycles,
@@ -254,9 +254,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (int c = 0; c < kBlockN; ++c)
                     if (c < clo || c > chi) sv[c] = kNegInf;
             }
-            float mx = sv[0];
+            // row max as a tree (8 independent chains) to keep the latency short
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
+            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+            for (int c = 8; c < kBlockN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_blk = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
@@ -268,7 +273,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             }
             const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
             const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
-            uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+            uint64_t rs2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
+                               f2_pack(0.f, 0.f)};
             // P (bf16 pairs) goes to the first 64 columns of S_t in two halves; every
             // S value is already in registers, so the overwrite is safe.
 #pragma unroll
@@ -279,12 +285,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     const int k = 64 * half + 2 * c;
                     const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
                     const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-                    rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
+                    rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + 32 * half, pk);
             }
-            const float2 rsum = f2_unpack(f2_add(rs2[0], rs2[1]));
+            const float2 rsum = f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])));
             l += rsum.x + rsum.y;
             if (__any_sync(0xffffffffu, rescale)) {
                 // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
