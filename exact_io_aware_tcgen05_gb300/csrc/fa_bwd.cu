@@ -232,9 +232,9 @@ __device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
 }
 
 template <int D>
-__device__ __forceinline__ void teardown_bwd_cta(BwdBars* bars, int warp, long long limit) {
+__device__ __forceinline__ void teardown_bwd_cta(BwdBars* bars, int warp) {
     if (bars->abort && threadIdx.x == 32)
-        mbar_wait_drain(smem_addr(&bars->acc_full), 0, limit);  // no tcgen05 op left in flight
+        mbar_wait_drain(smem_addr(&bars->acc_full), 0, kDrainCycles);  // no tcgen05 op left in flight
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -276,10 +276,9 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
         issued = i + 1;
     }
     if (*abort_flag) {
-        mbar_wait_drain(smem_addr(&bars->res_full), 0, p.timeout_cycles);
+        mbar_wait_drain(smem_addr(&bars->res_full), 0, kDrainCycles);
         for (int i = max(0, issued - C::kSlots); i < issued; ++i)
-            mbar_wait_drain(smem_addr(&bars->slot_full[i % C::kSlots]), (i / C::kSlots) & 1,
-                            p.timeout_cycles);
+            mbar_wait_drain(smem_addr(&bars->slot_full[i % C::kSlots]), (i / C::kSlots) & 1, kDrainCycles);
     }
 }
 
@@ -498,7 +497,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
                                  reinterpret_cast<__nv_bfloat16*>(p.dk) + row, valid);
         }
     }
-    teardown_bwd_cta<D>(bars, warp, p.timeout_cycles);
+    teardown_bwd_cta<D>(bars, warp);
 }
 
 // ---------------------------------------------------------------------- dQ
@@ -671,7 +670,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
                              reinterpret_cast<__nv_bfloat16*>(p.dq) + row, valid);
         }
     }
-    teardown_bwd_cta<D>(bars, warp, p.timeout_cycles);
+    teardown_bwd_cta<D>(bars, warp);
 }
 
 template <typename K>

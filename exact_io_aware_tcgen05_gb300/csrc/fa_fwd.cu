@@ -148,10 +148,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA exits
-                mbar_wait_drain(qbar, 0, p.timeout_cycles);
+                mbar_wait_drain(qbar, 0, kDrainCycles);
                 for (int i = max(0, issued - C::kStages); i < issued; ++i)
                     mbar_wait_drain(smem_addr(&bars->kv_full[i % C::kStages]),
-                                    (i / C::kStages) & 1, p.timeout_cycles);
+                                    (i / C::kStages) & 1, kDrainCycles);
             }
         }
     } else if (warp == 1) {
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     // ------------------------------------------------------------ teardown
     if (*abort_flag && warp == 1 && lane == 0) {
         // o_full was committed last: once it fires no tcgen05 op still uses TMEM
-        mbar_wait_drain(smem_addr(&bars->o_full), 0, p.timeout_cycles);
+        mbar_wait_drain(smem_addr(&bars->o_full), 0, kDrainCycles);
     }
     tc_fence_before();
     __syncthreads();

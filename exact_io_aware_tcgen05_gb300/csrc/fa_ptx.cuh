@@ -76,8 +76,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Wait used only while tearing down after an abort: ignores the abort flag
-// and gives up silently after `limit` cycles.
+// Cycle budget of the teardown drains below (about 1 s): independent of the
+// configurable wait limit, so a short limit never lets a CTA exit while its
+// own copies or MMAs are still in flight.
+constexpr long long kDrainCycles = 2000000000LL;
+
+// Wait used only while tearing down: ignores the abort flag and gives up
+// silently after `limit` cycles.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
