@@ -146,12 +146,12 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uin
                C::kIdescTS, (acc || kk > 0) ? 1u : 0u);
 }
 
-// TMEM accumulator row (D fp32 columns) * mul -> bf16 row in global memory.
-template <int D>
+// NC fp32 columns of a TMEM accumulator row * mul -> bf16 in global memory.
+template <int NC>
 __device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, __nv_bfloat16* dst,
                                               bool valid) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < NC / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(t_acc + c * 32, r);
         tmem_ld_wait();
@@ -299,6 +299,9 @@ template <int D>
 __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the dQ kernel reads nothing this kernel writes: let it start on SMs this
+    // grid's last CTAs leave idle
+    grid_launch_dependents();
     if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
     int b, g, kblk;
@@ -516,6 +519,12 @@ template <int D>
 __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Launched as a programmatic dependent of the dK/dV kernel: it may start while
+    // that grid finishes.  Before exiting, every CTA waits for that grid, so the
+    // completion of this kernel still implies the completion of all earlier work.
+    struct WaitPrimaryOnExit {
+        __device__ ~WaitPrimaryOnExit() { grid_dependency_wait(); }
+    } wait_on_exit;
     if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
     int b, h, qblk;
@@ -663,11 +672,12 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
-        if (ok && wg == 0) {
+        if (ok) {
             tc_fence_after();
+            // each warpgroup stores D/2 columns of the dQ row (scaled)
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-            store_acc_row<D>(tmem + lane_addr + C::kColAcc, p.scale,
-                             reinterpret_cast<__nv_bfloat16*>(p.dq) + row, valid);
+            store_acc_row<D / 2>(tmem + lane_addr + C::kColAcc + (D / 2) * wg, p.scale,
+                                 reinterpret_cast<__nv_bfloat16*>(p.dq) + row + (D / 2) * wg, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -700,10 +710,29 @@ cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream) {
                     : launch_tc(fa_bwd_dkdv_kernel<64>, p.num_work_dkdv, BwdCfg<64>::kSmemBytes, p, stream);
 }
 
+// The dQ kernel is launched as a programmatic dependent of the dK/dV kernel
+// (see fa_bwd_dq_kernel).
+template <typename K>
+cudaError_t launch_dependent(K kern, int grid, int smem, const BwdParams& p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(384);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dq <= 0) return cudaSuccess;
-    return d == 128 ? launch_tc(fa_bwd_dq_kernel<128>, p.num_work_dq, BwdCfg<128>::kSmemBytes, p, stream)
-                    : launch_tc(fa_bwd_dq_kernel<64>, p.num_work_dq, BwdCfg<64>::kSmemBytes, p, stream);
+    return d == 128 ? launch_dependent(fa_bwd_dq_kernel<128>, p.num_work_dq, BwdCfg<128>::kSmemBytes, p, stream)
+                    : launch_dependent(fa_bwd_dq_kernel<64>, p.num_work_dq, BwdCfg<64>::kSmemBytes, p, stream);
 }
 
 }  // namespace fa

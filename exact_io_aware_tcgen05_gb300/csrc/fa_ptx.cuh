@@ -255,6 +255,20 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Lets grids launched as programmatic dependents of this grid start once every
+// CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until the grids this grid programmatically depends on have completed
+// and their memory operations are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (the
