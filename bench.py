@@ -7,7 +7,8 @@ inputs already resident in HBM).  Prints ONE JSON line on rank 0:
   value        algorithmic TFLOP/s of the whole job (forward 4*d, backward 10*d
                per visible (query, key) pair and query head; causal halves it)
   e2e          the same metric through the C ABI with pinned HOST buffers: each
-               step copies Q, K, V, dO in and O, LSE, dQ, dK, dV out
+               step copies Q, K, V, dO in and O, LSE, dQ, dK, dV out (two device
+               buffer sets; copies of neighbouring steps overlap the kernels)
   roofline     the dominant kernel (largest device time): algorithmic FLOPs per
                launch / its mean launch time, from a second timed region of K
                steps in which the library records CUDA events around each of
@@ -382,25 +383,53 @@ def run_ours(args, w):
     value = job_tflops(fwd_flops + bwd_flops, world, ms_per_step)
 
     # ---- end to end through the C ABI with host buffers
+    # Each step copies its inputs in from pinned host memory and its results out.
+    # Two sets of device buffers let step k+1's input copy and step k-1's output
+    # copy overlap step k's kernels (three streams, ordered by events).
     E = max(1, args.e2e_steps)
-    d_out = {"o": o, "lse": lse}
+    d_out0 = {"o": o, "lse": lse}
     if bwd:
-        d_out.update(dq=dq, dk=dk, dv=dv)
-    h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d_out.items()}
+        d_out0.update(dq=dq, dk=dk, dv=dv)
+    h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d_out0.items()}
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    d_ins = [d_in, {n: torch.empty_like(t) for n, t in d_in.items()}]
+    d_outs = [d_out0, {n: torch.empty_like(t) for n, t in d_out0.items()}]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+
+    def e2e_step(k):
+        b = k & 1
+        di, do_ = d_ins[b], d_outs[b]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev["comp"][b])          # step k-2 done reading di
+            for n in h_in:
+                di[n].copy_(h_in[n], non_blocking=True)
+            ev["in"][b].record(s_in)
+        stream.wait_event(ev["in"][b])
+        if k >= 2:
+            stream.wait_event(ev["out"][b])             # step k-2's results copied out
+        fa.fa_fwd(di["q"], di["k"], di["v"], do_["o"], do_["lse"], *geo, s)
+        if bwd:
+            fa.fa_bwd(di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dout"], do_["dq"],
+                      do_["dk"], do_["dv"], *geo, ws, ws_bytes, s)
+        ev["comp"][b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][b])
+            for n in h_out:
+                h_out[n].copy_(do_[n], non_blocking=True)
+            ev["out"][b].record(s_out)
+
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(E):
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        step()
-        for n in h_out:
-            h_out[n].copy_(d_out[n], non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    for k in range(E):
+        e2e_step(k)
+    s_out.wait_event(ev["comp"][(E - 1) & 1])
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     fa.fa_device_status(s)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
