@@ -23,8 +23,9 @@
 //                      over the key tiles; S and dP in TMEM, dS (bf16) back to
 //                      TMEM feeds dQ += dS K
 // Warp roles in both tensor-core kernels: warp 0 TMA producer, warp 1 tcgen05
-// issuer (one thread, owns TMEM), warps 4..11 element-wise work + epilogue as
-// two warpgroups, each owning 64 of the 128 tile columns (TMEM lane = row).
+// issuer (one thread, owns TMEM), warps 4.. element-wise work + epilogue as two
+// (d = 128) or four (d = 64) warpgroups, each owning 64 or 32 of the 128 tile
+// columns (TMEM lane = row).
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 #include "fa_seq.cuh"
@@ -83,16 +84,28 @@ struct BwdCfg {
     static constexpr int kTileBytes = kBlockM * D * 2;
     // ring of single-tile slots for the streamed operands (Q/dO, or K/V)
     static constexpr int kSlots = (D == 128) ? 5 : 8;
-    static constexpr int kThreads = 384;     // warp 0 TMA, warp 1 MMA, warps 4..11 element-wise
-    static constexpr int kEwThreads = 256;   // two warpgroups, 64 tile columns each
+    // The streamed items alternate between two rings of slots: even items (Q_n,
+    // K_j) are held from their first product to their last, about one and a half
+    // steps; odd items (dO_n, V_j) about half a step.  Separate rings give each
+    // kind a prefetch distance of its own.
+    static constexpr int kSlotsOdd = (D == 128) ? 2 : 3;
+    static constexpr int kSlotsEven = kSlots - kSlotsOdd;
+    // element-wise warpgroups, each owning kEwCols of the 128 tile columns: d = 64 has
+    // half the tensor work per tile of d = 128 and the same element-wise work, so it
+    // gets twice the element-wise warps
+    static constexpr int kEwWG = (D == 64) ? 4 : 2;
+    static constexpr int kEwCols = 128 / kEwWG;
+    static constexpr int kEwThreads = 128 * kEwWG;
+    static constexpr int kThreads = 128 + kEwThreads;   // warp 0 TMA, warp 1 MMA, warp 2 relay, warps 4.. element-wise
+    static constexpr int kBarCount = kEwThreads + 64;   // named barriers: element-wise + issuer + relay warps
     static constexpr int kTmemCols = 512;
     static constexpr int kColS = 0;          // S (or S^T), 128 fp32 columns
     static constexpr int kColDP = 128;       // dP (or dP^T), 128 fp32 columns
     static constexpr int kColAcc = 256;      // accumulators: dQ, or dV then dK (D each)
     static constexpr int kColDP1 = 384;      // dQ kernel only: second dP buffer
-    // [barriers 256 B][row statistics: 2 warpgroups x 2 buffers x 128 fp32][pad] then
+    // [barriers 512 B][row statistics: warpgroups x 2 buffers x 2 kEwCols fp32][pad] then
     // tiles: resident pair (K,V or Q,dO) followed by the slot ring
-    static constexpr int kBarBytes = 256;
+    static constexpr int kBarBytes = 512;
     static constexpr int kStatOffset = kBarBytes;
     static constexpr int kHeadBytes = 3072;
     static constexpr int kTilesBytes = (2 + kSlots) * kTileBytes;
@@ -103,21 +116,26 @@ struct BwdCfg {
 static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
 
+// named barrier ids (0 is __syncthreads): element-wise results (and streamed
+// tiles) ready for the issuer's next products
+constexpr int kBarP = 1;     // P (P^T) written / S read
+constexpr int kBarDS0 = 2;   // dS (dS^T) written; the dQ kernel alternates kBarDS0 / kBarDS1
+constexpr int kBarDS1 = 3;
+
 struct BwdBars {
     uint64_t res_full;        // resident pair landed
     uint64_t s_full;          // S (S^T) tile computed
     uint64_t dp_full[2];      // dP (dP^T) tile computed, per dP buffer
-    uint64_t p_full;          // element-wise: S consumed (dK/dV: P^T written back)
-    uint64_t ds_full[2];      // element-wise: dS written back to TMEM, per dP buffer
     uint64_t acc_full;        // all accumulation done
     uint64_t slot_full[8];    // streamed tile landed in slot
     uint64_t slot_empty[8];   // streamed tile consumed
-    uint64_t stat_full[2][2]; // dK/dV: row statistics of a step staged [warpgroup][buffer]
+    uint64_t stat_full[4][2]; // dK/dV: row statistics of a step staged [warpgroup][buffer]
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(BwdBars) <= BwdCfg<128>::kBarBytes, "barrier block");
 static_assert(BwdCfg<128>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<128>::kHeadBytes, "stats");
+static_assert(BwdCfg<64>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<64>::kHeadBytes, "stats");
 
 // a[rows: K-major 128 x D] . b[rows: K-major 128 x D]^T -> tmem (128 x 128 fp32)
 template <int D>
@@ -132,9 +150,9 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a, uint32_t b
     }
 }
 
-// A = bf16 operand written back to TMEM by the element-wise warpgroups: the 64
-// tile columns of warpgroup w sit, packed two per 32-bit column, in the first
-// 32 TMEM columns of that warpgroup's own 64-column range (region + 64 w).
+// A = bf16 operand written back to TMEM by the element-wise warpgroups: the W =
+// kEwCols tile columns of warpgroup w sit, packed two per 32-bit column, in the
+// first W/2 TMEM columns of that warpgroup's own range (region + W w).
 // D (128 x D fp32) (+)= A (128 x 128) . b[smem rows: 128 x D, MN-major].
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uint32_t b, bool acc) {
@@ -142,7 +160,8 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uin
     const uint64_t bd = sdesc_sw128(b, C::kChunkBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 16; ++kk)
-        mma_ts(d_tmem, a_region + (kk / 4) * 64 + (kk % 4) * 8, bd + ((kk * 2048) >> 4),
+        mma_ts(d_tmem, a_region + (16 * kk / C::kEwCols) * C::kEwCols + (16 * kk % C::kEwCols) / 2,
+               bd + ((kk * 2048) >> 4),
                C::kIdescTS, (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -168,27 +187,37 @@ __device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, __nv_bf
     }
 }
 
-// Loads this warpgroup's 64 fp32 columns of one TMEM row.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+// Loads this warpgroup's W (32 or 64) fp32 columns of one TMEM row.
+template <int W>
+__device__ __forceinline__ void tmem_ldw(uint32_t taddr, float (&v)[W]) {
     uint32_t a[32], b[32];
     tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
+    if (W == 64) tmem_ld32(taddr + 32, b);
     tmem_ld_wait();
     reg_fence(a);
-    reg_fence(b);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        v[i] = __uint_as_float(a[i]);
-        v[32 + i] = __uint_as_float(b[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a[i]);
+    if (W == 64) {
+        reg_fence(b);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[(32 + i) % W] = __uint_as_float(b[i]);
     }
 }
 
-// Packs 64 fp32 values to bf16 pairs and stores them in the first 32 columns at taddr.
-__device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const float (&v)[64]) {
-    uint32_t w[32];
+// Packs W fp32 values to bf16 pairs and stores them in the first W/2 columns at taddr.
+template <int W>
+__device__ __forceinline__ void tmem_st_bf16(uint32_t taddr, const float (&v)[W]) {
+    if (W == 64) {
+        uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-    tmem_st32(taddr, w);
+        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[(2 * i) % W], v[(2 * i + 1) % W]);
+        tmem_st32(taddr, w);
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        tmem_st16(taddr, w);
+    }
 }
 
 // Returns false (uniformly for the CTA) if the dynamic shared memory base is not
@@ -208,17 +237,15 @@ __device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
         bars->abort = 0;
         mbar_init(smem_addr(&bars->res_full), 1);
         mbar_init(smem_addr(&bars->s_full), 1);
-        mbar_init(smem_addr(&bars->p_full), BwdCfg<D>::kEwThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&bars->dp_full[i]), 1);
-            mbar_init(smem_addr(&bars->ds_full[i]), BwdCfg<D>::kEwThreads);
         }
         mbar_init(smem_addr(&bars->acc_full), 1);
         for (int i = 0; i < BwdCfg<D>::kSlots; ++i) {
             mbar_init(smem_addr(&bars->slot_full[i]), 1);
             mbar_init(smem_addr(&bars->slot_empty[i]), 1);
         }
-        for (int w = 0; w < 2; ++w)
+        for (int w = 0; w < BwdCfg<D>::kEwWG; ++w)
             for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&bars->stat_full[w][i]), kBlockM);
         fence_barrier_init();
     }
@@ -243,6 +270,21 @@ __device__ __forceinline__ void teardown_bwd_cta(BwdBars* bars, int warp) {
     }
 }
 
+// Slot ring of streamed item i: physical slot, and use count of that slot.
+template <int D>
+__device__ __forceinline__ int slot_index(int i) {
+    using C = BwdCfg<D>;
+    const int k = i >> 1;
+    return (i & 1) ? C::kSlotsEven + k % C::kSlotsOdd : k % C::kSlotsEven;
+}
+
+template <int D>
+__device__ __forceinline__ int slot_use(int i) {
+    using C = BwdCfg<D>;
+    const int k = i >> 1;
+    return (i & 1) ? k / C::kSlotsOdd : k / C::kSlotsEven;
+}
+
 // Warp-uniform bounded wait (the TMEM accesses that follow are warp-collective).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           long long limit, int* status) {
@@ -261,7 +303,7 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
     const uint64_t keep = make_l2_policy_evict_last();
     int issued = 0;
     for (int i = 0; i < items; ++i) {
-        const int sl = i % C::kSlots, use = i / C::kSlots;
+        const int sl = slot_index<D>(i), use = slot_use<D>(i);
         if (use > 0 && !mbar_wait(smem_addr(&bars->slot_empty[sl]), (use - 1) & 1, abort_flag,
                                   p.timeout_cycles, p.status))
             break;
@@ -277,8 +319,14 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
     }
     if (*abort_flag) {
         mbar_wait_drain(smem_addr(&bars->res_full), 0, kDrainCycles);
-        for (int i = max(0, issued - C::kSlots); i < issued; ++i)
-            mbar_wait_drain(smem_addr(&bars->slot_full[i % C::kSlots]), (i / C::kSlots) & 1, kDrainCycles);
+        // the last item issued into each slot
+        unsigned seen = 0;
+        for (int i = issued - 1; i >= 0 && i >= issued - 2 * C::kSlots; --i) {
+            const int sl = slot_index<D>(i);
+            if (seen & (1u << sl)) continue;
+            seen |= 1u << sl;
+            mbar_wait_drain(smem_addr(&bars->slot_full[sl]), slot_use<D>(i) & 1, kDrainCycles);
+        }
     }
 }
 
@@ -294,9 +342,16 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
 // one thread execute in issue order).  Q_n and dO_n stream through the slot
 // ring as items 2n and 2n+1; the element-wise warps fetch the row statistics
 // (LSE, D) of step n+1 from global memory while they work on step n.
+//
+// Synchronisation: the issuer learns of the element-wise results (and, through
+// a relay warp that waits on the slot mbarriers, of the streamed tiles) from
+// two named barriers, kBarP and kBarDS0, one phase each per step; the
+// element-wise warps learn of finished products from tcgen05.commit mbarriers.
+// Each signal that would open phase n+1 of a named barrier depends on a product
+// issued after phase n completed, so no participant gets a phase ahead.
 
 template <int D>
-__global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the dQ kernel reads nothing this kernel writes: let it start on SMs this
@@ -316,7 +371,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const int nsteps = s.group * nq;
 
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
-    float* sStat = reinterpret_cast<float*>(smem_raw + C::kStatOffset);   // [wg][buf][128]
+    float* sStat = reinterpret_cast<float*>(smem_raw + C::kStatOffset);   // [wg][buf][2 W]
     uint8_t* sK = smem_raw + C::kHeadBytes;
     uint8_t* sV = sK + C::kTileBytes;
     uint8_t* sSlots = sV + C::kTileBytes;
@@ -345,159 +400,185 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        // The whole warp walks the step sequence (the named barriers are
+        // warp-collective); lane 0 issues.  It never waits on an mbarrier inside
+        // the loop and does not look at the abort flag: after an abort it keeps
+        // issuing (on stale data) so that every barrier phase still completes.
+        auto slot = [&](int i) { return smem_addr(sSlots + slot_index<D>(i) * C::kTileBytes); };
+        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[slot_index<D>(i)])); };
+        const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
         if (lane == 0) {
             auto wait = [&](uint64_t& bar, int parity) {
                 return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
             };
-            auto slot = [&](int i) { return smem_addr(sSlots + (i % C::kSlots) * C::kTileBytes); };
-            auto wait_slot = [&](int i) { return wait(bars->slot_full[i % C::kSlots], (i / C::kSlots) & 1); };
-            auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[i % C::kSlots])); };
-            const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
-            bool ok = wait(bars->res_full, 0) && wait_slot(0);
-            if (ok) {
-                tc_fence_after();
-                issue_ss<D>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
-                mma_commit(smem_addr(&bars->s_full));
-                ok = wait_slot(1);
-            }
-            if (ok) {
-                tc_fence_after();
-                issue_ss<D>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
-                mma_commit(smem_addr(&bars->dp_full[0]));
-            }
-            for (int n = 0; ok && n < nsteps; ++n) {
-                const bool more = n + 1 < nsteps;
-                if (!(ok = wait(bars->p_full, n & 1))) break;
+            if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
+                wait(bars->slot_full[slot_index<D>(1)], 0)) {}
+            tc_fence_after();
+            issue_ss<D>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
+            mma_commit(smem_addr(&bars->s_full));
+            issue_ss<D>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
+            mma_commit(smem_addr(&bars->dp_full[0]));
+        }
+        __syncwarp();
+        for (int n = 0; n < nsteps; ++n) {
+            const bool more = n + 1 < nsteps;
+            named_bar_sync(kBarP, C::kBarCount);          // P^T_n written, Q_{n+1} landed
+            if (lane == 0) {
                 tc_fence_after();
                 issue_ts<D>(tmem + C::kColAcc, tmem + C::kColS, slot(2 * n + 1), n > 0);   // dV += P^T dO
                 free_slot(2 * n + 1);
                 if (more) {
-                    if (!(ok = wait_slot(2 * n + 2))) break;
-                    tc_fence_after();
                     issue_ss<D>(tmem + C::kColS, aK, slot(2 * n + 2));                     // S^T_{n+1}
                     mma_commit(smem_addr(&bars->s_full));
                 }
-                if (!(ok = wait(bars->ds_full[0], n & 1))) break;
+            }
+            __syncwarp();
+            named_bar_sync(kBarDS0, C::kBarCount);        // dS^T_n written, dO_{n+1} landed
+            if (lane == 0) {
                 tc_fence_after();
                 issue_ts<D>(tmem + C::kColAcc + D, tmem + C::kColDP, slot(2 * n), n > 0);  // dK += dS^T Q
                 free_slot(2 * n);
                 if (more) {
-                    if (!(ok = wait_slot(2 * n + 3))) break;
-                    tc_fence_after();
                     issue_ss<D>(tmem + C::kColDP, aV, slot(2 * n + 3));                    // dP^T_{n+1}
                     mma_commit(smem_addr(&bars->dp_full[0]));
                 }
             }
-            mma_commit(smem_addr(&bars->acc_full));
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(smem_addr(&bars->acc_full));
+    } else if (warp == 2) {
+        // ------------------------------------------------------ slot relay
+        // Waits for the streamed tiles the next products read and passes that on
+        // through the issuer's named barriers.
+        for (int n = 0; n < nsteps; ++n) {
+            const bool more = n + 1 < nsteps;
+            if (lane == 0 && more)
+                mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(2 * n + 2)]),
+                          slot_use<D>(2 * n + 2) & 1, abort_flag, p.timeout_cycles, p.status);
+            __syncwarp();
+            named_bar_sync(kBarP, C::kBarCount);
+            if (lane == 0 && more)
+                mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(2 * n + 3)]),
+                          slot_use<D>(2 * n + 3) & 1, abort_flag, p.timeout_cycles, p.status);
+            __syncwarp();
+            named_bar_sync(kBarDS0, C::kBarCount);
         }
     } else if (warp >= 4) {
         // ------------------------------------------- element-wise + epilogue
-        const int wg = (warp - 4) / 4;      // query columns [64 wg, 64 wg + 64) of each tile
+        constexpr int W = C::kEwCols;
+        const int wg = (warp - 4) / 4;      // query columns [W wg, W wg + W) of each tile
         const int quad = warp % 4;
         const int r = quad * 32 + lane;     // key row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + C::kColS + 64 * wg;
-        const uint32_t tDP = tmem + lane_addr + C::kColDP + 64 * wg;
+        const uint32_t tS = tmem + lane_addr + C::kColS + W * wg;
+        const uint32_t tDP = tmem + lane_addr + C::kColDP + W * wg;
         const int kpos = kb + r;
         // queries that see this key: [qlo, qhi]; none if the key is past the end
         const int qlo = query_lo(s, kpos);
         const int qhi = (kpos < len) ? query_hi(s, kpos, len) : -1;
         const float sl2 = p.scale_log2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        // Row statistics of step m for this warpgroup's 64 query columns, negated:
-        // thread r fetches -LSE (in log2 units) of column r (r < 64) or -D of
-        // column r - 64; rows past the sequence end get -inf / 0 so they
+        // Row statistics of step m for this warpgroup's W query columns, negated:
+        // thread r fetches -LSE (in log2 units) of column r (r < W) or -D of
+        // column r - W (r < 2W); rows past the sequence end get -inf / 0 so they
         // contribute nothing.
         auto fetch_stat = [&](int m) -> float {
+            if (r >= 2 * W) return 0.f;
             const int h = g * s.group + m / nq;
-            const int q = (qt_first + m % nq) * kBlockM + 64 * wg + (r & 63);
-            if (q >= len) return r < 64 ? -kPosInf : 0.f;
+            const int q = (qt_first + m % nq) * kBlockM + W * wg + (r % W);
+            if (q >= len) return r < W ? -kPosInf : 0.f;
             const long long idx = row_stat_index(s, b, h, seq_start, q);
-            return r < 64 ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
+            return r < W ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
         };
         float next_stat = fetch_stat(0);
+        // `ok` turns false (warp-uniformly) when a wait gives up; the warp then
+        // skips the work but keeps taking part in every named-barrier phase,
+        // blocking (bar.sync) instead of arriving so it cannot run a phase ahead.
         bool ok = true;
         for (int n = 0; n < nsteps; ++n) {
             const int buf = n & 1;
-            float* sb = sStat + (wg * 2 + buf) * kBlockM;
-            sb[r] = next_stat;
-            mbar_arrive(smem_addr(&bars->stat_full[wg][buf]));
-            if (n + 1 < nsteps) next_stat = fetch_stat(n + 1);   // in flight during this step
-            const int q0 = (qt_first + n % nq) * kBlockM + 64 * wg;   // first query of my columns
-            const bool need_mask = !(q0 >= qlo && q0 + 63 <= qhi);
+            float* sb = sStat + (wg * 2 + buf) * (2 * W);
+            const int q0 = (qt_first + n % nq) * kBlockM + W * wg;   // first query of my columns
+            const bool need_mask = !(q0 >= qlo && q0 + W - 1 <= qhi);
             const int clo = qlo - q0, chi = qhi - q0;
-            if (!(ok = warp_wait(smem_addr(&bars->stat_full[wg][buf]), (n >> 1) & 1, abort_flag,
-                                 p.timeout_cycles, p.status)))
-                break;
             const float4* nlse4 = reinterpret_cast<const float4*>(sb);
-            const float4* ndlt4 = reinterpret_cast<const float4*>(sb + 64);
+            const float4* ndlt4 = reinterpret_cast<const float4*>(sb + W);
+            if (ok) {
+                if (r < 2 * W) sb[r] = next_stat;
+                mbar_arrive(smem_addr(&bars->stat_full[wg][buf]));
+                if (n + 1 < nsteps) next_stat = fetch_stat(n + 1);   // in flight during this step
+                ok = warp_wait(smem_addr(&bars->stat_full[wg][buf]), (n >> 1) & 1, abort_flag,
+                               p.timeout_cycles, p.status);
+            }
             // P^T = exp(S^T - LSE) (keys x queries), written back as bf16 in place
-            if (!(ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles,
-                                 p.status)))
-                break;
-            tc_fence_after();
-            float pv[64];
-            tmem_ld64(tS, pv);
+            if (ok) ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles, p.status);
+            float pv[W];
+            if (ok) {
+                tc_fence_after();
+                tmem_ldw<W>(tS, pv);
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-                const float4 nl = nlse4[c4];
-                const float2 a = f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2x2,
-                                                  f2_pack(nl.x, nl.y)));
-                const float2 e = f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2,
-                                                  f2_pack(nl.z, nl.w)));
-                pv[4 * c4] = ex2_approx(a.x);
-                pv[4 * c4 + 1] = ex2_approx(a.y);
-                pv[4 * c4 + 2] = ex2_approx(e.x);
-                pv[4 * c4 + 3] = ex2_approx(e.y);
-            }
-            if (need_mask) {
+                for (int c4 = 0; c4 < W / 4; ++c4) {
+                    const float4 nl = nlse4[c4];
+                    const float2 a = f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2x2,
+                                                      f2_pack(nl.x, nl.y)));
+                    const float2 e = f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2,
+                                                      f2_pack(nl.z, nl.w)));
+                    pv[4 * c4] = ex2_approx(a.x);
+                    pv[4 * c4 + 1] = ex2_approx(a.y);
+                    pv[4 * c4 + 2] = ex2_approx(e.x);
+                    pv[4 * c4 + 3] = ex2_approx(e.y);
+                }
+                if (need_mask) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < clo || c > chi) pv[c] = 0.f;
+                    for (int c = 0; c < W; ++c)
+                        if (c < clo || c > chi) pv[c] = 0.f;
+                }
+                tmem_st_bf16<W>(tS, pv);
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tmem_st_bf16x64(tS, pv);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars->p_full));
+            named_bar_signal(kBarP, C::kBarCount, ok);
             // dS^T = P^T (dP^T - D), written back as bf16 in place
-            if (!(ok = warp_wait(smem_addr(&bars->dp_full[0]), n & 1, abort_flag,
-                                 p.timeout_cycles, p.status)))
-                break;
-            tc_fence_after();
-            float dp[64];
-            tmem_ld64(tDP, dp);
+            if (ok) ok = warp_wait(smem_addr(&bars->dp_full[0]), n & 1, abort_flag, p.timeout_cycles, p.status);
+            if (ok) {
+                tc_fence_after();
+                float dp[W];
+                tmem_ldw<W>(tDP, dp);
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-                const float4 nd = ndlt4[c4];
-                const float2 a = f2_unpack(f2_mul(f2_pack(pv[4 * c4], pv[4 * c4 + 1]),
-                                                  f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]),
-                                                         f2_pack(nd.x, nd.y))));
-                const float2 e = f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
-                                                  f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]),
-                                                         f2_pack(nd.z, nd.w))));
-                dp[4 * c4] = a.x;
-                dp[4 * c4 + 1] = a.y;
-                dp[4 * c4 + 2] = e.x;
-                dp[4 * c4 + 3] = e.y;
+                for (int c4 = 0; c4 < W / 4; ++c4) {
+                    const float4 nd = ndlt4[c4];
+                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[4 * c4], pv[4 * c4 + 1]),
+                                                      f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]),
+                                                             f2_pack(nd.x, nd.y))));
+                    const float2 e = f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
+                                                      f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]),
+                                                             f2_pack(nd.z, nd.w))));
+                    dp[4 * c4] = a.x;
+                    dp[4 * c4 + 1] = a.y;
+                    dp[4 * c4 + 2] = e.x;
+                    dp[4 * c4 + 3] = e.y;
+                }
+                tmem_st_bf16<W>(tDP, dp);
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tmem_st_bf16x64(tDP, dp);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars->ds_full[0]));
+            named_bar_signal(kBarDS0, C::kBarCount, ok);
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
         if (ok) {
             tc_fence_after();
-            // warpgroup 0 stores dV, warpgroup 1 stores dK (scaled)
+            // the first half of the warpgroups stores dV, the second dK (scaled), each
+            // warpgroup kSC columns of the row
+            constexpr int kHalf = C::kEwWG / 2;
+            constexpr int kSC = D / kHalf;
             const bool valid = kpos < len;
+            const bool is_dk = wg >= kHalf;
+            const int c0 = kSC * (wg % kHalf);
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
-            if (wg == 0)
-                store_acc_row<D>(tmem + lane_addr + C::kColAcc, 1.f,
-                                 reinterpret_cast<__nv_bfloat16*>(p.dv) + row, valid);
-            else
-                store_acc_row<D>(tmem + lane_addr + C::kColAcc + D, p.scale,
-                                 reinterpret_cast<__nv_bfloat16*>(p.dk) + row, valid);
+            store_acc_row<kSC>(tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0,
+                               is_dk ? p.scale : 1.f,
+                               reinterpret_cast<__nv_bfloat16*>(is_dk ? p.dk : p.dv) + row + c0, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -511,12 +592,12 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dkdv_kernel(const __grid_consta
 // dP_j) it issues dQ += dS_j K_j.  The tensor cores thus compute the next
 // tile's S and dP while the element-wise warps turn dP_j into dS_j.  K_j and
 // V_j stream through the slot ring as items 2j and 2j+1; V_j's slot is
-// released as soon as dP_j is done, K_j's after dQ_j.  dP_full / ds_full have
-// one barrier per dP buffer, so neither can run two phases ahead of its
-// waiter.
+// released as soon as dP_j is done, K_j's after dQ_j.  dp_full has one
+// mbarrier per dP buffer and "dS_j written" alternates between two named
+// barriers, so no signal can run two phases ahead of its waiter.
 
 template <int D>
-__global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Launched as a programmatic dependent of the dK/dV kernel: it may start while
@@ -564,58 +645,70 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
                             abort_flag, p);
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        // (whole warp walks the tiles, lane 0 issues; as in the dK/dV kernel it
+        // never waits on an mbarrier inside the loop)
+        auto slot = [&](int i) { return smem_addr(sSlots + slot_index<D>(i) * C::kTileBytes); };
+        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[slot_index<D>(i)])); };
+        auto dp_col = [&](int j) { return tmem + ((j & 1) ? C::kColDP1 : C::kColDP); };
+        const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO);
         if (lane == 0) {
             auto wait = [&](uint64_t& bar, int parity) {
                 return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
             };
-            auto slot = [&](int i) { return smem_addr(sSlots + (i % C::kSlots) * C::kTileBytes); };
-            auto wait_slot = [&](int i) { return wait(bars->slot_full[i % C::kSlots], (i / C::kSlots) & 1); };
-            auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[i % C::kSlots])); };
-            auto dp_col = [&](int j) { return tmem + ((j & 1) ? C::kColDP1 : C::kColDP); };
-            const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO);
-            bool ok = wait(bars->res_full, 0) && wait_slot(0);
-            if (ok) {
+            if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
+                wait(bars->slot_full[slot_index<D>(1)], 0)) {}
+            tc_fence_after();
+            issue_ss<D>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
+            mma_commit(smem_addr(&bars->s_full));
+            issue_ss<D>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
+            mma_commit(smem_addr(&bars->dp_full[0]));
+            free_slot(1);
+        }
+        __syncwarp();
+        for (int j = 0; j < nk; ++j) {
+            named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} and V_{j+1} landed
+            if (lane == 0 && j + 1 < nk) {
+                // S_{j+1} once S_j is in registers; dP_{j+1} into the other buffer,
+                // whose dS_{j-1} the already issued dQ_{j-1} reads first
                 tc_fence_after();
-                issue_ss<D>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
+                issue_ss<D>(tmem + C::kColS, aQ, slot(2 * j + 2));
                 mma_commit(smem_addr(&bars->s_full));
-                ok = wait_slot(1);
+                issue_ss<D>(dp_col(j + 1), aDO, slot(2 * j + 3));
+                mma_commit(smem_addr(&bars->dp_full[(j + 1) & 1]));
+                free_slot(2 * j + 3);
             }
-            if (ok) {
-                tc_fence_after();
-                issue_ss<D>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
-                mma_commit(smem_addr(&bars->dp_full[0]));
-                free_slot(1);
-            }
-            for (int j = 0; ok && j < nk; ++j) {
-                if (j + 1 < nk) {
-                    // S_{j+1} once S_j is in registers; dP_{j+1} into the other buffer,
-                    // whose dS_{j-1} the already issued dQ_{j-1} reads first
-                    if (!(ok = wait(bars->p_full, j & 1))) break;
-                    if (!(ok = wait_slot(2 * j + 2))) break;
-                    tc_fence_after();
-                    issue_ss<D>(tmem + C::kColS, aQ, slot(2 * j + 2));
-                    mma_commit(smem_addr(&bars->s_full));
-                    if (!(ok = wait_slot(2 * j + 3))) break;
-                    tc_fence_after();
-                    issue_ss<D>(dp_col(j + 1), aDO, slot(2 * j + 3));
-                    mma_commit(smem_addr(&bars->dp_full[(j + 1) & 1]));
-                    free_slot(2 * j + 3);
-                }
-                if (!(ok = wait(bars->ds_full[j & 1], (j >> 1) & 1))) break;
+            __syncwarp();
+            named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);   // dS_j written
+            if (lane == 0) {
                 tc_fence_after();
                 issue_ts<D>(tmem + C::kColAcc, dp_col(j), slot(2 * j), j > 0);   // dQ += dS K
                 free_slot(2 * j);
             }
-            mma_commit(smem_addr(&bars->acc_full));
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(smem_addr(&bars->acc_full));
+    } else if (warp == 2) {
+        // ------------------------------------------------------ slot relay
+        for (int j = 0; j < nk; ++j) {
+            if (lane == 0 && j + 1 < nk) {
+                for (int i = 2 * j + 2; i <= 2 * j + 3; ++i)
+                    mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(i)]), slot_use<D>(i) & 1,
+                              abort_flag, p.timeout_cycles, p.status);
+            }
+            __syncwarp();
+            named_bar_sync(kBarP, C::kBarCount);
+            named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);
         }
     } else if (warp >= 4) {
-        const int wg = (warp - 4) / 4;      // key columns [64 wg, 64 wg + 64) of each tile
+        constexpr int W = C::kEwCols;
+        const int wg = (warp - 4) / 4;      // key columns [W wg, W wg + W) of each tile
         const int quad = warp % 4;
         const int r = quad * 32 + lane;     // query row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + C::kColS + 64 * wg;
-        const uint32_t tDP0 = tmem + lane_addr + C::kColDP + 64 * wg;
-        const uint32_t tDP1 = tmem + lane_addr + C::kColDP1 + 64 * wg;
+        const uint32_t tS = tmem + lane_addr + C::kColS + W * wg;
+        const uint32_t tDP0 = tmem + lane_addr + C::kColDP + W * wg;
+        const uint32_t tDP1 = tmem + lane_addr + C::kColDP1 + W * wg;
         const int q = q0 + r;
         const bool valid = q < len;
         float lse2 = kPosInf, dlt = 0.f;
@@ -627,67 +720,73 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
         const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
         const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndlt2 = f2_pack(-dlt, -dlt);
         const int lo_q = key_lo(s, q), hi_q = valid ? key_hi(s, q, len) : -1;
+        // `ok`: as in the dK/dV kernel, a warp that gave up keeps taking part in
+        // every named-barrier phase
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
-            const int kc = (kt_first + j) * kBlockN + 64 * wg;   // first key of my columns
-            const bool need_mask = !(kc >= lo_q && kc + 63 <= hi_q);
+            const int kc = (kt_first + j) * kBlockN + W * wg;   // first key of my columns
+            const bool need_mask = !(kc >= lo_q && kc + W - 1 <= hi_q);
             const int clo = lo_q - kc, chi = hi_q - kc;
-            if (!(ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles,
-                                 p.status)))
-                break;
-            tc_fence_after();
-            float pv[64];
-            tmem_ld64(tS, pv);
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars->p_full));   // S_j consumed: the next S may be issued
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 a = f2_unpack(f2_fma(f2_pack(pv[2 * i], pv[2 * i + 1]), sl2x2, nlse2));
-                pv[2 * i] = ex2_approx(a.x);
-                pv[2 * i + 1] = ex2_approx(a.y);
+            if (ok) ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles, p.status);
+            float pv[W];
+            if (ok) {
+                tc_fence_after();
+                tmem_ldw<W>(tS, pv);
+                tc_fence_before();
             }
-            if (need_mask) {
+            named_bar_signal(kBarP, C::kBarCount, ok);   // S_j consumed: the next S may be issued
+            if (ok) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < clo || c > chi) pv[c] = 0.f;
-            }
-            if (!(ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
-                                 p.timeout_cycles, p.status)))
-                break;
-            tc_fence_after();
-            const uint32_t tDP = (j & 1) ? tDP1 : tDP0;
-            float dp[64];
-            tmem_ld64(tDP, dp);
+                for (int i = 0; i < W / 2; ++i) {
+                    const float2 a = f2_unpack(f2_fma(f2_pack(pv[2 * i], pv[2 * i + 1]), sl2x2, nlse2));
+                    pv[2 * i] = ex2_approx(a.x);
+                    pv[2 * i + 1] = ex2_approx(a.y);
+                }
+                if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]),
-                                                  f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2)));
-                dp[2 * i] = a.x;
-                dp[2 * i + 1] = a.y;
+                    for (int c = 0; c < W; ++c)
+                        if (c < clo || c > chi) pv[c] = 0.f;
+                }
+                ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
+                               p.timeout_cycles, p.status);
             }
-            tmem_st_bf16x64(tDP, dp);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars->ds_full[j & 1]));
+            if (ok) {
+                tc_fence_after();
+                const uint32_t tDP = (j & 1) ? tDP1 : tDP0;
+                float dp[W];
+                tmem_ldw<W>(tDP, dp);
+#pragma unroll
+                for (int i = 0; i < W / 2; ++i) {
+                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]),
+                                                      f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2)));
+                    dp[2 * i] = a.x;
+                    dp[2 * i + 1] = a.y;
+                }
+                tmem_st_bf16<W>(tDP, dp);
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            named_bar_signal((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount, ok);
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
-        if (ok) {
+        // the warpgroups share the dQ row store: kSC (>= 32) columns each, as far as it goes
+        constexpr int kSC = (D / C::kEwWG >= 32) ? D / C::kEwWG : 32;
+        if (ok && wg * kSC < D) {
             tc_fence_after();
-            // each warpgroup stores D/2 columns of the dQ row (scaled)
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-            store_acc_row<D / 2>(tmem + lane_addr + C::kColAcc + (D / 2) * wg, p.scale,
-                                 reinterpret_cast<__nv_bfloat16*>(p.dq) + row + (D / 2) * wg, valid);
+            store_acc_row<kSC>(tmem + lane_addr + C::kColAcc + kSC * wg, p.scale,
+                               reinterpret_cast<__nv_bfloat16*>(p.dq) + row + kSC * wg, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
 }
 
 template <typename K>
-cudaError_t launch_tc(K kern, int grid, int smem, const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_tc(K kern, int grid, int threads, int smem, const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 384, smem, stream>>>(p);
+    kern<<<grid, threads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -706,19 +805,22 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dkdv <= 0) return cudaSuccess;
-    return d == 128 ? launch_tc(fa_bwd_dkdv_kernel<128>, p.num_work_dkdv, BwdCfg<128>::kSmemBytes, p, stream)
-                    : launch_tc(fa_bwd_dkdv_kernel<64>, p.num_work_dkdv, BwdCfg<64>::kSmemBytes, p, stream);
+    return d == 128 ? launch_tc(fa_bwd_dkdv_kernel<128>, p.num_work_dkdv, BwdCfg<128>::kThreads,
+                                BwdCfg<128>::kSmemBytes, p, stream)
+                    : launch_tc(fa_bwd_dkdv_kernel<64>, p.num_work_dkdv, BwdCfg<64>::kThreads,
+                                BwdCfg<64>::kSmemBytes, p, stream);
 }
 
 // The dQ kernel is launched as a programmatic dependent of the dK/dV kernel
 // (see fa_bwd_dq_kernel).
 template <typename K>
-cudaError_t launch_dependent(K kern, int grid, int smem, const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_dependent(K kern, int grid, int threads, int smem, const BwdParams& p,
+                             cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(384);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -731,8 +833,10 @@ cudaError_t launch_dependent(K kern, int grid, int smem, const BwdParams& p, cud
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dq <= 0) return cudaSuccess;
-    return d == 128 ? launch_dependent(fa_bwd_dq_kernel<128>, p.num_work_dq, BwdCfg<128>::kSmemBytes, p, stream)
-                    : launch_dependent(fa_bwd_dq_kernel<64>, p.num_work_dq, BwdCfg<64>::kSmemBytes, p, stream);
+    return d == 128 ? launch_dependent(fa_bwd_dq_kernel<128>, p.num_work_dq, BwdCfg<128>::kThreads,
+                                       BwdCfg<128>::kSmemBytes, p, stream)
+                    : launch_dependent(fa_bwd_dq_kernel<64>, p.num_work_dq, BwdCfg<64>::kThreads,
+                                       BwdCfg<64>::kSmemBytes, p, stream);
 }
 
 }  // namespace fa

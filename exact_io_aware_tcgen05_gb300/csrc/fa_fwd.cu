@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 }
                 mma_commit(smem_addr(&bars->kv_empty[kv_stage(0)]));
             }
+            // The waits are grouped, one group per Q tile: a shared-memory load by the
+            // issuing thread holds back the MMAs it issues next until those already in
+            // flight have drained, so each separate wait costs a pipeline bubble.
             for (int j = 0; ok && j < nkv; ++j) {
                 const int iv = 2 * j + 1, ik = 2 * j + 2;
                 if (!(ok = wait_kv(iv))) break;
@@ -200,11 +203,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     if (!(ok = mbar_wait(smem_addr(&bars->p_full[t]), j & 1, abort_flag,
                                          p.timeout_cycles, p.status)))
                         break;
+                    if (t == 0 && j + 1 < nkv && !(ok = wait_kv(ik))) break;
                     tc_fence_after();
                     issue_pv(t, kv_stage(iv), j > 0);
                     if (j + 1 < nkv) {
-                        if (t == 0 && !(ok = wait_kv(ik))) break;
-                        tc_fence_after();
                         issue_qk(t, kv_stage(ik));
                         mma_commit(smem_addr(&bars->s_full[t]));
                         if (t == kFwdQTiles - 1) mma_commit(smem_addr(&bars->kv_empty[kv_stage(ik)]));

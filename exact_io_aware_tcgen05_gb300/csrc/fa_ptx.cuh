@@ -91,6 +91,31 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, l
     return true;
 }
 
+// ------------------------------------------------------------ named barriers
+//
+// Hardware barrier `id` (1..15; 0 is __syncthreads) that completes when `count`
+// threads have arrived; whole warps take part (warp-collective).  They link the
+// tcgen05 issuer with the warps feeding it: an mbarrier wait is a shared-memory
+// load, and a shared-memory load by the issuing warp holds back the MMAs it
+// issues next until those already in flight have drained.  A named barrier
+// does not.
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// A producer warp's signal: arrive while running normally; once it has given up
+// (`live` false, warp-uniform) it blocks instead, so a warp that skips its work
+// can never get a phase ahead of the barrier's other participants.
+__device__ __forceinline__ void named_bar_signal(int id, int count, bool live) {
+    if (live) named_bar_arrive(id, count);
+    else named_bar_sync(id, count);
+}
+
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
