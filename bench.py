@@ -104,10 +104,17 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# headers every kernel is compiled with: a change there also changes the kernel
+SHARED_SOURCES = ("fa_ptx.cuh", "fa_seq.cuh", "fa_kernels.h")
+
+
 def source_sha(kernel: str) -> str:
-    path = os.path.join(ROOT, "exact_io_aware_tcgen05_gb300", "csrc", KERNEL_SOURCES[kernel])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """SHA-256 (first 16 hex digits) of the kernel's source file and the shared headers."""
+    h = hashlib.sha256()
+    for name in (KERNEL_SOURCES[kernel],) + SHARED_SOURCES:
+        with open(os.path.join(ROOT, "exact_io_aware_tcgen05_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):

@@ -14,7 +14,8 @@
 // One CTA owns 256 query rows of one (sequence, head) as two 128-row tiles and
 // streams the 128-key K/V tiles they need:
 //   warp 0        TMA producer: both Q tiles once, then K_j, V_j into a ring
-//   warp 1        tcgen05 issuer (one thread); owns the TMEM allocation
+//   warp 1        tcgen05 issuer (lane 0 issues); owns the TMEM allocation
+//   warp 2        relay: waits for the K/V tiles the next products read
 //   warps 4..7    softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8..11   softmax + epilogue of query tile 1
 // TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 and O_1 (D columns each)
@@ -26,6 +27,14 @@
 // with ex2.  The running max used for exponentiation is only raised when the
 // block max exceeds it by more than 8 (a factor 256); O and l always share
 // that reference, so the result is exact and most blocks skip the O rescale.
+//
+// The issuer hears from the softmax warps (and, through the relay warp, from
+// the K/V ring) by named barriers, one per query tile and one phase per key
+// block: an mbarrier wait is a shared-memory load, and one by the issuing warp
+// would hold back its next MMAs until those in flight drained.  The softmax
+// warps hear from the issuer by tcgen05.commit mbarriers.  The signal opening
+// phase j+1 of tile t's barrier needs S_t(j+1), issued after phase j completed,
+// so no one runs a phase ahead.
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 #include "fa_seq.cuh"
@@ -52,10 +61,14 @@ struct FwdCfg {
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
 };
 
+// named barrier of query tile t: kFwdBarP + t (0 is __syncthreads); softmax
+// warpgroup t + issuer warp + relay warp
+constexpr int kFwdBarP = 1;
+constexpr int kFwdBarCount = kBlockM + 64;
+
 struct FwdBars {
     uint64_t q_full;
     uint64_t s_full[kFwdQTiles];
-    uint64_t p_full[kFwdQTiles];
     uint64_t o_full;
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
@@ -101,7 +114,6 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         mbar_init(smem_addr(&bars->o_full), 1);
         for (int t = 0; t < kFwdQTiles; ++t) {
             mbar_init(smem_addr(&bars->s_full[t]), 1);
-            mbar_init(smem_addr(&bars->p_full[t]), kBlockM);
         }
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(smem_addr(&bars->kv_full[i]), 1);
@@ -156,54 +168,46 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            auto kv_stage = [&](int i) { return i % C::kStages; };
-            auto kv_phase = [&](int i) { return (i / C::kStages) & 1; };
-            auto wait_kv = [&](int i) {
-                return mbar_wait(smem_addr(&bars->kv_full[kv_stage(i)]), kv_phase(i), abort_flag,
-                                 p.timeout_cycles, p.status);
-            };
-            auto issue_qk = [&](int t, int st) {
-                // descriptor of the tile base; a k-step adds its byte offset >> 4
-                const uint64_t qd = sdesc_sw128(smem_addr(sQ + t * C::kTileBytes), 16, 1024);
-                const uint64_t kd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes), 16, 1024);
+        // The whole warp walks the blocks (named barriers are warp-collective);
+        // lane 0 issues.  No mbarrier wait and no look at the abort flag inside
+        // the loop: after an abort it keeps issuing on stale data, so every
+        // barrier phase still completes.
+        auto kv_stage = [&](int i) { return i % C::kStages; };
+        auto issue_qk = [&](int t, int st) {
+            // descriptor of the tile base; a k-step adds its byte offset >> 4
+            const uint64_t qd = sdesc_sw128(smem_addr(sQ + t * C::kTileBytes), 16, 1024);
+            const uint64_t kd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
-                    mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, C::kIdescQK, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int st, bool acc) {
-                const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes),
-                                                C::kChunkBytes, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
-                           vd + ((kk * 2048) >> 4), C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = mbar_wait(smem_addr(&bars->q_full), 0, abort_flag, p.timeout_cycles,
-                                p.status);
-            if (ok) ok = wait_kv(0);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < kFwdQTiles; ++t) {
-                    issue_qk(t, kv_stage(0));
-                    mma_commit(smem_addr(&bars->s_full[t]));
-                }
-                mma_commit(smem_addr(&bars->kv_empty[kv_stage(0)]));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, C::kIdescQK, kk > 0);
             }
-            // The waits are grouped, one group per Q tile: a shared-memory load by the
-            // issuing thread holds back the MMAs it issues next until those already in
-            // flight have drained, so each separate wait costs a pipeline bubble.
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int iv = 2 * j + 1, ik = 2 * j + 2;
-                if (!(ok = wait_kv(iv))) break;
-                for (int t = 0; t < kFwdQTiles; ++t) {
-                    if (!(ok = mbar_wait(smem_addr(&bars->p_full[t]), j & 1, abort_flag,
-                                         p.timeout_cycles, p.status)))
-                        break;
-                    if (t == 0 && j + 1 < nkv && !(ok = wait_kv(ik))) break;
+        };
+        auto issue_pv = [&](int t, int st, bool acc) {
+            const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes),
+                                            C::kChunkBytes, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
+                       vd + ((kk * 2048) >> 4), C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+            }
+        };
+        if (lane == 0) {
+            if (mbar_wait(smem_addr(&bars->q_full), 0, abort_flag, p.timeout_cycles, p.status))
+                mbar_wait(smem_addr(&bars->kv_full[0]), 0, abort_flag, p.timeout_cycles, p.status);
+            tc_fence_after();
+            for (int t = 0; t < kFwdQTiles; ++t) {
+                issue_qk(t, kv_stage(0));
+                mma_commit(smem_addr(&bars->s_full[t]));
+            }
+            mma_commit(smem_addr(&bars->kv_empty[kv_stage(0)]));
+        }
+        __syncwarp();
+        for (int j = 0; j < nkv; ++j) {
+            const int iv = 2 * j + 1, ik = 2 * j + 2;
+            for (int t = 0; t < kFwdQTiles; ++t) {
+                named_bar_sync(kFwdBarP + t, kFwdBarCount);   // P_t(j) written (V_j, K_{j+1} landed)
+                if (lane == 0) {
                     tc_fence_after();
                     issue_pv(t, kv_stage(iv), j > 0);
                     if (j + 1 < nkv) {
@@ -212,10 +216,22 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         if (t == kFwdQTiles - 1) mma_commit(smem_addr(&bars->kv_empty[kv_stage(ik)]));
                     }
                 }
-                if (ok) mma_commit(smem_addr(&bars->kv_empty[kv_stage(iv)]));
+                __syncwarp();
             }
-            // o_full also tells the teardown that no MMA is still running.
-            mma_commit(smem_addr(&bars->o_full));
+            if (lane == 0) mma_commit(smem_addr(&bars->kv_empty[kv_stage(iv)]));
+        }
+        // o_full also tells the teardown that no MMA is still running.
+        if (lane == 0) mma_commit(smem_addr(&bars->o_full));
+    } else if (warp == 2) {
+        // ------------------------------------------------------ K/V relay
+        for (int j = 0; j < nkv; ++j) {
+            if (lane == 0) {
+                for (int i = 2 * j + 1; i <= 2 * j + 2 && i < 2 * nkv; ++i)
+                    mbar_wait(smem_addr(&bars->kv_full[i % C::kStages]), (i / C::kStages) & 1,
+                              abort_flag, p.timeout_cycles, p.status);
+            }
+            __syncwarp();
+            for (int t = 0; t < kFwdQTiles; ++t) named_bar_sync(kFwdBarP + t, kFwdBarCount);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------- softmax + epilogue
@@ -234,84 +250,89 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
         float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
         float l = 0.f;
+        // `ok` turns false (warp-uniformly: the TMEM accesses are warp-collective)
+        // when a wait gives up; the warp then skips the work but keeps taking part
+        // in every named-barrier phase, blocking instead of arriving.
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full[t]), j & 1, abort_flag,
-                                                   p.timeout_cycles, p.status));
-            if (!ok) break;  // warp-uniform: the TMEM accesses below are warp-collective
-            tc_fence_after();
-            uint32_t sr[kBlockN];
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full[t]), j & 1, abort_flag,
+                                                       p.timeout_cycles, p.status));
+            if (ok) {
+                tc_fence_after();
+                uint32_t sr[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c)
-                tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-            tmem_ld_wait();
-            reg_fence(sr);
-            float sv[kBlockN];
+                for (int c = 0; c < kBlockN / 32; ++c)
+                    tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                tmem_ld_wait();
+                reg_fence(sr);
+                float sv[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) sv[c] = __uint_as_float(sr[c]);
-            const int kb = (kv_first + j) * kBlockN;
-            if (!(kb >= full_lo && kb + kBlockN - 1 <= full_hi)) {
-                const int clo = lo_q - kb, chi = hi_q - kb;
+                for (int c = 0; c < kBlockN; ++c) sv[c] = __uint_as_float(sr[c]);
+                const int kb = (kv_first + j) * kBlockN;
+                if (!(kb >= full_lo && kb + kBlockN - 1 <= full_hi)) {
+                    const int clo = lo_q - kb, chi = hi_q - kb;
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (c < clo || c > chi) sv[c] = kNegInf;
-            }
-            // row max as a tree (8 independent chains) to keep the latency short
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-            for (int c = 8; c < kBlockN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_blk = mx * sl2;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (m_blk > m_ref + kRescaleThreshold) {
-                alpha = ex2_approx(m_ref - m_blk);  // 0 on the first visible block
-                rescale = (j > 0);
-                m_ref = m_blk;
-                l *= alpha;
-            }
-            const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
-            uint64_t rs2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
-                               f2_pack(0.f, 0.f)};
-            // P (bf16 pairs) goes to the first 64 columns of S_t in two halves; every
-            // S value is already in registers, so the overwrite is safe.
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int k = 64 * half + 2 * c;
-                    const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
-                    const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-                    rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
-                    pk[c] = pack_bf16x2(p0, p1);
+                    for (int c = 0; c < kBlockN; ++c)
+                        if (c < clo || c > chi) sv[c] = kNegInf;
                 }
-                tmem_st32(tS + 32 * half, pk);
-            }
-            const float2 rsum = f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])));
-            l += rsum.x + rsum.y;
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
-                // signalled; scale it in place before the next product accumulates.
+                // row max as a tree (8 independent chains) to keep the latency short
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t orow[32];
-                    tmem_ld32(tO + c * 32, orow);
-                    tmem_ld_wait();
-                    reg_fence(orow);
+                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                    tmem_st32(tO + c * 32, orow);
+                for (int c = 8; c < kBlockN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float m_blk = mx * sl2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_blk > m_ref + kRescaleThreshold) {
+                    alpha = ex2_approx(m_ref - m_blk);  // 0 on the first visible block
+                    rescale = (j > 0);
+                    m_ref = m_blk;
+                    l *= alpha;
                 }
+                const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
+                uint64_t rs2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
+                                   f2_pack(0.f, 0.f)};
+                // P (bf16 pairs) goes to the first 64 columns of S_t in two halves; every
+                // S value is already in registers, so the overwrite is safe.
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int k = 64 * half + 2 * c;
+                        const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
+                        const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                        rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
+                        pk[c] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(tS + 32 * half, pk);
+                }
+                const float2 rsum = f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])));
+                l += rsum.x + rsum.y;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
+                    // signalled; scale it in place before the next product accumulates.
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t orow[32];
+                        tmem_ld32(tO + c * 32, orow);
+                        tmem_ld_wait();
+                        reg_fence(orow);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                        tmem_st32(tO + c * 32, orow);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&bars->p_full[t]));
+            named_bar_signal(kFwdBarP + t, kFwdBarCount, ok);
         }
         // ------------------------------------------------------------ epilogue
         if (ok)
