@@ -184,37 +184,45 @@ class ClockSampler:
 # ---------------------------------------------------------------- oracle
 
 def oracle_sample(w, x, target_s: float):
-    """Time the fp64 oracle (forward, and backward if the workload has one) on a prefix of sequence 0 for the
-    query heads of key/value head 0, growing the prefix until the run takes about
-    target_s seconds.  Returns (TFLOP/s, threads, description, seconds, prefix length)."""
+    """Time the fp64 oracle (forward, and backward if the workload has one) on a sample of
+    sequence 0: a prefix of it for the query heads of key/value head 0, grown until the run
+    takes about target_s seconds; once the prefix is the whole sequence, further key/value
+    heads (with their query heads) join.  Returns (TFLOP/s, threads, description, seconds,
+    prefix length, key/value heads)."""
     import oracle
     oracle.build()
     G = w.Hq // w.Hkv
     L_full = w.seq_lengths()[0]
-    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))
-    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), slice(0, 1))
-    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), slice(0, 1))
-    do = oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G)) if w.backward else None
+    cu = w.cu_seqlens()
+    q = oracle.sequence_views(x["q"], 0, cu, slice(0, w.Hq))
+    k = oracle.sequence_views(x["k"], 0, cu, slice(0, w.Hkv))
+    v = oracle.sequence_views(x["v"], 0, cu, slice(0, w.Hkv))
+    do = oracle.sequence_views(x["dout"], 0, cu, slice(0, w.Hq)) if w.backward else None
 
-    def run(L):
-        qg = q[:L, :G].transpose(1, 0, 2)
+    def run(L, n_kv):
         t0 = time.perf_counter()
-        oracle.fwd_group(qg, k[:L, 0], v[:L, 0], w.causal, w.window, w.scale)
-        if w.backward:
-            oracle.bwd_group(qg, k[:L, 0], v[:L, 0], do[:L, :G].transpose(1, 0, 2), w.causal,
-                             w.window, w.scale)
+        for g in range(n_kv):
+            qg = q[:L, g * G:(g + 1) * G].transpose(1, 0, 2)
+            oracle.fwd_group(qg, k[:L, g], v[:L, g], w.causal, w.window, w.scale)
+            if w.backward:
+                oracle.bwd_group(qg, k[:L, g], v[:L, g], do[:L, g * G:(g + 1) * G].transpose(1, 0, 2),
+                                 w.causal, w.window, w.scale)
         return time.perf_counter() - t0
 
-    L = min(256, L_full)
-    t = run(L)
+    L, n_kv = min(256, L_full), 1
+    t = run(L, n_kv)
     while L < L_full and t < target_s / 3:
         L_new = min(L_full, int(L * max(1.25, min(4.0, math.sqrt(target_s / max(t, 1e-3))))))
         L_new = max(L + 1, L_new)
-        L, t = L_new, run(L_new)
-    flops = (14 if w.backward else 4) * w.d * G * visible_pairs(L, w.causal, w.window)
-    desc = (f"sequence 0, first {L} of {L_full} tokens, query heads 0..{G - 1} (key/value head 0), "
+        L, t = L_new, run(L_new, n_kv)
+    if L == L_full and t < target_s / 2 and w.Hkv > 1:
+        n_kv = min(w.Hkv, max(2, int(target_s / max(t, 1e-3))))
+        t = run(L, n_kv)
+    flops = (14 if w.backward else 4) * w.d * G * n_kv * visible_pairs(L, w.causal, w.window)
+    desc = (f"sequence 0, first {L} of {L_full} tokens, query heads 0..{G * n_kv - 1} "
+            f"(key/value heads 0..{n_kv - 1}), "
             f"{'forward + backward' if w.backward else 'forward'} in fp64")
-    return flops / t / 1e12, oracle.threads(), desc, t, L
+    return flops / t / 1e12, oracle.threads(), desc, t, L, n_kv
 
 
 # ------------------------------------------------------------ reference arm
@@ -226,23 +234,26 @@ def run_reference(args, w):
     x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=w.backward)
     total = args.steps + args.warmup
     per_step = min(10.0, max(0.3, 120.0 / max(total, 1)))   # whole run within a few minutes
-    _, threads, desc, _, L = oracle_sample(w, x, per_step)
+    _, threads, desc, _, L, n_kv = oracle_sample(w, x, per_step)
     import oracle
     G = w.Hq // w.Hkv
-    q = oracle.sequence_views(x["q"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
-    do = (oracle.sequence_views(x["dout"], 0, w.cu_seqlens(), slice(0, G))[:L].transpose(1, 0, 2)
-          if w.backward else None)
-    k = oracle.sequence_views(x["k"], 0, w.cu_seqlens(), 0)[:L]
-    v = oracle.sequence_views(x["v"], 0, w.cu_seqlens(), 0)[:L]
+    cu = w.cu_seqlens()
+    q = oracle.sequence_views(x["q"], 0, cu, slice(0, G * n_kv))[:L]
+    do = oracle.sequence_views(x["dout"], 0, cu, slice(0, G * n_kv))[:L] if w.backward else None
+    k = oracle.sequence_views(x["k"], 0, cu, slice(0, n_kv))[:L]
+    v = oracle.sequence_views(x["v"], 0, cu, slice(0, n_kv))[:L]
     times = []
     for i in range(total):
         t0 = time.perf_counter()
-        oracle.fwd_group(q, k, v, w.causal, w.window, w.scale)
-        if w.backward:
-            oracle.bwd_group(q, k, v, do, w.causal, w.window, w.scale)
+        for g in range(n_kv):
+            qg = q[:, g * G:(g + 1) * G].transpose(1, 0, 2)
+            oracle.fwd_group(qg, k[:, g], v[:, g], w.causal, w.window, w.scale)
+            if w.backward:
+                oracle.bwd_group(qg, k[:, g], v[:, g], do[:, g * G:(g + 1) * G].transpose(1, 0, 2),
+                                 w.causal, w.window, w.scale)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    flops = (14 if w.backward else 4) * w.d * G * visible_pairs(L, w.causal, w.window)
+    flops = (14 if w.backward else 4) * w.d * G * n_kv * visible_pairs(L, w.causal, w.window)
     ms = 1e3 * sum(times) / len(times)
     value = flops / (ms / 1e3) / 1e12
     line = {
@@ -481,7 +492,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, threads, desc, secs, _ = oracle_sample(w, x, args.cpu_seconds)
+        tf, threads, desc, secs, _, _ = oracle_sample(w, x, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": secs}
 
