@@ -231,7 +231,7 @@ def run_reference(args, w):
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=w.backward)
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=w.backward, dtype=w.dtype)
     total = args.steps + args.warmup
     per_step = min(10.0, max(0.3, 120.0 / max(total, 1)))   # whole run within a few minutes
     _, threads, desc, _, L, n_kv = oracle_sample(w, x, per_step)
@@ -272,7 +272,8 @@ def run_reference(args, w):
 def workload_config(w, l2_note):
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
            "causal": w.causal, "window": w.window, "packed": w.packed,
-           "total_tokens": w.total_tokens, "scale": "1/sqrt(d)", "inputs": "bf16 iid N(0,1), seed 0",
+           "total_tokens": w.total_tokens, "scale": "1/sqrt(d)",
+           "inputs": f"{w.dtype} iid N(0,1), seed 0",
            "l2": l2_note}
     if w.packed:
         cfg["lengths"] = list(w.lengths)
@@ -296,9 +297,12 @@ def run_ours(args, w):
     fa.load()
 
     bwd = w.backward          # forward-only workloads time fa_fwd alone
-    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=bwd)
+    x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=bwd, dtype=w.dtype)
+    dtype_code = fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16
 
     def pinned(a):
+        if a.dtype == np.float16:
+            return torch.from_numpy(a).pin_memory()
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
 
     h_in = {n: pinned(x[n]) for n in (("q", "k", "v", "dout") if bwd else ("q", "k", "v"))}
@@ -318,13 +322,13 @@ def run_ours(args, w):
     def step(ev_f=None, ev_b=None):
         if ev_f is not None:
             fa.fa_set_launch_events(ev_f)
-        fa.fa_fwd(d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
+        fa.fa_fwd_typed(dtype_code, d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
         if not bwd:
             return
         if ev_b is not None:
             fa.fa_set_launch_events(ev_b)
-        fa.fa_bwd(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk, dv, *geo, ws,
-                  ws_bytes, s)
+        fa.fa_bwd_typed(dtype_code, d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk,
+                        dv, *geo, ws, ws_bytes, s)
 
     in_bytes = sum(t.numel() * 2 for t in d_in.values()) + o.numel() * 2
     flush = in_bytes < 2 * L2_BYTES
@@ -428,10 +432,10 @@ def run_ours(args, w):
         stream.wait_event(ev["in"][b])
         if k >= 2:
             stream.wait_event(ev["out"][b])             # step k-2's results copied out
-        fa.fa_fwd(di["q"], di["k"], di["v"], do_["o"], do_["lse"], *geo, s)
+        fa.fa_fwd_typed(dtype_code, di["q"], di["k"], di["v"], do_["o"], do_["lse"], *geo, s)
         if bwd:
-            fa.fa_bwd(di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dout"], do_["dq"],
-                      do_["dk"], do_["dv"], *geo, ws, ws_bytes, s)
+            fa.fa_bwd_typed(dtype_code, di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dout"],
+                            do_["dq"], do_["dk"], do_["dv"], *geo, ws, ws_bytes, s)
         ev["comp"][b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][b])
@@ -500,7 +504,7 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": workload_config(w, l2_note),
             "pct_of_peak": value / world / peak_tf,
             "fwd_tflops": fwd_tf, "fwd_pct_of_peak": (fwd_tf / peak_tf) if fwd_tf else None,

@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FAError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_static_workspace",
+    "FAError", "load", "fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_bwd_workspace_size",
+    "fa_bwd_static_workspace", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
     "library_path",
@@ -29,6 +30,8 @@ library_path = os.path.join(_HERE, "libfa_gb300.so")
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
                 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+
+FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1   # fa_dtype
 
 _lib = None
 _vp, _i, _f, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
@@ -56,6 +59,10 @@ def load(path: str | None = None):
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                            _vp, _i, _f, _vp, _sz, _vp]
     lib.fa_bwd.restype = _i
+    lib.fa_fwd_typed.argtypes = [_i] + lib.fa_fwd.argtypes
+    lib.fa_fwd_typed.restype = _i
+    lib.fa_bwd_typed.argtypes = [_i] + lib.fa_bwd.argtypes
+    lib.fa_bwd_typed.restype = _i
     lib.fa_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
                                             _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
     lib.fa_bwd_static_workspace.restype = _i
@@ -121,6 +128,30 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, 
     return st
 
 
+def fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
+                 total_tokens, scale, stream=None, check: bool = True) -> int:
+    """fa_fwd for element type ``dtype`` (FA_DTYPE_BF16 or FA_DTYPE_F16)."""
+    st = load().fa_fwd_typed(int(dtype), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                             N, d, int(bool(causal)), int(window), _ptr(cu_seqlens),
+                             int(total_tokens), float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
+                 cu_seqlens, total_tokens, scale, workspace, workspace_bytes, stream=None,
+                 check: bool = True) -> int:
+    """fa_bwd for element type ``dtype`` (FA_DTYPE_BF16 or FA_DTYPE_F16)."""
+    st = load().fa_bwd_typed(int(dtype), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                             _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)),
+                             int(window), _ptr(cu_seqlens), int(total_tokens), float(scale),
+                             _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
 def fa_bwd_static_workspace(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
                             cu_seqlens, total_tokens, scale, stream=None, check: bool = True) -> int:
     """fa_bwd without a workspace argument, for callers that cannot allocate device
@@ -179,17 +210,30 @@ def _geometry(q, k, cu_seqlens, max_seqlen):
     return B, int(max_seqlen), Hq, k.shape[1], d, T
 
 
+def _dtype_code(*tensors) -> int:
+    """fa_dtype of torch tensors that must all be bf16, or all fp16."""
+    import torch
+    codes = {torch.bfloat16: FA_DTYPE_BF16, torch.float16: FA_DTYPE_F16}
+    kinds = {t.dtype for t in tensors}
+    if len(kinds) != 1 or next(iter(kinds)) not in codes:
+        raise TypeError(f"q, k, v (and o, dout) must all be bfloat16 or all float16, got {kinds}")
+    return codes[next(iter(kinds))]
+
+
 def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens=None,
                       max_seqlen=None, stream=None):
-    """O, LSE for bf16 CUDA tensors q, k, v in the library's layouts (allocates outputs)."""
+    """O, LSE for CUDA tensors q, k, v (all bf16 or all fp16) in the library's layouts
+    (allocates outputs)."""
     import torch
+    dtype = _dtype_code(q, k, v)
     B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((Hq, T) if cu_seqlens is not None else (B, Hq, N), dtype=torch.float32,
                       device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T, scale, stream)
+    fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T, scale,
+                 stream)
     return o, lse
 
 
@@ -197,6 +241,7 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=N
                        cu_seqlens=None, max_seqlen=None, stream=None, workspace=None):
     """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace)."""
     import torch
+    dtype = _dtype_code(q, k, v, o, dout)
     B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -204,6 +249,7 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=N
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T,
-           scale, workspace, workspace.numel() * workspace.element_size(), stream)
+    fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
+                 cu_seqlens, T, scale, workspace, workspace.numel() * workspace.element_size(),
+                 stream)
     return dq, dk, dv

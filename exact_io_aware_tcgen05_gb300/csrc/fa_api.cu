@@ -71,10 +71,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [tokens, heads, d] bf16 viewed as a 3-D tensor (d, heads, tokens); the box is
-// 64 elements of d (128 bytes, the swizzle span) x 1 head x 128 tokens.
+// [tokens, heads, d] 16-bit elements (bf16 or fp16) viewed as a 3-D tensor (d,
+// heads, tokens); the box is 64 elements of d (128 bytes, the swizzle span) x 1
+// head x 128 tokens.
 fa_status make_token_map(CUtensorMap* map, const void* base, int tokens, int heads, int d,
-                         const char* name) {
+                         fa_dtype dtype, const char* name) {
     auto enc = encode_fn();
     if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
@@ -83,7 +84,9 @@ fa_status make_token_map(CUtensorMap* map, const void* base, int tokens, int hea
                              static_cast<cuuint64_t>(heads) * d * 2};
     cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockM)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+    const CUtensorMapDataType type = dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = enc(map, type, 3, const_cast<void*>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -169,6 +172,16 @@ int num_blocks(const Geometry& g, int rows, int heads) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+fa_status check_dtype(fa_dtype dtype, const char* who) {
+    if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
+        return fail(FA_ERR_UNSUPPORTED, "%s: element type %d is neither FA_DTYPE_BF16 nor FA_DTYPE_F16",
+                    who, static_cast<int>(dtype));
+    return FA_OK;
+}
+
+// the kernels' element-type codes are the ABI's
+static_assert(FA_DTYPE_BF16 == kElemBf16Code && FA_DTYPE_F16 == kElemF16Code, "element codes");
+
 }  // namespace
 
 int* device_status_word() { return status_word_ptr(); }
@@ -201,6 +214,13 @@ void fa_set_wait_limit_cycles(long long cycles) {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                  int Hkv, int N, int d, int causal, int window, const int* cu_seqlens,
                  int total_tokens, float scale, cudaStream_t stream) {
+    return fa_fwd_typed(FA_DTYPE_BF16, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window,
+                        cu_seqlens, total_tokens, scale, stream);
+}
+
+fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                       const int* cu_seqlens, int total_tokens, float scale, cudaStream_t stream) {
     t_last_error[0] = '\0';
     const cudaEvent_t* ev = nullptr;
     if (take_events(1, &ev) != FA_OK)
@@ -209,16 +229,18 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return fail(FA_ERR_INVALID_ARG, "fa_fwd: q, k, v, o and lse must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return fail(FA_ERR_INVALID_ARG, "fa_fwd: tensors must be 16-byte aligned");
+    fa_status st = check_dtype(dtype, "fa_fwd");
+    if (st != FA_OK) return st;
     Geometry g;
-    fa_status st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens,
-                                scale, &g);
+    st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale, &g);
     if (st != FA_OK) return st;
     if (g.tokens == 0) return FA_OK;
 
     FwdParams p;
-    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, "q")) != FA_OK) return st;
-    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, "k")) != FA_OK) return st;
-    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, "v")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, dtype, "q")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, dtype, "k")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, dtype, "v")) != FA_OK) return st;
+    p.elem = static_cast<int>(dtype);
     p.seq = g.seq;
     p.o = o;
     p.lse = lse;
@@ -248,6 +270,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
                  int d, int causal, int window, const int* cu_seqlens, int total_tokens,
                  float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fa_bwd_typed(FA_DTYPE_BF16, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal,
+                        window, cu_seqlens, total_tokens, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int N, int d, int causal, int window,
+                       const int* cu_seqlens, int total_tokens, float scale, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
     t_last_error[0] = '\0';
     const cudaEvent_t* ev = nullptr;
     if (take_events(3, &ev) != FA_OK)
@@ -257,9 +288,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: tensors must be 16-byte aligned");
+    fa_status st = check_dtype(dtype, "fa_bwd");
+    if (st != FA_OK) return st;
     Geometry g;
-    fa_status st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens,
-                                scale, &g);
+    st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale, &g);
     if (st != FA_OK) return st;
     const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, N, d, cu_seqlens ? total_tokens : 0);
     if (!workspace || workspace_bytes < need)
@@ -270,10 +302,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (g.tokens == 0) return FA_OK;
 
     BwdParams p;
-    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, "q")) != FA_OK) return st;
-    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, "k")) != FA_OK) return st;
-    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, "v")) != FA_OK) return st;
-    if ((st = make_token_map(&p.tm_do, dout, g.tokens, Hq, d, "dout")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, dtype, "q")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, dtype, "k")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, dtype, "v")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_do, dout, g.tokens, Hq, d, dtype, "dout")) != FA_OK) return st;
+    p.elem = static_cast<int>(dtype);
     p.seq = g.seq;
     p.o = o;
     p.dout = dout;

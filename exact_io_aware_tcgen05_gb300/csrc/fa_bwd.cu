@@ -41,8 +41,8 @@ constexpr float kPosInf = __builtin_huge_valf();
 // ------------------------------------------------------------- preprocess
 
 // D_i = sum_c dO_ic O_ic in fp32 for every (token, query head).  A group of
-// D/8 lanes handles one row, 8 bf16 (16 bytes) per lane.
-template <int D>
+// D/8 lanes handles one row, 8 elements (16 bytes) per lane.  E: element type.
+template <int D, int E>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const __grid_constant__ BwdParams p) {
     constexpr int kLanesPerRow = D / 8;
     const SeqInfo& s = p.seq;
@@ -53,12 +53,11 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const __grid_con
     if (row < rows) {
         const uint4 o4 = reinterpret_cast<const uint4*>(p.o)[row * kLanesPerRow + sub];
         const uint4 d4 = reinterpret_cast<const uint4*>(p.dout)[row * kLanesPerRow + sub];
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
-        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d4);
+        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 a = __bfloat1622float2(o2[i]);
-            const float2 c = __bfloat1622float2(d2[i]);
+            const float2 a = unpack2<E>(ow[i]);
+            const float2 c = unpack2<E>(dw[i]);
             acc = fmaf(a.x, c.x, acc);
             acc = fmaf(a.y, c.y, acc);
         }
@@ -110,8 +109,6 @@ struct BwdCfg {
     static constexpr int kHeadBytes = 3072;
     static constexpr int kTilesBytes = (2 + kSlots) * kTileBytes;
     static constexpr int kSmemBytes = kHeadBytes + kTilesBytes;
-    static constexpr uint32_t kIdescSS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-    static constexpr uint32_t kIdescTS = idesc_bf16_f32(kBlockM, D, false, true);
 };
 static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
@@ -137,37 +134,40 @@ static_assert(sizeof(BwdBars) <= BwdCfg<128>::kBarBytes, "barrier block");
 static_assert(BwdCfg<128>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<128>::kHeadBytes, "stats");
 static_assert(BwdCfg<64>::kStatOffset + 2 * 2 * kBlockM * 4 <= BwdCfg<64>::kHeadBytes, "stats");
 
-// a[rows: K-major 128 x D] . b[rows: K-major 128 x D]^T -> tmem (128 x 128 fp32)
-template <int D>
+// a[rows: K-major 128 x D] . b[rows: K-major 128 x D]^T -> tmem (128 x 128 fp32);
+// E: element type of both operands
+template <int D, int E>
 __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a, uint32_t b) {
     using C = BwdCfg<D>;
+    constexpr uint32_t kIdescSS = idesc_f32acc(kBlockM, kBlockN, false, false, E);
     // descriptor of the tile base; a k-step adds its byte offset >> 4
     const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
-        mma_ss(d_tmem, ad + off, bd + off, C::kIdescSS, kk > 0);
+        mma_ss(d_tmem, ad + off, bd + off, kIdescSS, kk > 0);
     }
 }
 
-// A = bf16 operand written back to TMEM by the element-wise warpgroups: the W =
+// A = 16-bit operand written back to TMEM by the element-wise warpgroups: the W =
 // kEwCols tile columns of warpgroup w sit, packed two per 32-bit column, in the
 // first W/2 TMEM columns of that warpgroup's own range (region + W w).
 // D (128 x D fp32) (+)= A (128 x 128) . b[smem rows: 128 x D, MN-major].
-template <int D>
+template <int D, int E>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uint32_t b, bool acc) {
     using C = BwdCfg<D>;
+    constexpr uint32_t kIdescTS = idesc_f32acc(kBlockM, D, false, true, E);
     const uint64_t bd = sdesc_sw128(b, C::kChunkBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kBlockN / 16; ++kk)
         mma_ts(d_tmem, a_region + (16 * kk / C::kEwCols) * C::kEwCols + (16 * kk % C::kEwCols) / 2,
                bd + ((kk * 2048) >> 4),
-               C::kIdescTS, (acc || kk > 0) ? 1u : 0u);
+               kIdescTS, (acc || kk > 0) ? 1u : 0u);
 }
 
-// NC fp32 columns of a TMEM accumulator row * mul -> bf16 in global memory.
-template <int NC>
-__device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, __nv_bfloat16* dst,
+// NC fp32 columns of a TMEM accumulator row * mul -> element type E in global memory.
+template <int NC, int E>
+__device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, uint16_t* dst,
                                               bool valid) {
 #pragma unroll
     for (int c = 0; c < NC / 32; ++c) {
@@ -178,7 +178,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, __nv_bf
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+            w[i] = pack2<E>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
         if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -204,18 +204,18 @@ __device__ __forceinline__ void tmem_ldw(uint32_t taddr, float (&v)[W]) {
     }
 }
 
-// Packs W fp32 values to bf16 pairs and stores them in the first W/2 columns at taddr.
-template <int W>
-__device__ __forceinline__ void tmem_st_bf16(uint32_t taddr, const float (&v)[W]) {
+// Packs W fp32 values to pairs of element type E and stores them in the first W/2 columns at taddr.
+template <int W, int E>
+__device__ __forceinline__ void tmem_st_pk(uint32_t taddr, const float (&v)[W]) {
     if (W == 64) {
         uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[(2 * i) % W], v[(2 * i + 1) % W]);
+        for (int i = 0; i < 32; ++i) w[i] = pack2<E>(v[(2 * i) % W], v[(2 * i + 1) % W]);
         tmem_st32(taddr, w);
     } else {
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) w[i] = pack2<E>(v[2 * i], v[2 * i + 1]);
         tmem_st16(taddr, w);
     }
 }
@@ -350,7 +350,7 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
 // Each signal that would open phase n+1 of a named barrier depends on a product
 // issued after phase n completed, so no participant gets a phase ahead.
 
-template <int D>
+template <int D, int E>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -414,9 +414,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
                 wait(bars->slot_full[slot_index<D>(1)], 0)) {}
             tc_fence_after();
-            issue_ss<D>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
+            issue_ss<D, E>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
             mma_commit(smem_addr(&bars->s_full));
-            issue_ss<D>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
+            issue_ss<D, E>(tmem + C::kColDP, aV, slot(1));     // dP^T_0 = V dO_0^T
             mma_commit(smem_addr(&bars->dp_full[0]));
         }
         __syncwarp();
@@ -425,10 +425,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             named_bar_sync(kBarP, C::kBarCount);          // P^T_n written, Q_{n+1} landed
             if (lane == 0) {
                 tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc, tmem + C::kColS, slot(2 * n + 1), n > 0);   // dV += P^T dO
+                issue_ts<D, E>(tmem + C::kColAcc, tmem + C::kColS, slot(2 * n + 1), n > 0);   // dV += P^T dO
                 free_slot(2 * n + 1);
                 if (more) {
-                    issue_ss<D>(tmem + C::kColS, aK, slot(2 * n + 2));                     // S^T_{n+1}
+                    issue_ss<D, E>(tmem + C::kColS, aK, slot(2 * n + 2));                     // S^T_{n+1}
                     mma_commit(smem_addr(&bars->s_full));
                 }
             }
@@ -436,10 +436,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             named_bar_sync(kBarDS0, C::kBarCount);        // dS^T_n written, dO_{n+1} landed
             if (lane == 0) {
                 tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc + D, tmem + C::kColDP, slot(2 * n), n > 0);  // dK += dS^T Q
+                issue_ts<D, E>(tmem + C::kColAcc + D, tmem + C::kColDP, slot(2 * n), n > 0);  // dK += dS^T Q
                 free_slot(2 * n);
                 if (more) {
-                    issue_ss<D>(tmem + C::kColDP, aV, slot(2 * n + 3));                    // dP^T_{n+1}
+                    issue_ss<D, E>(tmem + C::kColDP, aV, slot(2 * n + 3));                    // dP^T_{n+1}
                     mma_commit(smem_addr(&bars->dp_full[0]));
                 }
             }
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                     for (int c = 0; c < W; ++c)
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
-                tmem_st_bf16<W>(tS, pv);
+                tmem_st_pk<W, E>(tS, pv);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                     dp[4 * c4 + 2] = e.x;
                     dp[4 * c4 + 3] = e.y;
                 }
-                tmem_st_bf16<W>(tDP, dp);
+                tmem_st_pk<W, E>(tDP, dp);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -576,9 +576,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             const bool is_dk = wg >= kHalf;
             const int c0 = kSC * (wg % kHalf);
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
-            store_acc_row<kSC>(tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0,
+            store_acc_row<kSC, E>(tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0,
                                is_dk ? p.scale : 1.f,
-                               reinterpret_cast<__nv_bfloat16*>(is_dk ? p.dk : p.dv) + row + c0, valid);
+                                  static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + row + c0, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 // mbarrier per dP buffer and "dS_j written" alternates between two named
 // barriers, so no signal can run two phases ahead of its waiter.
 
-template <int D>
+template <int D, int E>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -659,9 +659,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
                 wait(bars->slot_full[slot_index<D>(1)], 0)) {}
             tc_fence_after();
-            issue_ss<D>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
+            issue_ss<D, E>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
             mma_commit(smem_addr(&bars->s_full));
-            issue_ss<D>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
+            issue_ss<D, E>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
             mma_commit(smem_addr(&bars->dp_full[0]));
             free_slot(1);
         }
@@ -672,9 +672,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 // S_{j+1} once S_j is in registers; dP_{j+1} into the other buffer,
                 // whose dS_{j-1} the already issued dQ_{j-1} reads first
                 tc_fence_after();
-                issue_ss<D>(tmem + C::kColS, aQ, slot(2 * j + 2));
+                issue_ss<D, E>(tmem + C::kColS, aQ, slot(2 * j + 2));
                 mma_commit(smem_addr(&bars->s_full));
-                issue_ss<D>(dp_col(j + 1), aDO, slot(2 * j + 3));
+                issue_ss<D, E>(dp_col(j + 1), aDO, slot(2 * j + 3));
                 mma_commit(smem_addr(&bars->dp_full[(j + 1) & 1]));
                 free_slot(2 * j + 3);
             }
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);   // dS_j written
             if (lane == 0) {
                 tc_fence_after();
-                issue_ts<D>(tmem + C::kColAcc, dp_col(j), slot(2 * j), j > 0);   // dQ += dS K
+                issue_ts<D, E>(tmem + C::kColAcc, dp_col(j), slot(2 * j), j > 0);   // dQ += dS K
                 free_slot(2 * j);
             }
             __syncwarp();
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                     dp[2 * i] = a.x;
                     dp[2 * i + 1] = a.y;
                 }
-                tmem_st_bf16<W>(tDP, dp);
+                tmem_st_pk<W, E>(tDP, dp);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -775,8 +775,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         if (ok && wg * kSC < D) {
             tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-            store_acc_row<kSC>(tmem + lane_addr + C::kColAcc + kSC * wg, p.scale,
-                               reinterpret_cast<__nv_bfloat16*>(p.dq) + row + kSC * wg, valid);
+            store_acc_row<kSC, E>(tmem + lane_addr + C::kColAcc + kSC * wg, p.scale,
+                                  static_cast<uint16_t*>(p.dq) + row + kSC * wg, valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -798,17 +798,28 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream
     const long long threads = rows * lanes;
     const int grid = static_cast<int>((threads + 255) / 256);
     if (grid <= 0) return cudaSuccess;
-    if (d == 128) fa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(p);
-    else fa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(p);
+    const bool f16 = p.elem == kElemF16;
+    if (d == 128) {
+        if (f16) fa_bwd_preprocess_kernel<128, kElemF16><<<grid, 256, 0, stream>>>(p);
+        else fa_bwd_preprocess_kernel<128, kElemBf16><<<grid, 256, 0, stream>>>(p);
+    } else {
+        if (f16) fa_bwd_preprocess_kernel<64, kElemF16><<<grid, 256, 0, stream>>>(p);
+        else fa_bwd_preprocess_kernel<64, kElemBf16><<<grid, 256, 0, stream>>>(p);
+    }
     return cudaGetLastError();
+}
+
+template <int D, int E>
+cudaError_t launch_bwd_dkdv_d(const BwdParams& p, cudaStream_t stream) {
+    return launch_tc(fa_bwd_dkdv_kernel<D, E>, p.num_work_dkdv, BwdCfg<D>::kThreads,
+                     BwdCfg<D>::kSmemBytes, p, stream);
 }
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dkdv <= 0) return cudaSuccess;
-    return d == 128 ? launch_tc(fa_bwd_dkdv_kernel<128>, p.num_work_dkdv, BwdCfg<128>::kThreads,
-                                BwdCfg<128>::kSmemBytes, p, stream)
-                    : launch_tc(fa_bwd_dkdv_kernel<64>, p.num_work_dkdv, BwdCfg<64>::kThreads,
-                                BwdCfg<64>::kSmemBytes, p, stream);
+    if (p.elem == kElemF16)
+        return d == 128 ? launch_bwd_dkdv_d<128, kElemF16>(p, stream) : launch_bwd_dkdv_d<64, kElemF16>(p, stream);
+    return d == 128 ? launch_bwd_dkdv_d<128, kElemBf16>(p, stream) : launch_bwd_dkdv_d<64, kElemBf16>(p, stream);
 }
 
 // The dQ kernel is launched as a programmatic dependent of the dK/dV kernel
@@ -831,12 +842,17 @@ cudaError_t launch_dependent(K kern, int grid, int threads, int smem, const BwdP
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int D, int E>
+cudaError_t launch_bwd_dq_d(const BwdParams& p, cudaStream_t stream) {
+    return launch_dependent(fa_bwd_dq_kernel<D, E>, p.num_work_dq, BwdCfg<D>::kThreads,
+                            BwdCfg<D>::kSmemBytes, p, stream);
+}
+
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dq <= 0) return cudaSuccess;
-    return d == 128 ? launch_dependent(fa_bwd_dq_kernel<128>, p.num_work_dq, BwdCfg<128>::kThreads,
-                                       BwdCfg<128>::kSmemBytes, p, stream)
-                    : launch_dependent(fa_bwd_dq_kernel<64>, p.num_work_dq, BwdCfg<64>::kThreads,
-                                       BwdCfg<64>::kSmemBytes, p, stream);
+    if (p.elem == kElemF16)
+        return d == 128 ? launch_bwd_dq_d<128, kElemF16>(p, stream) : launch_bwd_dq_d<64, kElemF16>(p, stream);
+    return d == 128 ? launch_bwd_dq_d<128, kElemBf16>(p, stream) : launch_bwd_dq_d<64, kElemBf16>(p, stream);
 }
 
 }  // namespace fa

@@ -19,7 +19,7 @@
 //   warps 4..7    softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8..11   softmax + epilogue of query tile 1
 // TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 and O_1 (D columns each)
-// from 256.  P_t (bf16) overwrites the first 64 columns of S_t and feeds the
+// from 256.  P_t (bf16 or fp16, the input type) overwrites the first 64 columns of S_t and feeds the
 // P.V product straight from TMEM.  The issuer interleaves the two tiles so the
 // tensor cores work on one tile while the softmax warps work on the other:
 //   S0=Q0K0 S1=Q1K0 | O0+=P0V0 S0=Q0K1 | O1+=P1V0 S1=Q1K1 | O0+=P0V1 ...
@@ -39,15 +39,15 @@
 #include "fa_ptx.cuh"
 #include "fa_seq.cuh"
 
-#include <cuda_bf16.h>
 
 namespace fa {
+static_assert(kElemBf16 == kElemBf16Code && kElemF16 == kElemF16Code, "element-type codes");
 namespace {
 
 template <int D>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle column blocks
-    static constexpr int kChunkBytes = kBlockM * 128;      // 128 rows x 64 bf16
+    static constexpr int kChunkBytes = kBlockM * 128;      // 128 rows x 64 16-bit elements
     static constexpr int kTileBytes = kBlockM * D * 2;
     static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring depth
     static constexpr int kThreads = 384;
@@ -57,8 +57,6 @@ struct FwdCfg {
     static constexpr int kTilesBytes = (kFwdQTiles + kStages) * kTileBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kTilesBytes + kBarBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-    static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
 };
 
 // named barrier of query tile t: kFwdBarP + t (0 is __syncthreads); softmax
@@ -81,9 +79,12 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// E: element type of q, k, v and o (kElemBf16 or kElemF16)
+template <int D, int E>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
+    constexpr uint32_t kIdescQK = idesc_f32acc(kBlockM, kBlockN, false, false, E);
+    constexpr uint32_t kIdescPV = idesc_f32acc(kBlockM, D, false, true, E);
     const SeqInfo& s = p.seq;
 
     int b, h, qblk;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, C::kIdescQK, kk > 0);
+                mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, kIdescQK, kk > 0);
             }
         };
         auto issue_pv = [&](int t, int st, bool acc) {
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk) {
                 mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
-                       vd + ((kk * 2048) >> 4), C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                       vd + ((kk * 2048) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
             }
         };
         if (lane == 0) {
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
                 uint64_t rs2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
                                    f2_pack(0.f, 0.f)};
-                // P (bf16 pairs) goes to the first 64 columns of S_t in two halves; every
+                // P (16-bit pairs) goes to the first 64 columns of S_t in two halves; every
                 // S value is already in registers, so the overwrite is safe.
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
                         const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
                         rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
-                        pk[c] = pack_bf16x2(p0, p1);
+                        pk[c] = pack2<E>(p0, p1);
                     }
                     tmem_st32(tS + 32 * half, pk);
                 }
@@ -342,8 +343,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             tc_fence_after();
             const bool valid = q < len;
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            __nv_bfloat16* orow_g = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                    (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
+            uint16_t* orow_g = static_cast<uint16_t*>(p.o) +
+                               (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orow[32];
@@ -353,8 +354,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
-                                       __uint_as_float(orow[2 * i + 1]) * inv_l);
+                    w[i] = pack2<E>(__uint_as_float(orow[2 * i]) * inv_l,
+                                    __uint_as_float(orow[2 * i + 1]) * inv_l);
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
 #pragma unroll
@@ -381,10 +382,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     }
 }
 
-template <int D>
+template <int D, int E>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D>;
+    auto kern = fa_fwd_kernel<D, E>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -396,7 +397,9 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work <= 0) return cudaSuccess;
-    return d == 128 ? launch_fwd_d<128>(p, stream) : launch_fwd_d<64>(p, stream);
+    if (p.elem == kElemF16)
+        return d == 128 ? launch_fwd_d<128, kElemF16>(p, stream) : launch_fwd_d<64, kElemF16>(p, stream);
+    return d == 128 ? launch_fwd_d<128, kElemBf16>(p, stream) : launch_fwd_d<64, kElemBf16>(p, stream);
 }
 
 }  // namespace fa

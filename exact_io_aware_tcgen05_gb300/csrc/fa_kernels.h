@@ -14,6 +14,10 @@ namespace fa {
 constexpr int kBlockM = 128;   // rows of one MMA tile (TMEM lanes)
 constexpr int kBlockN = 128;   // keys per key/value tile
 constexpr int kFwdQTiles = 2;  // query tiles per forward CTA (ping-pong)
+// element-type codes of FwdParams::elem / BwdParams::elem (the values of fa_dtype;
+// the kernels name them kElemBf16 / kElemF16)
+constexpr int kElemBf16Code = 0;
+constexpr int kElemF16Code = 1;
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 // Token / sequence geometry common to all kernels.  Dense batches are the
@@ -28,14 +32,15 @@ struct SeqInfo {
 };
 
 struct FwdParams {
-    CUtensorMap tm_q;  // [total_tokens, Hq, d] bf16, box 64 x 1 x 128, 128B swizzle
+    CUtensorMap tm_q;  // [total_tokens, Hq, d] bf16 or fp16, box 64 x 1 x 128, 128B swizzle
     CUtensorMap tm_k;  // [total_tokens, Hkv, d]
     CUtensorMap tm_v;
     SeqInfo seq;
-    void* o;            // bf16 [tokens, Hq, d]
+    void* o;            // [tokens, Hq, d], element type of q
     float* lse;         // fp32 dense [B, Hq, N]; packed [Hq, total_tokens]
     float scale_log2;   // softmax scale * log2(e)
     int num_work;       // launched CTAs (upper bound on work items)
+    int elem;           // element type of q, k, v, o (kElemBf16Code / kElemF16Code)
     long long timeout_cycles;
     int* status;        // device status word
 };
@@ -43,16 +48,17 @@ struct FwdParams {
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as in FwdParams; dO like Q
     SeqInfo seq;
-    const void* o;      // bf16 forward output (for the preprocess)
-    const void* dout;   // bf16 dO (for the preprocess)
+    const void* o;      // forward output (for the preprocess)
+    const void* dout;   // dO (for the preprocess)
     const float* lse;   // forward logsumexp, layout as FwdParams::lse
     float* delta;       // fp32 D_i = rowsum(dO * O), same layout as lse
-    void* dq;           // bf16 outputs
+    void* dq;           // outputs, element type of q
     void* dk;
     void* dv;
     float scale;        // softmax scale
     float scale_log2;
     int num_work_dq, num_work_dkdv;
+    int elem;           // element type of every 16-bit tensor (kElemBf16Code / kElemF16Code)
     long long timeout_cycles;
     int* status;
 };

@@ -316,24 +316,48 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16 for bf16 A and B with an f32
-// accumulator: D format bits 4-5 = 1 (f32), A format bits 7-9 = 1 (bf16),
-// B format bits 10-12 = 1 (bf16), A / B major bits 15 / 16 (0 = K-major,
-// 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+// Element type of the operands and outputs (accumulation is always fp32); the
+// codes of the C ABI's fa_dtype.
+constexpr int kElemBf16 = 0;
+constexpr int kElemF16 = 1;
+
+// Instruction descriptor of tcgen05.mma.kind::f16 with an f32 accumulator and
+// A, B both of element type `elem`: D format bits 4-5 = 1 (f32), A format bits
+// 7-9 and B format bits 10-12 (1 = bf16, 0 = fp16; one kind::f16 product takes
+// one type for both), A / B major bits 15 / 16 (0 = K-major, 1 = MN-major),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_major,
+                                                    bool b_mn_major, int elem) {
+    return (1u << 4) | ((elem == kElemBf16 ? 1u : 0u) << 7) |
+           ((elem == kElemBf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // -------------------------------------------------------------- conversions
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// Two fp32 values rounded (to nearest even) to element type E and packed, `lo`
+// in the low half.
+template <int E>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t r;
     // cvt packs its first source operand into the upper half.
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    if (E == kElemBf16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// A packed pair of element type E widened to fp32 (exact).
+template <int E>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if (E == kElemBf16)
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(w));
+    return make_float2(lo, hi);
 }
 
 // Packed fp32 pairs for the f32x2 instructions (two fp32 lanes per 64-bit

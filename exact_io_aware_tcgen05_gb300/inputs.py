@@ -7,7 +7,9 @@ Recipe (the pages name no dataset; these stand in for real activations):
 * Q, K, V and dO are iid N(0, 1): ``numpy.random.default_rng(seed)
   .standard_normal(shape, dtype=float32)``, rounded to bf16 by
   round-to-nearest-even on the bit pattern, and returned as uint16 bf16 bit
-  patterns, so both the CUDA path and the oracle see the same bytes.
+  patterns, so both the CUDA path and the oracle see the same bytes.  For
+  fp16 runs the same float32 draws are rounded to IEEE binary16 (numpy's
+  float32 -> float16 cast, round-to-nearest-even) and returned as float16.
 * Seeds: Q = s, K = s + 1, V = s + 2, dO = s + 3.
 * Packed variable-length batches draw their lengths with
   ``default_rng(seed).integers(lo, hi + 1, size=n)`` (both ends inclusive).
@@ -33,6 +35,12 @@ def normal_bf16(shape, seed: int) -> np.ndarray:
     return bf16_bits_rne(x)
 
 
+def normal_f16(shape, seed: int) -> np.ndarray:
+    """iid N(0,1) drawn in float32 from ``default_rng(seed)``, rounded to float16."""
+    x = np.random.default_rng(seed).standard_normal(size=shape, dtype=np.float32)
+    return x.astype(np.float16)
+
+
 def varlen_lengths(seed: int, n: int = 16, lo: int = 256, hi: int = 8192) -> np.ndarray:
     """Sequence lengths drawn uniformly from [lo, hi] (inclusive)."""
     return np.random.default_rng(seed).integers(lo, hi + 1, size=n).astype(np.int64)
@@ -44,13 +52,18 @@ def cu_seqlens_of(lengths) -> np.ndarray:
     return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
 
 
-def attention_inputs(q_shape, kv_shape, seed: int, with_dout: bool = True):
-    """Q, K, V (and dO) bf16 bit patterns with the seed offsets of the recipe."""
+def attention_inputs(q_shape, kv_shape, seed: int, with_dout: bool = True, dtype: str = "bf16"):
+    """Q, K, V (and dO) with the seed offsets of the recipe: bf16 bit patterns
+    (dtype "bf16") or float16 arrays (dtype "f16")."""
+    draws = {"bf16": normal_bf16, "f16": normal_f16}
+    if dtype not in draws:
+        raise ValueError(f"dtype must be 'bf16' or 'f16', got {dtype!r}")
+    draw = draws[dtype]
     out = {
-        "q": normal_bf16(q_shape, seed),
-        "k": normal_bf16(kv_shape, seed + 1),
-        "v": normal_bf16(kv_shape, seed + 2),
+        "q": draw(q_shape, seed),
+        "k": draw(kv_shape, seed + 1),
+        "v": draw(kv_shape, seed + 2),
     }
     if with_dout:
-        out["dout"] = normal_bf16(q_shape, seed + 3)
+        out["dout"] = draw(q_shape, seed + 3)
     return out

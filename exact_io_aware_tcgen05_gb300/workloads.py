@@ -30,6 +30,7 @@ class Workload:
     window: int            # 0: none; else keys visible per query, including itself
     backward: bool         # whether the workload includes the backward pass
     lengths: Optional[Tuple[int, ...]] = None   # packed batch: per-sequence lengths
+    dtype: str = "bf16"    # element type of the 16-bit tensors: "bf16" or "f16"
 
     @property
     def scale(self) -> float:
@@ -105,6 +106,8 @@ WORKLOADS = {
         Workload("fwdbwd_b2_h16_n8192_d128_causal", 2, 16, 16, 8192, 128, True, 0, True),
         Workload("fwdbwd_b1_h32kv8_n16384_d128_causal_w4096", 1, 32, 8, 16384, 128, True, 4096,
                  True),
+        Workload("fwdbwd_b2_h16_n8192_d128_causal_f16", 2, 16, 16, 8192, 128, True, 0, True,
+                 dtype="f16"),
         _varlen(128),
         _varlen(64),
     ]

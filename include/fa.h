@@ -14,14 +14,15 @@
  *    Attention Does" (causal masking, variable-length sequences, GQA/MQA),
  *    "Key Features" (sliding window), "Architecture Overview" (backward from
  *    the saved output and logsumexp statistics), "Self-Hosting &
- *    Configuration" (BF16).
+ *    Configuration" (FP16 and BF16).
  *
  * Conventions for every entry point
  * ---------------------------------
  * Pointers marked "device" are CUDA device pointers owned by the caller; the
  * library never allocates, frees or keeps them, and never synchronises the
  * stream (fa_device_status excepted).  Every tensor is contiguous, bf16 unless
- * stated, and 16-byte aligned (TMA requirement).
+ * stated (fa_fwd_typed / fa_bwd_typed also take fp16), and 16-byte aligned
+ * (TMA requirement).
  *
  *   dense batch (cu_seqlens == NULL): B sequences of N tokens each
  *     q, o, dout, dq   [B, N, Hq, d]      k, v, dk, dv   [B, N, Hkv, d]
@@ -49,8 +50,8 @@
  *   sequence is empty) gets O = 0 and LSE = -inf.
  *
  * Supported: d in {64, 128}; 1 <= Hkv <= Hq, Hq % Hkv == 0.  Outputs are
- * written in full (no accumulate mode), rounded to bf16 by round-to-nearest-
- * even from fp32 accumulators.
+ * written in full (no accumulate mode), rounded to the input element type
+ * (bf16 unless stated) by round-to-nearest-even from fp32 accumulators.
  *
  * Errors: argument checks run before anything is enqueued and return
  * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE; a failed launch
@@ -68,6 +69,13 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* Element type of the 16-bit tensors (q, k, v, o, dout, dq, dk, dv); products
+ * accumulate in fp32 either way and lse / workspace stay fp32. */
+typedef enum fa_dtype {
+    FA_DTYPE_BF16 = 0,       /* bfloat16 (the type of fa_fwd / fa_bwd)             */
+    FA_DTYPE_F16 = 1         /* IEEE binary16                                       */
+} fa_dtype;
 
 typedef enum fa_status {
     FA_OK = 0,
@@ -100,6 +108,25 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * B * N rows are used).  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens);
+
+/*
+ * fa_fwd and fa_bwd for an explicit element type: `dtype` gives the type of
+ * every 16-bit tensor of the call (all of them share it; "Flash Attention --
+ * Fast Memory-Efficient Exact Attention", "Self-Hosting & Configuration", lists
+ * FP16 and BF16).  The probabilities P
+ * and the gradient dS that feed the second products are rounded to the same
+ * type.  fa_fwd and fa_bwd are these with FA_DTYPE_BF16.  A dtype outside
+ * fa_dtype returns FA_ERR_UNSUPPORTED before anything is enqueued; all other
+ * arguments and errors are those of fa_fwd / fa_bwd.
+ */
+fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                       const int* cu_seqlens, int total_tokens, float scale, cudaStream_t stream);
+fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int N, int d, int causal, int window,
+                       const int* cu_seqlens, int total_tokens, float scale, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Backward pass of fa_fwd for the loss gradient dO, recomputing S and P from

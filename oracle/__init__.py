@@ -88,7 +88,8 @@ def threads() -> int:
 
 
 def to_f64(a: np.ndarray) -> np.ndarray:
-    """uint16 bf16 bit patterns -> float64 (exact); float arrays are just upcast."""
+    """uint16 bf16 bit patterns -> float64 (exact); float arrays (float16 included)
+    are just upcast, also exactly."""
     a = np.asarray(a)
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -13,8 +13,9 @@ LSE_MAX_ABS = 1e-3      # logsumexp (fp32), max abs error
 GRAD_REL_FRO = 2e-2     # dQ, dK, dV: ||g - g*||_F / ||g*||_F
 
 
-def make_case(B, Hq, Hkv, N, d, seed, lengths=None, with_dout=True):
-    """Seeded inputs in the dense ([B, N, H, d]) or packed ([T, H, d]) layout."""
+def make_case(B, Hq, Hkv, N, d, seed, lengths=None, with_dout=True, dtype="bf16"):
+    """Seeded inputs in the dense ([B, N, H, d]) or packed ([T, H, d]) layout
+    (bf16 bit patterns, or float16 arrays for dtype "f16")."""
     if lengths is not None:
         T = int(sum(lengths))
         qs, kvs = (T, Hq, d), (T, Hkv, d)
@@ -22,14 +23,18 @@ def make_case(B, Hq, Hkv, N, d, seed, lengths=None, with_dout=True):
     else:
         qs, kvs = (B, N, Hq, d), (B, N, Hkv, d)
         cu = None
-    x = attention_inputs(qs, kvs, seed, with_dout=with_dout)
+    x = attention_inputs(qs, kvs, seed, with_dout=with_dout, dtype=dtype)
     x["cu"] = cu
     return x
 
 
 def to_dev(a):
+    """bf16 bit patterns (uint16) -> a bf16 CUDA tensor; float16 -> a float16 one."""
     import torch
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return torch.from_numpy(a).cuda()
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
 
 
 def cu_dev(cu):

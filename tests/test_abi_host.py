@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status"):
+    for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_bwd_workspace_size",
+              "fa_last_error", "fa_device_status"):
         assert n in names
 
 
@@ -60,6 +61,21 @@ def test_forward_rejects_bad_arguments(lib, over, status):
     fa, _ = lib
     assert _fwd(fa, **over) == status
     assert fa.fa_last_error() != ""
+
+
+def test_typed_entry_points_reject_unknown_element_types(lib):
+    fa, _ = lib
+    st = fa.fa_fwd_typed(7, 16, 16, 16, 16, 16, 1, 2, 1, 128, 128, 1, 0, None, 0, 0.125, None,
+                         check=False)
+    assert st == 2 and "element type" in fa.fa_last_error()
+    need = fa.fa_bwd_workspace_size(1, 2, 1, 128, 128, 0)
+    st = fa.fa_bwd_typed(-1, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 1, 128, 128, 1, 0, None, 0,
+                         0.125, 256, need, None, check=False)
+    assert st == 2 and "element type" in fa.fa_last_error()
+    # known element types still get the ordinary argument checks
+    st = fa.fa_fwd_typed(fa.FA_DTYPE_F16, None, 16, 16, 16, 16, 1, 2, 1, 128, 128, 1, 0, None, 0,
+                         0.125, None, check=False)
+    assert st == 1
 
 
 def test_backward_rejects_small_workspace(lib):

@@ -40,7 +40,11 @@ def run_workload(fa, w, x):
     dev = torch.device("cuda", 0)
 
     def d(a):
+        if a.dtype == np.float16:
+            return torch.from_numpy(a).to(dev)
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    code = fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16
 
     q, k, v = d(x["q"]), d(x["k"]), d(x["v"])
     cu = None if not w.packed else torch.from_numpy(w.cu_seqlens()).to(dev)
@@ -49,14 +53,14 @@ def run_workload(fa, w, x):
     lse = torch.empty(w.lse_shape, dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream(dev)
     geo = (w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, cu, T, w.scale)
-    fa.fa_fwd(q, k, v, o, lse, *geo, s)
+    fa.fa_fwd_typed(code, q, k, v, o, lse, *geo, s)
     out = {"o": o, "lse": lse}
     if w.backward:
         do = d(x["dout"])
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *geo, ws, ws_bytes, s)
+        fa.fa_bwd_typed(code, q, k, v, o, lse, do, dq, dk, dv, *geo, ws, ws_bytes, s)
         out.update(dq=dq, dk=dk, dv=dv)
     fa.fa_device_status(s)
     return {n: t.float().cpu().numpy().astype(np.float64) for n, t in out.items()}
@@ -72,7 +76,7 @@ def token_index(w, b, rows):
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_full_size_sampled(fa, oracle_mod, name):
     w = WORKLOADS[name]
-    x = attention_inputs(w.q_shape, w.kv_shape, 0, with_dout=w.backward)
+    x = attention_inputs(w.q_shape, w.kv_shape, 0, with_dout=w.backward, dtype=w.dtype)
     got = run_workload(fa, w, x)
     cu = w.cu_seqlens()
     G = w.Hq // w.Hkv

@@ -327,3 +327,45 @@ def test_bf16_decode_is_exact(oracle_mod):
     back = oracle_mod.to_f64(bits)
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
     np.testing.assert_array_equal(back, ref)
+
+
+def test_f16_decode_is_exact(oracle_mod):
+    """IEEE binary16 bit patterns decode to the values the format defines (sign,
+    5-bit exponent with bias 15, 10-bit fraction, subnormals at exponent 0),
+    worked out by hand here, not by numpy's own float16 conversion."""
+    cases = {
+        0x3C00: 1.0,                     # 2^0
+        0xC000: -2.0,                    # sign, 2^1
+        0x7BFF: 65504.0,                 # largest finite: (2 - 2^-10) * 2^15
+        0x0400: 2.0 ** -14,              # smallest normal
+        0x0001: 2.0 ** -24,              # smallest subnormal: 2^-10 * 2^-14
+        0x3555: (1 + 0x155 / 1024) * 2.0 ** -2,   # 0.333251953125
+        0x8000: -0.0,
+    }
+    bits = np.array(list(cases), dtype=np.uint16)
+    got = oracle_mod.to_f64(bits.view(np.float16))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+    assert np.signbit(got[-1])
+
+
+def test_f16_inputs_round_to_nearest_even(oracle_mod):
+    """The fp16 input draws are the float32 draws rounded to nearest, ties to even:
+    check against the rounding written out on the bit patterns."""
+    from exact_io_aware_tcgen05_gb300.inputs import normal_f16
+    x32 = np.random.default_rng(4).standard_normal(size=4096, dtype=np.float32)
+    got = oracle_mod.to_f64(normal_f16(4096, 4))
+    # |x| < 65504 and, for these draws, >= 2^-14 or exactly representable: round the
+    # 23-bit fraction to 10 bits by hand (normal range) and compare
+    u = x32.view(np.uint32).astype(np.int64)
+    sign = np.where(u >> 31, -1.0, 1.0)
+    e = ((u >> 23) & 0xFF) - 127
+    frac = (u & 0x7FFFFF) | 0x800000            # 24-bit significand
+    normal = e >= -14
+    shift = np.where(normal, 13, 13 + (-14 - e))  # bits dropped below fp16's last place
+    shift = np.minimum(shift, 40)
+    q = frac >> shift
+    rem = frac - (q << shift)
+    half = np.int64(1) << (shift - 1)
+    q = q + ((rem > half) | ((rem == half) & ((q & 1) == 1)))
+    ref = sign * q.astype(np.float64) * 2.0 ** (e - 23 + shift)
+    np.testing.assert_array_equal(got, ref)
