@@ -240,6 +240,7 @@ fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if ((st = make_token_map(&p.tm_q, q, g.tokens, Hq, d, dtype, "q")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, dtype, "k")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, dtype, "v")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_o, o, g.tokens, Hq, d, dtype, "o")) != FA_OK) return st;
     p.elem = static_cast<int>(dtype);
     p.seq = g.seq;
     p.o = o;
@@ -306,6 +307,9 @@ fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if ((st = make_token_map(&p.tm_k, k, g.tokens, Hkv, d, dtype, "k")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, dtype, "v")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_do, dout, g.tokens, Hq, d, dtype, "dout")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_dq, dq, g.tokens, Hq, d, dtype, "dq")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_dk, dk, g.tokens, Hkv, d, dtype, "dk")) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_dv, dv, g.tokens, Hkv, d, dtype, "dv")) != FA_OK) return st;
     p.elem = static_cast<int>(dtype);
     p.seq = g.seq;
     p.o = o;

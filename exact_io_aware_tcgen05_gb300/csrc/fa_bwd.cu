@@ -118,6 +118,7 @@ static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
 constexpr int kBarP = 1;     // P (P^T) written / S read
 constexpr int kBarDS0 = 2;   // dS (dS^T) written; the dQ kernel alternates kBarDS0 / kBarDS1
 constexpr int kBarDS1 = 3;
+constexpr int kBarEpi = 4;   // element-wise warps among themselves: the epilogue
 
 struct BwdBars {
     uint64_t res_full;        // resident pair landed
@@ -566,19 +567,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
-        if (ok) {
+        // The first half of the warpgroups stores dV, the second dK (scaled), each
+        // warpgroup kSC columns of the row.  A tile of 128 keys inside the sequence
+        // leaves through shared memory (the idle slot ring) and TMA stores, coalesced
+        // and asynchronous; a tile cut by the sequence end is stored row by row.
+        // The choice is made uniform over the element-wise warps.
+        constexpr int kHalf = C::kEwWG / 2;
+        constexpr int kSC = D / kHalf;
+        const bool is_dk = wg >= kHalf;
+        const int c0 = kSC * (wg % kHalf);
+        const uint32_t t_acc = tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0;
+        const float mul = is_dk ? p.scale : 1.f;
+        if (named_bar_all(kBarEpi, C::kEwThreads, ok && kb + kBlockN <= len)) {
             tc_fence_after();
-            // the first half of the warpgroups stores dV, the second dK (scaled), each
-            // warpgroup kSC columns of the row
-            constexpr int kHalf = C::kEwWG / 2;
-            constexpr int kSC = D / kHalf;
-            const bool valid = kpos < len;
-            const bool is_dk = wg >= kHalf;
-            const int c0 = kSC * (wg % kHalf);
+            stage_acc_row<kSC, E>(t_acc, mul, sSlots + (is_dk ? C::kTileBytes : 0), C::kChunkBytes,
+                                  r, c0);
+            fence_proxy_async_smem();
+            named_bar_sync(kBarEpi, C::kEwThreads);
+            if (warp == 4 && lane == 0) {
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_store_3d(&p.tm_dv, smem_addr(sSlots + c * C::kChunkBytes), c * 64, g,
+                                 seq_start + kb);
+                    tma_store_3d(&p.tm_dk, smem_addr(sSlots + C::kTileBytes + c * C::kChunkBytes),
+                                 c * 64, g, seq_start + kb);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();   // the CTA's shared memory outlives the reads
+            }
+        } else if (ok) {
+            tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
-            store_acc_row<kSC, E>(tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0,
-                               is_dk ? p.scale : 1.f,
-                                  static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + row + c0, valid);
+            store_acc_row<kSC, E>(t_acc, mul,
+                                  static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + row + c0,
+                                  kpos < len);
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -770,13 +791,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
-        // the warpgroups share the dQ row store: kSC (>= 32) columns each, as far as it goes
+        // The warpgroups share the dQ row store: kSC (>= 32) columns each, as far as it
+        // goes.  A whole query tile leaves through shared memory and TMA stores, a tile
+        // cut by the sequence end row by row (see the dK/dV epilogue).
         constexpr int kSC = (D / C::kEwWG >= 32) ? D / C::kEwWG : 32;
-        if (ok && wg * kSC < D) {
+        const bool mine = wg * kSC < D;
+        const uint32_t t_acc = tmem + lane_addr + C::kColAcc + kSC * wg;
+        if (named_bar_all(kBarEpi, C::kEwThreads, ok && q0 + kBlockM <= len)) {
+            if (mine) {
+                tc_fence_after();
+                stage_acc_row<kSC, E>(t_acc, p.scale, sSlots, C::kChunkBytes, r, kSC * wg);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(kBarEpi, C::kEwThreads);
+            if (warp == 4 && lane == 0) {
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_3d(&p.tm_dq, smem_addr(sSlots + c * C::kChunkBytes), c * 64, h,
+                                 seq_start + q0);
+                bulk_commit_group();
+                bulk_wait_read_all();
+            }
+        } else if (ok && mine) {
             tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-            store_acc_row<kSC, E>(tmem + lane_addr + C::kColAcc + kSC * wg, p.scale,
-                                  static_cast<uint16_t*>(p.dq) + row + kSC * wg, valid);
+            store_acc_row<kSC, E>(t_acc, p.scale, static_cast<uint16_t*>(p.dq) + row + kSC * wg,
+                                  valid);
         }
     }
     teardown_bwd_cta<D>(bars, warp);

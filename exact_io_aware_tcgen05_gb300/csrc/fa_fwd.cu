@@ -63,6 +63,7 @@ struct FwdCfg {
 // warpgroup t + issuer warp + relay warp
 constexpr int kFwdBarP = 1;
 constexpr int kFwdBarCount = kBlockM + 64;
+constexpr int kFwdBarEpi = 3;   // + t: softmax warpgroup t among itself, the epilogue
 
 struct FwdBars {
     uint64_t q_full;
@@ -339,10 +340,27 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         if (ok)
             ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->o_full), 0, abort_flag,
                                                    p.timeout_cycles, p.status));
-        if (ok) {
+        // A tile of 128 query rows inside the sequence leaves through shared memory
+        // (its K/V stage, idle by now) and TMA stores, coalesced and asynchronous; a
+        // tile cut by the sequence end is stored row by row.  The choice is made
+        // uniform over the warpgroup.
+        const bool valid = q < len;
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        if (named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
             tc_fence_after();
-            const bool valid = q < len;
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            uint8_t* stage = sKV + t * C::kTileBytes;
+            stage_acc_row<D, E>(tO, inv_l, stage, C::kChunkBytes, r, 0);
+            fence_proxy_async_smem();
+            named_bar_sync(kFwdBarEpi + t, kBlockM);
+            if (quad == 0 && lane == 0) {
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
+                                 seq_start + tile_q_first);
+                bulk_commit_group();
+                bulk_wait_read_all();   // the CTA's shared memory outlives the reads
+            }
+        } else if (ok) {
+            tc_fence_after();
             uint16_t* orow_g = static_cast<uint16_t*>(p.o) +
                                (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
 #pragma unroll
@@ -363,10 +381,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
             }
-            if (valid)
-                p.lse[row_stat_index(s, b, h, seq_start, q)] =
-                    (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
         }
+        if (ok && valid)
+            p.lse[row_stat_index(s, b, h, seq_start, q)] =
+                (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
     }
 
     // ------------------------------------------------------------ teardown

@@ -35,6 +35,7 @@ struct FwdParams {
     CUtensorMap tm_q;  // [total_tokens, Hq, d] bf16 or fp16, box 64 x 1 x 128, 128B swizzle
     CUtensorMap tm_k;  // [total_tokens, Hkv, d]
     CUtensorMap tm_v;
+    CUtensorMap tm_o;  // output, same layout as tm_q (stores of whole tiles)
     SeqInfo seq;
     void* o;            // [tokens, Hq, d], element type of q
     float* lse;         // fp32 dense [B, Hq, N]; packed [Hq, total_tokens]
@@ -47,6 +48,7 @@ struct FwdParams {
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as in FwdParams; dO like Q
+    CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs (stores of whole tiles)
     SeqInfo seq;
     const void* o;      // forward output (for the preprocess)
     const void* dout;   // dO (for the preprocess)

@@ -108,6 +108,21 @@ __device__ __forceinline__ void named_bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over its `count` threads: every
+// participant gets the same verdict (a way to make a choice uniform).
+__device__ __forceinline__ bool named_bar_all(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.and.pred pout, %2, %3, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // A producer warp's signal: arrive while running normally; once it has given up
 // (`live` false, warp-uniform) it blocks instead, so a warp that skips its work
 // can never get a phase ahead of the barrier's other participants.
@@ -141,6 +156,32 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
+}
+
+// 3-D tiled store shared -> global, tracked by the thread's bulk groups.  The
+// shared tile uses the tensor map's layout (128-byte swizzle); the coordinates
+// must not be negative and x (c0) * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk store this thread committed has finished reading shared
+// memory (the source may then be reused, or the CTA exit).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Orders this thread's earlier shared-memory writes before later async-proxy
+// (TMA) accesses issued after a thread synchronisation.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t make_l2_policy_evict_last() {
@@ -349,6 +390,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// Row r of a [128 rows x 64 elements] 16-bit tile in the 128-byte-swizzled layout
+// TMA uses: 16-byte unit u of the row sits at unit position u ^ (r % 8).
+__device__ __forceinline__ uint4* swizzled_unit(uint8_t* tile, int r, int u) {
+    return reinterpret_cast<uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
+}
+
 // A packed pair of element type E widened to fp32 (exact).
 template <int E>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
@@ -397,6 +444,33 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---------------------------------------------------------------- epilogues
+
+// NC fp32 columns of a TMEM accumulator row * mul, rounded to element type E, into
+// row r of a 128-row staging tile of the output (128-byte swizzle, chunks of 64
+// columns `chunk_bytes` apart); c0 is the output column of the first one.
+template <int NC, int E>
+__device__ __forceinline__ void stage_acc_row(uint32_t t_acc, float mul, uint8_t* stage,
+                                              int chunk_bytes, int r, int c0) {
+#pragma unroll
+    for (int c = 0; c < NC / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t_acc + c * 32, v);
+        tmem_ld_wait();
+        reg_fence(v);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int col = c0 + 32 * c + 8 * u;
+            uint4 w;
+            w.x = pack2<E>(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+            w.y = pack2<E>(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+            w.z = pack2<E>(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+            w.w = pack2<E>(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+            *swizzled_unit(stage + (col / 64) * chunk_bytes, r, (col % 64) / 8) = w;
+        }
+    }
 }
 
 }  // namespace fa
