@@ -183,6 +183,31 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle
 
+def oracle_pass(w, q, k, v, do, L: int, n_kv: int) -> None:
+    """One fp64 oracle pass (forward, and backward if the workload has one) over the first
+    L tokens of one sequence for key/value heads 0..n_kv-1 and their query heads.
+    q, do: [tokens, Hq', d]; k, v: [tokens, Hkv', d] float64 views of that sequence."""
+    import oracle
+    G = w.Hq // w.Hkv
+    if w.p_drop > 0:
+        # the dropout oracle (dense, numpy)
+        from oracle import dropout as odrop
+        from exact_io_aware_tcgen05_gb300.workloads import DROPOUT_OFFSET, DROPOUT_SEED
+        kw = dict(causal=w.causal, window=w.window, scale=w.scale, p_drop=w.p_drop,
+                  seed=DROPOUT_SEED, offset=DROPOUT_OFFSET)
+        qq, kk, vv = q[None, :L, :G * n_kv], k[None, :L, :n_kv], v[None, :L, :n_kv]
+        odrop.attention_fwd(qq, kk, vv, **kw)
+        if w.backward:
+            odrop.attention_bwd(qq, kk, vv, do[None, :L, :G * n_kv], **kw)
+        return
+    for g in range(n_kv):
+        qg = q[:L, g * G:(g + 1) * G].transpose(1, 0, 2)
+        oracle.fwd_group(qg, k[:L, g], v[:L, g], w.causal, w.window, w.scale)
+        if w.backward:
+            oracle.bwd_group(qg, k[:L, g], v[:L, g], do[:L, g * G:(g + 1) * G].transpose(1, 0, 2),
+                             w.causal, w.window, w.scale)
+
+
 def oracle_sample(w, x, target_s: float):
     """Time the fp64 oracle (forward, and backward if the workload has one) on a sample of
     sequence 0: a prefix of it for the query heads of key/value head 0, grown until the run
@@ -201,12 +226,7 @@ def oracle_sample(w, x, target_s: float):
 
     def run(L, n_kv):
         t0 = time.perf_counter()
-        for g in range(n_kv):
-            qg = q[:L, g * G:(g + 1) * G].transpose(1, 0, 2)
-            oracle.fwd_group(qg, k[:L, g], v[:L, g], w.causal, w.window, w.scale)
-            if w.backward:
-                oracle.bwd_group(qg, k[:L, g], v[:L, g], do[:L, g * G:(g + 1) * G].transpose(1, 0, 2),
-                                 w.causal, w.window, w.scale)
+        oracle_pass(w, q, k, v, do, L, n_kv)
         return time.perf_counter() - t0
 
     L, n_kv = min(256, L_full), 1
@@ -221,7 +241,8 @@ def oracle_sample(w, x, target_s: float):
     flops = (14 if w.backward else 4) * w.d * G * n_kv * visible_pairs(L, w.causal, w.window)
     desc = (f"sequence 0, first {L} of {L_full} tokens, query heads 0..{G * n_kv - 1} "
             f"(key/value heads 0..{n_kv - 1}), "
-            f"{'forward + backward' if w.backward else 'forward'} in fp64")
+            f"{'forward + backward' if w.backward else 'forward'} in fp64"
+            + (f", dropout {w.p_drop}" if w.p_drop > 0 else ""))
     return flops / t / 1e12, oracle.threads(), desc, t, L, n_kv
 
 
@@ -245,12 +266,7 @@ def run_reference(args, w):
     times = []
     for i in range(total):
         t0 = time.perf_counter()
-        for g in range(n_kv):
-            qg = q[:, g * G:(g + 1) * G].transpose(1, 0, 2)
-            oracle.fwd_group(qg, k[:, g], v[:, g], w.causal, w.window, w.scale)
-            if w.backward:
-                oracle.bwd_group(qg, k[:, g], v[:, g], do[:, g * G:(g + 1) * G].transpose(1, 0, 2),
-                                 w.causal, w.window, w.scale)
+        oracle_pass(w, q, k, v, do, L, n_kv)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     flops = (14 if w.backward else 4) * w.d * G * n_kv * visible_pairs(L, w.causal, w.window)
@@ -277,6 +293,8 @@ def workload_config(w, l2_note):
            "l2": l2_note}
     if w.packed:
         cfg["lengths"] = list(w.lengths)
+    if w.p_drop > 0:
+        cfg["p_drop"] = w.p_drop
     return cfg
 
 
@@ -299,6 +317,19 @@ def run_ours(args, w):
     bwd = w.backward          # forward-only workloads time fa_fwd alone
     x = attention_inputs(w.q_shape, w.kv_shape, args.seed, with_dout=bwd, dtype=w.dtype)
     dtype_code = fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16
+    from exact_io_aware_tcgen05_gb300.workloads import DROPOUT_OFFSET, DROPOUT_SEED
+    if w.p_drop > 0:
+        def fwd_call(*a):
+            fa.fa_fwd_dropout(dtype_code, w.p_drop, DROPOUT_SEED, DROPOUT_OFFSET, *a)
+
+        def bwd_call(*a):
+            fa.fa_bwd_dropout(dtype_code, w.p_drop, DROPOUT_SEED, DROPOUT_OFFSET, *a)
+    else:
+        def fwd_call(*a):
+            fa.fa_fwd_typed(dtype_code, *a)
+
+        def bwd_call(*a):
+            fa.fa_bwd_typed(dtype_code, *a)
 
     def pinned(a):
         if a.dtype == np.float16:
@@ -322,13 +353,13 @@ def run_ours(args, w):
     def step(ev_f=None, ev_b=None):
         if ev_f is not None:
             fa.fa_set_launch_events(ev_f)
-        fa.fa_fwd_typed(dtype_code, d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
+        fwd_call(d_in["q"], d_in["k"], d_in["v"], o, lse, *geo, s)
         if not bwd:
             return
         if ev_b is not None:
             fa.fa_set_launch_events(ev_b)
-        fa.fa_bwd_typed(dtype_code, d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk,
-                        dv, *geo, ws, ws_bytes, s)
+        bwd_call(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dout"], dq, dk, dv, *geo, ws,
+                 ws_bytes, s)
 
     in_bytes = sum(t.numel() * 2 for t in d_in.values()) + o.numel() * 2
     flush = in_bytes < 2 * L2_BYTES
@@ -432,10 +463,10 @@ def run_ours(args, w):
         stream.wait_event(ev["in"][b])
         if k >= 2:
             stream.wait_event(ev["out"][b])             # step k-2's results copied out
-        fa.fa_fwd_typed(dtype_code, di["q"], di["k"], di["v"], do_["o"], do_["lse"], *geo, s)
+        fwd_call(di["q"], di["k"], di["v"], do_["o"], do_["lse"], *geo, s)
         if bwd:
-            fa.fa_bwd_typed(dtype_code, di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dout"],
-                            do_["dq"], do_["dk"], do_["dv"], *geo, ws, ws_bytes, s)
+            bwd_call(di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dout"], do_["dq"],
+                     do_["dk"], do_["dv"], *geo, ws, ws_bytes, s)
         ev["comp"][b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][b])

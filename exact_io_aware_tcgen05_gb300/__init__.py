@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FAError", "load", "fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_bwd_workspace_size",
+    "FAError", "load", "fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
+    "fa_bwd_dropout", "fa_bwd_workspace_size",
     "fa_bwd_static_workspace", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
@@ -63,6 +64,11 @@ def load(path: str | None = None):
     lib.fa_fwd_typed.restype = _i
     lib.fa_bwd_typed.argtypes = [_i] + lib.fa_bwd.argtypes
     lib.fa_bwd_typed.restype = _i
+    _u64, _u32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_fwd_dropout.argtypes = [_i, _f, _u64, _u32] + lib.fa_fwd.argtypes
+    lib.fa_fwd_dropout.restype = _i
+    lib.fa_bwd_dropout.argtypes = [_i, _f, _u64, _u32] + lib.fa_bwd.argtypes
+    lib.fa_bwd_dropout.restype = _i
     lib.fa_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
                                             _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
     lib.fa_bwd_static_workspace.restype = _i
@@ -152,6 +158,32 @@ def fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, cau
     return st
 
 
+def fa_fwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window,
+                   cu_seqlens, total_tokens, scale, stream=None, check: bool = True) -> int:
+    """fa_fwd with dropout of the probabilities (see include/fa.h for the keep mask)."""
+    st = load().fa_fwd_dropout(int(dtype), float(p_drop), int(seed), int(offset), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)),
+                               int(window), _ptr(cu_seqlens), int(total_tokens), float(scale),
+                               _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_bwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d,
+                   causal, window, cu_seqlens, total_tokens, scale, workspace, workspace_bytes,
+                   stream=None, check: bool = True) -> int:
+    """fa_bwd of fa_fwd_dropout (same p_drop, seed, offset)."""
+    st = load().fa_bwd_dropout(int(dtype), float(p_drop), int(seed), int(offset), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                               B, Hq, Hkv, N, d, int(bool(causal)), int(window), _ptr(cu_seqlens),
+                               int(total_tokens), float(scale), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
 def fa_bwd_static_workspace(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
                             cu_seqlens, total_tokens, scale, stream=None, check: bool = True) -> int:
     """fa_bwd without a workspace argument, for callers that cannot allocate device
@@ -221,7 +253,7 @@ def _dtype_code(*tensors) -> int:
 
 
 def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens=None,
-                      max_seqlen=None, stream=None):
+                      max_seqlen=None, stream=None, dropout=None):
     """O, LSE for CUDA tensors q, k, v (all bf16 or all fp16) in the library's layouts
     (allocates outputs)."""
     import torch
@@ -232,13 +264,19 @@ def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens
     lse = torch.empty((Hq, T) if cu_seqlens is not None else (B, Hq, N), dtype=torch.float32,
                       device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T, scale,
-                 stream)
+    if dropout is not None:
+        p_drop, seed, offset = dropout
+        fa_fwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, B, Hq, Hkv, N, d, causal,
+                       window, cu_seqlens, T, scale, stream)
+    else:
+        fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T,
+                     scale, stream)
     return o, lse
 
 
 def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=None,
-                       cu_seqlens=None, max_seqlen=None, stream=None, workspace=None):
+                       cu_seqlens=None, max_seqlen=None, stream=None, workspace=None,
+                       dropout=None):
     """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace)."""
     import torch
     dtype = _dtype_code(q, k, v, o, dout)
@@ -249,7 +287,12 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=N
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
-                 cu_seqlens, T, scale, workspace, workspace.numel() * workspace.element_size(),
-                 stream)
+    ws_given = workspace.numel() * workspace.element_size()
+    if dropout is not None:
+        p_drop, seed, offset = dropout
+        fa_bwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv,
+                       N, d, causal, window, cu_seqlens, T, scale, workspace, ws_given, stream)
+    else:
+        fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
+                     cu_seqlens, T, scale, workspace, ws_given, stream)
     return dq, dk, dv

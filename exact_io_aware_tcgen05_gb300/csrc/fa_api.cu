@@ -182,6 +182,35 @@ fa_status check_dtype(fa_dtype dtype, const char* who) {
 // the kernels' element-type codes are the ABI's
 static_assert(FA_DTYPE_BF16 == kElemBf16Code && FA_DTYPE_F16 == kElemF16Code, "element codes");
 
+// Dropout parameters of a call: a pair is dropped with probability thresh / 256,
+// thresh = round(256 p_drop) (p_drop as float; see fa_fwd_dropout in fa.h).
+fa_status make_dropout(float p_drop, unsigned long long seed, unsigned int offset,
+                       DropoutParams* d, const char* who) {
+    if (!(p_drop >= 0.f) || !(p_drop < 1.f))
+        return fail(FA_ERR_INVALID_ARG, "%s: p_drop must be in [0, 1) (got %g)", who,
+                    static_cast<double>(p_drop));
+    const float t = std::floor(p_drop * 256.0f + 0.5f);
+    if (t > 255.f)
+        return fail(FA_ERR_UNSUPPORTED, "%s: p_drop %g rounds to 256/256; the largest is 255/256",
+                    who, static_cast<double>(p_drop));
+    d->thresh = static_cast<uint32_t>(t);
+    d->rscale = 256.0f / static_cast<float>(256u - d->thresh);
+    d->seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+    d->seed_hi = static_cast<uint32_t>(seed >> 32);
+    d->offset = offset;
+    return FA_OK;
+}
+
+fa_status fwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, const void* k,
+                   const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+                   int causal, int window, const int* cu_seqlens, int total_tokens, float scale,
+                   cudaStream_t stream);
+fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, const void* k,
+                   const void* v, const void* o, const float* lse, const void* dout, void* dq,
+                   void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal,
+                   int window, const int* cu_seqlens, int total_tokens, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 }  // namespace
 
 int* device_status_word() { return status_word_ptr(); }
@@ -222,6 +251,33 @@ fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
                        float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
                        const int* cu_seqlens, int total_tokens, float scale, cudaStream_t stream) {
     t_last_error[0] = '\0';
+    const DropoutParams none{};
+    return fwd_impl(dtype, none, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
+                    total_tokens, scale, stream);
+}
+
+fa_status fa_fwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
+                         unsigned int offset, const void* q, const void* k, const void* v, void* o,
+                         float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                         const int* cu_seqlens, int total_tokens, float scale,
+                         cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    DropoutParams drop{};
+    const fa_status st = make_dropout(p_drop, seed, offset, &drop, "fa_fwd_dropout");
+    if (st != FA_OK) return st;
+    return fwd_impl(dtype, drop, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
+                    total_tokens, scale, stream);
+}
+
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+fa_status fwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, const void* k,
+                   const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+                   int causal, int window, const int* cu_seqlens, int total_tokens, float scale,
+                   cudaStream_t stream) {
     const cudaEvent_t* ev = nullptr;
     if (take_events(1, &ev) != FA_OK)
         return fail(FA_ERR_INVALID_ARG, "fa_fwd: fa_set_launch_events needs >= 2 events");
@@ -242,6 +298,7 @@ fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if ((st = make_token_map(&p.tm_v, v, g.tokens, Hkv, d, dtype, "v")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_o, o, g.tokens, Hq, d, dtype, "o")) != FA_OK) return st;
     p.elem = static_cast<int>(dtype);
+    p.drop = drop;
     p.seq = g.seq;
     p.o = o;
     p.lse = lse;
@@ -256,6 +313,11 @@ fa_status fa_fwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
     return FA_OK;
 }
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
 
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens) {
     if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128) || total_tokens < 0)
@@ -281,6 +343,35 @@ fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
                        const int* cu_seqlens, int total_tokens, float scale, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream) {
     t_last_error[0] = '\0';
+    const DropoutParams none{};
+    return bwd_impl(dtype, none, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal,
+                    window, cu_seqlens, total_tokens, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
+                         unsigned int offset, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                         void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                         const int* cu_seqlens, int total_tokens, float scale, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    DropoutParams drop{};
+    const fa_status st = make_dropout(p_drop, seed, offset, &drop, "fa_bwd_dropout");
+    if (st != FA_OK) return st;
+    return bwd_impl(dtype, drop, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal,
+                    window, cu_seqlens, total_tokens, scale, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, const void* k,
+                   const void* v, const void* o, const float* lse, const void* dout, void* dq,
+                   void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal,
+                   int window, const int* cu_seqlens, int total_tokens, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     const cudaEvent_t* ev = nullptr;
     if (take_events(3, &ev) != FA_OK)
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: fa_set_launch_events needs >= 4 events");
@@ -311,6 +402,7 @@ fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if ((st = make_token_map(&p.tm_dk, dk, g.tokens, Hkv, d, dtype, "dk")) != FA_OK) return st;
     if ((st = make_token_map(&p.tm_dv, dv, g.tokens, Hkv, d, dtype, "dv")) != FA_OK) return st;
     p.elem = static_cast<int>(dtype);
+    p.drop = drop;
     p.seq = g.seq;
     p.o = o;
     p.dout = dout;
@@ -338,6 +430,11 @@ fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dq launch");
     return FA_OK;
 }
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
 
 fa_status fa_device_status(cudaStream_t stream) {
     t_last_error[0] = '\0';

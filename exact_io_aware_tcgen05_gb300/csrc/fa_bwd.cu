@@ -221,6 +221,29 @@ __device__ __forceinline__ void tmem_st_pk(uint32_t taddr, const float (&v)[W]) 
     }
 }
 
+// keep factor (0 or 1 / keep probability) of column c, from the row's dropout words
+template <int W>
+__device__ __forceinline__ float col_keep(const uint32_t (&dw)[W / 4], int c, const DropoutParams& d) {
+    return keep_factor(dw[c >> 2], c & 3, d.thresh, d.rscale);
+}
+
+// tmem_st_pk of v with the dropped columns zeroed (the 1 / keep-probability factor is
+// left to the fp32 side: the dV epilogue, the dS arithmetic)
+template <int W, int E>
+__device__ __forceinline__ void tmem_st_pk_dropped(uint32_t taddr, const float (&v)[W],
+                                                   const uint32_t (&dw)[W / 4],
+                                                   const DropoutParams& d) {
+    uint32_t w[W / 2];
+#pragma unroll
+    for (int i = 0; i < W / 2; ++i)
+        w[i] = pack2<E>(v[2 * i] * keep_factor(dw[i >> 1], (2 * i) & 3, d.thresh, 1.f),
+                        v[2 * i + 1] * keep_factor(dw[i >> 1], (2 * i + 1) & 3, d.thresh, 1.f));
+    if constexpr (W == 64)
+        tmem_st32(taddr, w);
+    else
+        tmem_st16(taddr, w);
+}
+
 // Returns false (uniformly for the CTA) if the dynamic shared memory base is not
 // 1024-byte aligned, which the 128-byte-swizzled tiles and the exact shared
 // memory budget rely on.
@@ -351,7 +374,7 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
 // Each signal that would open phase n+1 of a named barrier depends on a product
 // issued after phase n completed, so no participant gets a phase ahead.
 
-template <int D, int E>
+template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -511,11 +534,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                 ok = warp_wait(smem_addr(&bars->stat_full[wg][buf]), (n >> 1) & 1, abort_flag,
                                p.timeout_cycles, p.status);
             }
-            // P^T = exp(S^T - LSE) (keys x queries), written back as bf16 in place
+            // P^T = exp(S^T - LSE) (keys x queries), written back as bf16 in place (with
+            // dropout: the kept entries only, the operand of dV; dV is scaled by the
+            // inverse keep probability in its epilogue)
             if (ok) ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles, p.status);
             float pv[W];
+            uint32_t dw[DROP ? W / 4 : 1];   // dropout bytes of this key row, 4 queries a word
             if (ok) {
                 tc_fence_after();
+                if (DROP)
+                    dropout_words_cols<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q0 >> 2, kpos >> 2,
+                                              static_cast<uint32_t>(b * s.Hq + g * s.group + n / nq),
+                                              p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
                 tmem_ldw<W>(tS, pv);
 #pragma unroll
                 for (int c4 = 0; c4 < W / 4; ++c4) {
@@ -534,7 +564,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                     for (int c = 0; c < W; ++c)
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
-                tmem_st_pk<W, E>(tS, pv);
+                if (DROP)
+                    tmem_st_pk_dropped<W, E>(tS, pv, *reinterpret_cast<const uint32_t(*)[W / 4]>(dw), p.drop);
+                else
+                    tmem_st_pk<W, E>(tS, pv);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -545,6 +578,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                 tc_fence_after();
                 float dp[W];
                 tmem_ldw<W>(tDP, dp);
+                if (DROP) {
+                    // dS = P (keep dZ - D): dZ is the product's dP, taken through the keep factors
+#pragma unroll
+                    for (int c = 0; c < W; ++c)
+                        dp[c] *= col_keep<W>(*reinterpret_cast<const uint32_t(*)[W / 4]>(dw), c, p.drop);
+                }
 #pragma unroll
                 for (int c4 = 0; c4 < W / 4; ++c4) {
                     const float4 nd = ndlt4[c4];
@@ -577,7 +616,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
         const bool is_dk = wg >= kHalf;
         const int c0 = kSC * (wg % kHalf);
         const uint32_t t_acc = tmem + lane_addr + C::kColAcc + (is_dk ? D : 0) + c0;
-        const float mul = is_dk ? p.scale : 1.f;
+        const float mul = is_dk ? p.scale : (DROP ? p.drop.rscale : 1.f);   // dV = r (keep P)^T dO
         if (named_bar_all(kBarEpi, C::kEwThreads, ok && kb + kBlockN <= len)) {
             tc_fence_after();
             stage_acc_row<kSC, E>(t_acc, mul, sSlots + (is_dk ? C::kTileBytes : 0), C::kChunkBytes,
@@ -617,7 +656,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 // mbarrier per dP buffer and "dS_j written" alternates between two named
 // barriers, so no signal can run two phases ahead of its waiter.
 
-template <int D, int E>
+template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -750,6 +789,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             const int clo = lo_q - kc, chi = hi_q - kc;
             if (ok) ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles, p.status);
             float pv[W];
+            uint32_t dw[DROP ? W / 4 : 1];   // dropout bytes of this query row, 4 keys a word
             if (ok) {
                 tc_fence_after();
                 tmem_ldw<W>(tS, pv);
@@ -768,6 +808,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                     for (int c = 0; c < W; ++c)
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
+                if (DROP)
+                    dropout_words_rows<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q >> 2, kc >> 2,
+                                              static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
+                                              p.drop.seed_lo, p.drop.seed_hi, lane);
                 ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
                                p.timeout_cycles, p.status);
             }
@@ -776,6 +820,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 const uint32_t tDP = (j & 1) ? tDP1 : tDP0;
                 float dp[W];
                 tmem_ldw<W>(tDP, dp);
+                if (DROP) {
+                    // dS = P (keep dZ - D): dZ is the product's dP, taken through the keep factors
+#pragma unroll
+                    for (int c = 0; c < W; ++c)
+                        dp[c] *= col_keep<W>(*reinterpret_cast<const uint32_t(*)[W / 4]>(dw), c, p.drop);
+                }
 #pragma unroll
                 for (int i = 0; i < W / 2; ++i) {
                     const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]),
@@ -848,17 +898,22 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream
     return cudaGetLastError();
 }
 
-template <int D, int E>
+template <int D, int E, bool DROP>
 cudaError_t launch_bwd_dkdv_d(const BwdParams& p, cudaStream_t stream) {
-    return launch_tc(fa_bwd_dkdv_kernel<D, E>, p.num_work_dkdv, BwdCfg<D>::kThreads,
+    return launch_tc(fa_bwd_dkdv_kernel<D, E, DROP>, p.num_work_dkdv, BwdCfg<D>::kThreads,
                      BwdCfg<D>::kSmemBytes, p, stream);
+}
+
+template <int D, int E>
+cudaError_t launch_bwd_dkdv_de(const BwdParams& p, cudaStream_t stream) {
+    return p.drop.thresh ? launch_bwd_dkdv_d<D, E, true>(p, stream) : launch_bwd_dkdv_d<D, E, false>(p, stream);
 }
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dkdv <= 0) return cudaSuccess;
     if (p.elem == kElemF16)
-        return d == 128 ? launch_bwd_dkdv_d<128, kElemF16>(p, stream) : launch_bwd_dkdv_d<64, kElemF16>(p, stream);
-    return d == 128 ? launch_bwd_dkdv_d<128, kElemBf16>(p, stream) : launch_bwd_dkdv_d<64, kElemBf16>(p, stream);
+        return d == 128 ? launch_bwd_dkdv_de<128, kElemF16>(p, stream) : launch_bwd_dkdv_de<64, kElemF16>(p, stream);
+    return d == 128 ? launch_bwd_dkdv_de<128, kElemBf16>(p, stream) : launch_bwd_dkdv_de<64, kElemBf16>(p, stream);
 }
 
 // The dQ kernel is launched as a programmatic dependent of the dK/dV kernel
@@ -881,17 +936,22 @@ cudaError_t launch_dependent(K kern, int grid, int threads, int smem, const BwdP
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int D, int E>
+template <int D, int E, bool DROP>
 cudaError_t launch_bwd_dq_d(const BwdParams& p, cudaStream_t stream) {
-    return launch_dependent(fa_bwd_dq_kernel<D, E>, p.num_work_dq, BwdCfg<D>::kThreads,
+    return launch_dependent(fa_bwd_dq_kernel<D, E, DROP>, p.num_work_dq, BwdCfg<D>::kThreads,
                             BwdCfg<D>::kSmemBytes, p, stream);
+}
+
+template <int D, int E>
+cudaError_t launch_bwd_dq_de(const BwdParams& p, cudaStream_t stream) {
+    return p.drop.thresh ? launch_bwd_dq_d<D, E, true>(p, stream) : launch_bwd_dq_d<D, E, false>(p, stream);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work_dq <= 0) return cudaSuccess;
     if (p.elem == kElemF16)
-        return d == 128 ? launch_bwd_dq_d<128, kElemF16>(p, stream) : launch_bwd_dq_d<64, kElemF16>(p, stream);
-    return d == 128 ? launch_bwd_dq_d<128, kElemBf16>(p, stream) : launch_bwd_dq_d<64, kElemBf16>(p, stream);
+        return d == 128 ? launch_bwd_dq_de<128, kElemF16>(p, stream) : launch_bwd_dq_de<64, kElemF16>(p, stream);
+    return d == 128 ? launch_bwd_dq_de<128, kElemBf16>(p, stream) : launch_bwd_dq_de<64, kElemBf16>(p, stream);
 }
 
 }  // namespace fa

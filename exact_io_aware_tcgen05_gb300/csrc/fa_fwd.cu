@@ -80,8 +80,8 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// E: element type of q, k, v and o (kElemBf16 or kElemF16)
-template <int D, int E>
+// E: element type of q, k, v and o (kElemBf16 or kElemF16); DROP: dropout of P
+template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
     constexpr uint32_t kIdescQK = idesc_f32acc(kBlockM, kBlockN, false, false, E);
@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int full_lo = key_lo(s, tile_q_last);            // keys >= this are >= every row's lo
         const int full_hi = key_hi(s, tile_q_first, len);      // keys <= this are <= every row's hi
         const float sl2 = p.scale_log2;
+        const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h);   // dropout counter word
 
         float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
         float l = 0.f;
@@ -304,13 +305,28 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
+                    // dropout: the random bytes of keys kb + 64 half .. + 63 of this row;
+                    // l sums the probabilities before dropout, the product takes the kept
+                    // ones (the 1 / keep-probability factor is applied to O in fp32 at the
+                    // end, so the 16-bit P carries no extra rounding)
+                    uint32_t dw[DROP ? 16 : 1];
+                    if (DROP)
+                        dropout_words_rows<16>(*reinterpret_cast<uint32_t(*)[16]>(dw), q >> 2,
+                                               (kb + 64 * half) >> 2, hs, p.drop.offset,
+                                               p.drop.seed_lo, p.drop.seed_hi, lane);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int k = 64 * half + 2 * c;
                         const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
                         const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
                         rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
-                        pk[c] = pack2<E>(p0, p1);
+                        if (DROP)
+                            pk[c] = pack2<E>(p0 * keep_factor(dw[(c >> 1) % (DROP ? 16 : 1)], (2 * c) & 3,
+                                                              p.drop.thresh, 1.f),
+                                             p1 * keep_factor(dw[(c >> 1) % (DROP ? 16 : 1)], (2 * c + 1) & 3,
+                                                              p.drop.thresh, 1.f));
+                        else
+                            pk[c] = pack2<E>(p0, p1);
                     }
                     tmem_st32(tS + 32 * half, pk);
                 }
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         // tile cut by the sequence end is stored row by row.  The choice is made
         // uniform over the warpgroup.
         const bool valid = q < len;
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) / l : 0.f;
         if (named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
             tc_fence_after();
             uint8_t* stage = sKV + t * C::kTileBytes;
@@ -400,10 +416,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     }
 }
 
-template <int D, int E>
+template <int D, int E, bool DROP>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, E>;
+    auto kern = fa_fwd_kernel<D, E, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -415,9 +431,13 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work <= 0) return cudaSuccess;
-    if (p.elem == kElemF16)
-        return d == 128 ? launch_fwd_d<128, kElemF16>(p, stream) : launch_fwd_d<64, kElemF16>(p, stream);
-    return d == 128 ? launch_fwd_d<128, kElemBf16>(p, stream) : launch_fwd_d<64, kElemBf16>(p, stream);
+    const bool f16 = p.elem == kElemF16, drop = p.drop.thresh != 0;
+    if (drop) {
+        if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, true>(p, stream) : launch_fwd_d<64, kElemF16, true>(p, stream);
+        return d == 128 ? launch_fwd_d<128, kElemBf16, true>(p, stream) : launch_fwd_d<64, kElemBf16, true>(p, stream);
+    }
+    if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, false>(p, stream) : launch_fwd_d<64, kElemF16, false>(p, stream);
+    return d == 128 ? launch_fwd_d<128, kElemBf16, false>(p, stream) : launch_fwd_d<64, kElemBf16, false>(p, stream);
 }
 
 }  // namespace fa

@@ -31,6 +31,15 @@ struct SeqInfo {
     int causal, window;     // window <= 0: none
 };
 
+// Dropout of the attention probabilities (see fa_fwd_dropout in fa.h): a pair is
+// kept iff its random byte is >= thresh (thresh == 0: no dropout, the kernels
+// compiled without it run); kept probabilities are scaled by rscale.
+struct DropoutParams {
+    uint32_t thresh;    // 0 .. 255
+    float rscale;       // 256 / (256 - thresh)
+    uint32_t seed_lo, seed_hi, offset;
+};
+
 struct FwdParams {
     CUtensorMap tm_q;  // [total_tokens, Hq, d] bf16 or fp16, box 64 x 1 x 128, 128B swizzle
     CUtensorMap tm_k;  // [total_tokens, Hkv, d]
@@ -42,6 +51,7 @@ struct FwdParams {
     float scale_log2;   // softmax scale * log2(e)
     int num_work;       // launched CTAs (upper bound on work items)
     int elem;           // element type of q, k, v, o (kElemBf16Code / kElemF16Code)
+    DropoutParams drop;
     long long timeout_cycles;
     int* status;        // device status word
 };
@@ -61,6 +71,7 @@ struct BwdParams {
     float scale_log2;
     int num_work_dq, num_work_dkdv;
     int elem;           // element type of every 16-bit tensor (kElemBf16Code / kElemF16Code)
+    DropoutParams drop;
     long long timeout_cycles;
     int* status;
 };

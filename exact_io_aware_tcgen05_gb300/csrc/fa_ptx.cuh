@@ -473,4 +473,111 @@ __device__ __forceinline__ void stage_acc_row(uint32_t t_acc, float mul, uint8_t
     }
 }
 
+// ------------------------------------------------------------------ dropout
+//
+// Philox4x32-10, the counter-based generator of Salmon, Moraes, Dror and Shaw,
+// "Parallel Random Numbers: As Easy as 1, 2, 3" (SC 2011): ten rounds of
+// (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+// with the key bumped by the Weyl constants between rounds.
+struct Philox4 {
+    uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+    constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+    constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += kW0;
+            k1 += kW1;
+        }
+        const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
+        const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return Philox4{c0, c1, c2, c3};
+}
+
+__device__ __forceinline__ uint32_t pick4(const Philox4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// The dropout draw of one 4 x 4 block of (query, key) pairs -- queries 4 I .. 4 I + 3,
+// keys 4 J .. 4 J + 3 of one (sequence, query head) -- is one Philox call with
+// counter (J, I, head_seq, offset) and key (seed low, seed high): output word w
+// belongs to query 4 I + w, its byte k (bits 8k .. 8k + 7) to key 4 J + k.  A pair
+// is kept iff its byte is >= the threshold.
+//
+// Four consecutive lanes 4m .. 4m + 3 of a warp form a group.  gather_rows: the
+// lanes hold 4 consecutive query rows (lane 4m + a = query 4 I + a) and want the
+// 4 keys of each block J in a list; gather_cols: the lanes hold 4 consecutive key
+// rows (lane 4m + a = key 4 J + a) and want the 4 queries of each block I.  In
+// round r lane 4m + a draws the block of index 4 r + a of the list and the group
+// transposes the four draws, so every lane gets, for each of the 4 list entries
+// of the round, one 32-bit word with the 4 bytes of its own row.
+__device__ __forceinline__ void group_transpose4(const uint32_t (&mine)[4], uint32_t (&out)[4],
+                                                 int lane) {
+    const int a = lane & 3, base = lane & ~3;
+    out[a] = mine[a];
+#pragma unroll
+    for (int s = 1; s < 4; ++s) {
+        const uint32_t send = mine[(a + s) & 3];
+        const int src = (a - s) & 3;
+        out[src] = __shfl_sync(0xffffffffu, send, base | src);
+    }
+}
+
+// Rows are queries: word (query row) of the block's draw, per block J of the list
+template <int NB>   // list length, a multiple of 4
+__device__ __forceinline__ void dropout_words_rows(uint32_t (&words)[NB], int I, int J0, uint32_t hs,
+                                                   uint32_t offset, uint32_t k0, uint32_t k1,
+                                                   int lane) {
+#pragma unroll
+    for (int r = 0; r < NB / 4; ++r) {
+        const Philox4 v = philox4x32_10(static_cast<uint32_t>(J0 + 4 * r + (lane & 3)),
+                                        static_cast<uint32_t>(I), hs, offset, k0, k1);
+        const uint32_t mine[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+        group_transpose4(mine, out, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) words[4 * r + u] = out[u];
+    }
+}
+
+// Rows are keys: per block I of the list, the 4 bytes of this key row (byte w =
+// query 4 I + w), gathered from the four words of the draw.
+template <int NB>
+__device__ __forceinline__ void dropout_words_cols(uint32_t (&words)[NB], int I0, int J, uint32_t hs,
+                                                   uint32_t offset, uint32_t k0, uint32_t k1,
+                                                   int lane) {
+#pragma unroll
+    for (int r = 0; r < NB / 4; ++r) {
+        const Philox4 v = philox4x32_10(static_cast<uint32_t>(J),
+                                        static_cast<uint32_t>(I0 + 4 * r + (lane & 3)), hs, offset,
+                                        k0, k1);
+        // byte k of words 0..3 packed: the bytes key 4 J + k needs from this block
+        uint32_t mine[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mine[k] = ((v.x >> (8 * k)) & 0xFFu) | (((v.y >> (8 * k)) & 0xFFu) << 8) |
+                      (((v.z >> (8 * k)) & 0xFFu) << 16) | (((v.w >> (8 * k)) & 0xFFu) << 24);
+        }
+        uint32_t out[4];
+        group_transpose4(mine, out, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) words[4 * r + u] = out[u];
+    }
+}
+
+// keep factor of byte b of a word: rscale if kept, else 0
+__device__ __forceinline__ float keep_factor(uint32_t word, int b, uint32_t thresh, float rscale) {
+    return ((word >> (8 * b)) & 0xFFu) >= thresh ? rscale : 0.f;
+}
+
 }  // namespace fa

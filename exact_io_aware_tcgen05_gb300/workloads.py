@@ -31,6 +31,7 @@ class Workload:
     backward: bool         # whether the workload includes the backward pass
     lengths: Optional[Tuple[int, ...]] = None   # packed batch: per-sequence lengths
     dtype: str = "bf16"    # element type of the 16-bit tensors: "bf16" or "f16"
+    p_drop: float = 0.0    # dropout probability of the attention probabilities (0: none)
 
     @property
     def scale(self) -> float:
@@ -108,10 +109,15 @@ WORKLOADS = {
                  True),
         Workload("fwdbwd_b2_h16_n8192_d128_causal_f16", 2, 16, 16, 8192, 128, True, 0, True,
                  dtype="f16"),
+        Workload("fwdbwd_b2_h16_n8192_d128_causal_dropout10", 2, 16, 16, 8192, 128, True, 0, True,
+                 p_drop=0.1),
         _varlen(128),
         _varlen(64),
     ]
 }
+
+#: dropout seed and offset of the workloads with p_drop > 0
+DROPOUT_SEED, DROPOUT_OFFSET = 0x5EED, 0
 
 #: the workload the benchmark times by default: long causal sequences, d = 128, fwd + bwd
 BENCH_DEFAULT = "fwdbwd_b2_h16_n8192_d128_causal"

@@ -129,6 +129,41 @@ fa_status fa_bwd_typed(fa_dtype dtype, const void* q, const void* k, const void*
                        size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Forward and backward with dropout on the attention probabilities.  The pages
+ * give dropout no semantics; this library defines them.  With P the softmax
+ * probabilities (computed before dropout, so LSE is that of fa_fwd),
+ *   O_i = sum_j Z_ij v_j,    Z_ij = P_ij * keep_ij * r,
+ * keep_ij in {0, 1}, r = 256 / (256 - t) and t = floor(256 * p_drop + 1/2) (in
+ * float; p_drop in [0, 1), t <= 255), so a pair is dropped with probability
+ * t / 256 and kept pairs are scaled to keep the expectation.  The backward pass
+ * is the gradient of that O for the same keep mask:
+ *   dV_j = sum_i Z_ij dO_i,  dP_ij = keep_ij * r * (dO_i . v_j),
+ *   dS_ij = P_ij (dP_ij - D_i) with D_i = dO_i . O_i, dQ and dK from dS as in fa_bwd.
+ * keep_ij comes from Philox4x32-10 (Salmon, Moraes, Dror, Shaw: "Parallel
+ * Random Numbers: As Easy as 1, 2, 3", SC 2011) with key (seed & 0xffffffff,
+ * seed >> 32): for query i and key j of sequence b (positions within the
+ * sequence) and query head h, the call with counter
+ *   (j / 4, i / 4, b * Hq + h, offset)
+ * returns four 32-bit words; byte (j % 4) (bits 8 (j%4) .. +7) of word (i % 4)
+ * is the pair's random byte, and keep_ij = (byte >= t).  fa_bwd_dropout must be
+ * called with the p_drop, seed and offset of the matching fa_fwd_dropout.
+ * p_drop == 0 gives exactly fa_fwd_typed / fa_bwd_typed.  Errors: p_drop
+ * outside [0, 1) is FA_ERR_INVALID_ARG, t == 256 FA_ERR_UNSUPPORTED; the rest
+ * as fa_fwd / fa_bwd.
+ */
+fa_status fa_fwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
+                         unsigned int offset, const void* q, const void* k, const void* v, void* o,
+                         float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                         const int* cu_seqlens, int total_tokens, float scale,
+                         cudaStream_t stream);
+fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
+                         unsigned int offset, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                         void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                         const int* cu_seqlens, int total_tokens, float scale, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Backward pass of fa_fwd for the loss gradient dO, recomputing S and P from
  * the saved logsumexp ("3. Recomputation in the Backward Pass"):
  *   D_i = dO_i . O_i,  P_ij = exp(S_ij - LSE_i),  dP_ij = dO_i . v_j,

@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_bwd_workspace_size",
-              "fa_last_error", "fa_device_status"):
+    for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
+              "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status"):
         assert n in names
 
 
@@ -111,3 +111,18 @@ def test_binding_fails_loudly_without_library(tmp_path):
             fa.load(str(tmp_path / "missing.so"))
     finally:
         fa._lib = saved
+
+
+def test_dropout_entry_points_reject_bad_probabilities(lib):
+    fa, _ = lib
+    for p in (-0.1, 1.0, float("nan")):
+        st = fa.fa_fwd_dropout(fa.FA_DTYPE_BF16, p, 1, 0, 16, 16, 16, 16, 16, 1, 2, 1, 128, 128,
+                               1, 0, None, 0, 0.125, None, check=False)
+        assert st == 1 and "p_drop" in fa.fa_last_error()
+    st = fa.fa_fwd_dropout(fa.FA_DTYPE_BF16, 0.999, 1, 0, 16, 16, 16, 16, 16, 1, 2, 1, 128, 128,
+                           1, 0, None, 0, 0.125, None, check=False)
+    assert st == 2
+    need = fa.fa_bwd_workspace_size(1, 2, 1, 128, 128, 0)
+    st = fa.fa_bwd_dropout(fa.FA_DTYPE_BF16, 1.5, 1, 0, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 1,
+                           128, 128, 1, 0, None, 0, 0.125, 256, need, None, check=False)
+    assert st == 1
