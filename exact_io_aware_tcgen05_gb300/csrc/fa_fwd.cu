@@ -59,6 +59,16 @@ struct FwdCfg {
     static constexpr int kSmemBytes = kTilesBytes + kBarBytes + 1024;  // + alignment slack
 };
 
+// Registers per thread: the kernel is built for 384 threads at 168 (one CTA per
+// SM); at the start the warpgroup of warps 0..3 (producer, issuer, relay, idle)
+// drops to kFwdRegsCtl and the two softmax warpgroups rise to kFwdRegsSoftmax,
+// which keeps a row of 128 scores and its P in registers without spilling.
+constexpr int kFwdRegsLaunch = 168;
+constexpr int kFwdRegsCtl = 152;
+constexpr int kFwdRegsSoftmax = 176;
+static_assert(128 * kFwdRegsCtl + 256 * kFwdRegsSoftmax <= 384 * kFwdRegsLaunch,
+              "register split exceeds the launch's registers");
+
 // named barrier of query tile t: kFwdBarP + t (0 is __syncthreads); softmax
 // warpgroup t + issuer warp + relay warp
 constexpr int kFwdBarP = 1;
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        regs_lower<kFwdRegsCtl>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
@@ -170,6 +181,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        regs_lower<kFwdRegsCtl>();
         // The whole warp walks the blocks (named barriers are warp-collective);
         // lane 0 issues.  No mbarrier wait and no look at the abort flag inside
         // the loop: after an abort it keeps issuing on stale data, so every
@@ -226,6 +238,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         if (lane == 0) mma_commit(smem_addr(&bars->o_full));
     } else if (warp == 2) {
         // ------------------------------------------------------ K/V relay
+        regs_lower<kFwdRegsCtl>();
         for (int j = 0; j < nkv; ++j) {
             if (lane == 0) {
                 for (int i = 2 * j + 1; i <= 2 * j + 2 && i < 2 * nkv; ++i)
@@ -235,8 +248,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             __syncwarp();
             for (int t = 0; t < kFwdQTiles; ++t) named_bar_sync(kFwdBarP + t, kFwdBarCount);
         }
+    } else if (warp == 3) {
+        regs_lower<kFwdRegsCtl>();   // idle; its warpgroup gives registers away
     } else if (warp >= 4) {
         // ------------------------------------------------- softmax + epilogue
+        regs_raise<kFwdRegsSoftmax>();
         const int t = (warp - 4) / 4;
         const int quad = warp % 4;
         const int r = quad * 32 + lane;               // row within the tile = TMEM lane
@@ -420,6 +436,15 @@ template <int D, int E, bool DROP>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D>;
     auto kern = fa_fwd_kernel<D, E, DROP>;
+    // the register split needs the launch's full 168 registers per thread: a
+    // build that gave the kernel fewer would make the softmax warps wait forever
+    static const cudaError_t regs_ok = [&] {
+        cudaFuncAttributes fa;
+        const cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        return fa.numRegs >= kFwdRegsLaunch ? cudaSuccess : cudaErrorInvalidKernelImage;
+    }();
+    if (regs_ok != cudaSuccess) return regs_ok;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -196,6 +196,26 @@ __device__ __forceinline__ uint64_t make_l2_policy_evict_first() {
     return p;
 }
 
+// ------------------------------------------------------- register budgets
+//
+// setmaxnreg: every warp of a warpgroup lowers (or raises) its per-thread
+// register count to N together, moving registers between the warpgroups of a
+// CTA.  A raise waits until the registers are free, so the counts summed over
+// the CTA's threads must not exceed what the launch reserved (threads x the
+// kernel's register count); the launcher checks the kernel's count.
+
+template <int N>
+__device__ __forceinline__ void regs_lower() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void regs_raise() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // TMEM allocation: executed by one full warp; the base address is written to
