@@ -97,6 +97,14 @@ struct BwdCfg {
     static constexpr int kEwThreads = 128 * kEwWG;
     static constexpr int kThreads = 128 + kEwThreads;   // warp 0 TMA, warp 1 MMA, warp 2 relay, warps 4.. element-wise
     static constexpr int kBarCount = kEwThreads + 64;   // named barriers: element-wise + issuer + relay warps
+    // registers per thread: the launch reserves kRegsLaunch for every thread (one CTA
+    // per SM); the warpgroup of warps 0..3 then drops to kRegsCtl and the
+    // element-wise warpgroups rise to kRegsEw (setmaxnreg)
+    static constexpr int kRegsLaunch = (65536 / kThreads) & ~7;
+    static constexpr int kRegsCtl = (D == 128) ? 152 : 64;
+    static constexpr int kRegsEw = (D == 128) ? 176 : 104;
+    static_assert(128 * kRegsCtl + kEwThreads * kRegsEw <= kThreads * kRegsLaunch,
+                  "register split exceeds the launch's registers");
     static constexpr int kTmemCols = 512;
     static constexpr int kColS = 0;          // S (or S^T), 128 fp32 columns
     static constexpr int kColDP = 128;       // dP (or dP^T), 128 fp32 columns
@@ -406,6 +414,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
+        regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ producer
         if (lane == 0) {
             const uint32_t rb = smem_addr(&bars->res_full);
@@ -423,6 +432,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                             abort_flag, p);
         }
     } else if (warp == 1) {
+        regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ MMA issuer
         // The whole warp walks the step sequence (the named barriers are
         // warp-collective); lane 0 issues.  It never waits on an mbarrier inside
@@ -471,6 +481,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
         }
         if (lane == 0) mma_commit(smem_addr(&bars->acc_full));
     } else if (warp == 2) {
+        regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ slot relay
         // Waits for the streamed tiles the next products read and passes that on
         // through the issuer's named barriers.
@@ -487,7 +498,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             __syncwarp();
             named_bar_sync(kBarDS0, C::kBarCount);
         }
+    } else if (warp == 3) {
+        regs_lower<C::kRegsCtl>();   // idle; its warpgroup gives registers away
     } else if (warp >= 4) {
+        regs_raise<C::kRegsEw>();
         // ------------------------------------------- element-wise + epilogue
         constexpr int W = C::kEwCols;
         const int wg = (warp - 4) / 4;      // query columns [W wg, W wg + W) of each tile
@@ -690,6 +704,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
+        regs_lower<C::kRegsCtl>();
         if (lane == 0) {
             const uint32_t rb = smem_addr(&bars->res_full);
             mbar_arrive_expect_tx(rb, 2 * C::kTileBytes);
@@ -705,6 +720,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                             abort_flag, p);
         }
     } else if (warp == 1) {
+        regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ MMA issuer
         // (whole warp walks the tiles, lane 0 issues; as in the dK/dV kernel it
         // never waits on an mbarrier inside the loop)
@@ -749,6 +765,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         }
         if (lane == 0) mma_commit(smem_addr(&bars->acc_full));
     } else if (warp == 2) {
+        regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ slot relay
         for (int j = 0; j < nk; ++j) {
             if (lane == 0 && j + 1 < nk) {
@@ -760,7 +777,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             named_bar_sync(kBarP, C::kBarCount);
             named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);
         }
+    } else if (warp == 3) {
+        regs_lower<C::kRegsCtl>();   // idle; its warpgroup gives registers away
     } else if (warp >= 4) {
+        regs_raise<C::kRegsEw>();
         constexpr int W = C::kEwCols;
         const int wg = (warp - 4) / 4;      // key columns [W wg, W wg + W) of each tile
         const int quad = warp % 4;
@@ -871,6 +891,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     teardown_bwd_cta<D>(bars, warp);
 }
 
+// The register split inside the tensor-core kernels needs the launch's full
+// per-thread count: a build that gave a kernel fewer would make its element-wise
+// warps wait forever, so such a kernel is refused.
+template <typename K>
+cudaError_t check_regs(K kern, int need) {
+    cudaFuncAttributes fa;
+    const cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+    if (r != cudaSuccess) return r;
+    return fa.numRegs >= need ? cudaSuccess : cudaErrorInvalidKernelImage;
+}
+
 template <typename K>
 cudaError_t launch_tc(K kern, int grid, int threads, int smem, const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -900,6 +931,8 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream
 
 template <int D, int E, bool DROP>
 cudaError_t launch_bwd_dkdv_d(const BwdParams& p, cudaStream_t stream) {
+    static const cudaError_t regs_ok = check_regs(fa_bwd_dkdv_kernel<D, E, DROP>, BwdCfg<D>::kRegsLaunch);
+    if (regs_ok != cudaSuccess) return regs_ok;
     return launch_tc(fa_bwd_dkdv_kernel<D, E, DROP>, p.num_work_dkdv, BwdCfg<D>::kThreads,
                      BwdCfg<D>::kSmemBytes, p, stream);
 }
@@ -938,6 +971,8 @@ cudaError_t launch_dependent(K kern, int grid, int threads, int smem, const BwdP
 
 template <int D, int E, bool DROP>
 cudaError_t launch_bwd_dq_d(const BwdParams& p, cudaStream_t stream) {
+    static const cudaError_t regs_ok = check_regs(fa_bwd_dq_kernel<D, E, DROP>, BwdCfg<D>::kRegsLaunch);
+    if (regs_ok != cudaSuccess) return regs_ok;
     return launch_dependent(fa_bwd_dq_kernel<D, E, DROP>, p.num_work_dq, BwdCfg<D>::kThreads,
                             BwdCfg<D>::kSmemBytes, p, stream);
 }
