@@ -529,6 +529,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             return r < W ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
         };
         float next_stat = fetch_stat(0);
+        // Dropout bytes of this key row for the current step, 4 queries a word.  They
+        // do not depend on the products, so the next step's are drawn at the end of
+        // each step, while the tensor cores work on that step's S^T.
+        uint32_t dw[DROP ? W / 4 : 1];
+        auto draw = [&](int n) {
+            dropout_words_cols<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw),
+                                      ((qt_first + n % nq) * kBlockM + W * wg) >> 2, kpos >> 2,
+                                      static_cast<uint32_t>(b * s.Hq + g * s.group + n / nq),
+                                      p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
+        };
+        if (DROP) draw(0);
         // `ok` turns false (warp-uniformly) when a wait gives up; the warp then
         // skips the work but keeps taking part in every named-barrier phase,
         // blocking (bar.sync) instead of arriving so it cannot run a phase ahead.
@@ -553,13 +564,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             // inverse keep probability in its epilogue)
             if (ok) ok = warp_wait(smem_addr(&bars->s_full), n & 1, abort_flag, p.timeout_cycles, p.status);
             float pv[W];
-            uint32_t dw[DROP ? W / 4 : 1];   // dropout bytes of this key row, 4 queries a word
             if (ok) {
                 tc_fence_after();
-                if (DROP)
-                    dropout_words_cols<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q0 >> 2, kpos >> 2,
-                                              static_cast<uint32_t>(b * s.Hq + g * s.group + n / nq),
-                                              p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
                 tmem_ldw<W>(tS, pv);
 #pragma unroll
                 for (int c4 = 0; c4 < W / 4; ++c4) {
@@ -617,6 +623,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                 tc_fence_before();
             }
             named_bar_signal(kBarDS0, C::kBarCount, ok);
+            if (DROP && ok && n + 1 < nsteps) draw(n + 1);
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
@@ -800,6 +807,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
         const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndlt2 = f2_pack(-dlt, -dlt);
         const int lo_q = key_lo(s, q), hi_q = valid ? key_hi(s, q, len) : -1;
+        // dropout bytes of this query row for the current key tile, 4 keys a word; as in
+        // the dK/dV kernel the next tile's are drawn at the end of each step
+        uint32_t dw[DROP ? W / 4 : 1];
+        auto draw = [&](int j) {
+            dropout_words_rows<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q >> 2,
+                                      ((kt_first + j) * kBlockN + W * wg) >> 2,
+                                      static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
+                                      p.drop.seed_lo, p.drop.seed_hi, lane);
+        };
+        if (DROP) draw(0);
         // `ok`: as in the dK/dV kernel, a warp that gave up keeps taking part in
         // every named-barrier phase
         bool ok = true;
@@ -809,7 +826,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             const int clo = lo_q - kc, chi = hi_q - kc;
             if (ok) ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles, p.status);
             float pv[W];
-            uint32_t dw[DROP ? W / 4 : 1];   // dropout bytes of this query row, 4 keys a word
             if (ok) {
                 tc_fence_after();
                 tmem_ldw<W>(tS, pv);
@@ -828,10 +844,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                     for (int c = 0; c < W; ++c)
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
-                if (DROP)
-                    dropout_words_rows<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q >> 2, kc >> 2,
-                                              static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
-                                              p.drop.seed_lo, p.drop.seed_hi, lane);
                 ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
                                p.timeout_cycles, p.status);
             }
@@ -858,6 +870,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 tc_fence_before();
             }
             named_bar_signal((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount, ok);
+            if (DROP && ok && j + 1 < nk) draw(j + 1);
         }
         if (ok)
             ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);

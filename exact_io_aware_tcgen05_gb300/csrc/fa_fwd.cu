@@ -57,6 +57,11 @@ struct FwdCfg {
     static constexpr int kTilesBytes = (kFwdQTiles + kStages) * kTileBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kTilesBytes + kBarBytes + 1024;  // + alignment slack
+    // dropout only: the random words of each softmax row for its next key block
+    // (32 words per row of 128 keys), after the barrier block
+    static constexpr int kDropBytes = kFwdQTiles * kBlockM * (kBlockN / 4) * 4;
+    static constexpr int kSmemBytesDrop = kSmemBytes + kDropBytes;
+    static_assert(kSmemBytesDrop <= 232448, "shared memory per CTA");
 };
 
 // Registers per thread: the kernel is built for 384 threads at 168 (one CTA per
@@ -267,6 +272,23 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const float sl2 = p.scale_log2;
         const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h);   // dropout counter word
 
+        // Dropout: the Philox words of a key block do not depend on the scores, so each
+        // row draws those of its next block right after handing P over, while the tensor
+        // cores compute that block's scores, and parks them in shared memory (its own
+        // 128-byte row; 16-byte chunks XOR-swizzled by the row so that a warp's
+        // accesses spread over the banks).
+        uint4* drop_row = reinterpret_cast<uint4*>(smem + C::kTilesBytes + C::kBarBytes) +
+                          (t * kBlockM + r) * (kBlockN / 16);
+        auto draw_block = [&](int jj) {
+            uint32_t dw[kBlockN / 4];
+            dropout_words_rows<kBlockN / 4>(dw, q >> 2, ((kv_first + jj) * kBlockN) >> 2, hs,
+                                            p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
+#pragma unroll
+            for (int c = 0; c < kBlockN / 16; ++c)
+                drop_row[c ^ (r & 7)] = make_uint4(dw[4 * c], dw[4 * c + 1], dw[4 * c + 2], dw[4 * c + 3]);
+        };
+        if (DROP) draw_block(0);
+
         float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
         float l = 0.f;
         // `ok` turns false (warp-uniformly: the TMEM accesses are warp-collective)
@@ -326,10 +348,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     // ones (the 1 / keep-probability factor is applied to O in fp32 at the
                     // end, so the 16-bit P carries no extra rounding)
                     uint32_t dw[DROP ? 16 : 1];
-                    if (DROP)
-                        dropout_words_rows<16>(*reinterpret_cast<uint32_t(*)[16]>(dw), q >> 2,
-                                               (kb + 64 * half) >> 2, hs, p.drop.offset,
-                                               p.drop.seed_lo, p.drop.seed_hi, lane);
+                    if (DROP) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = drop_row[(4 * half + c) ^ (r & 7)];
+                            dw[(4 * c) % (DROP ? 16 : 1)] = v.x;
+                            dw[(4 * c + 1) % (DROP ? 16 : 1)] = v.y;
+                            dw[(4 * c + 2) % (DROP ? 16 : 1)] = v.z;
+                            dw[(4 * c + 3) % (DROP ? 16 : 1)] = v.w;
+                        }
+                    }
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int k = 64 * half + 2 * c;
@@ -367,6 +395,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 tc_fence_before();
             }
             named_bar_signal(kFwdBarP + t, kFwdBarCount, ok);
+            if (DROP && ok && j + 1 < nkv) draw_block(j + 1);
         }
         // ------------------------------------------------------------ epilogue
         if (ok)
@@ -445,10 +474,10 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
         return fa.numRegs >= kFwdRegsLaunch ? cudaSuccess : cudaErrorInvalidKernelImage;
     }();
     if (regs_ok != cudaSuccess) return regs_ok;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    constexpr int smem = DROP ? C::kSmemBytesDrop : C::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<p.num_work, C::kThreads, C::kSmemBytes, stream>>>(p);
+    kern<<<p.num_work, C::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -513,8 +513,10 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
             k0 += kW0;
             k1 += kW1;
         }
-        const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
-        const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
+        // one 32 x 32 -> 64-bit product each (its high and low words)
+        const uint64_t m0 = static_cast<uint64_t>(kM0) * c0, m1 = static_cast<uint64_t>(kM1) * c2;
+        const uint32_t hi0 = static_cast<uint32_t>(m0 >> 32), lo0 = static_cast<uint32_t>(m0);
+        const uint32_t hi1 = static_cast<uint32_t>(m1 >> 32), lo1 = static_cast<uint32_t>(m1);
         const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
         c0 = n0;
         c1 = lo1;
@@ -543,13 +545,25 @@ __device__ __forceinline__ uint32_t pick4(const Philox4& v, int i) {
 // of the round, one 32-bit word with the 4 bytes of its own row.
 __device__ __forceinline__ void group_transpose4(const uint32_t (&mine)[4], uint32_t (&out)[4],
                                                  int lane) {
-    const int a = lane & 3, base = lane & ~3;
-    out[a] = mine[a];
+    // Two butterfly stages over the 4 x 4 block (lane a holds row a, wants column
+    // a): first with lane a ^ 1 on the entries whose index differs from a in bit 0,
+    // then with lane a ^ 2 on bit 1.  Constant register indices only, so nothing
+    // goes to local memory.
+    const bool b0 = lane & 1, b1 = lane & 2;
+    uint32_t u[4];
 #pragma unroll
-    for (int s = 1; s < 4; ++s) {
-        const uint32_t send = mine[(a + s) & 3];
-        const int src = (a - s) & 3;
-        out[src] = __shfl_sync(0xffffffffu, send, base | src);
+    for (int pr = 0; pr < 2; ++pr) {
+        const uint32_t lo = mine[2 * pr], hi = mine[2 * pr + 1];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, b0 ? lo : hi, 1);
+        u[2 * pr] = b0 ? got : lo;
+        u[2 * pr + 1] = b0 ? hi : got;
+    }
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+        const uint32_t lo = u[pr], hi = u[pr + 2];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, b1 ? lo : hi, 2);
+        out[pr] = b1 ? got : lo;
+        out[pr + 2] = b1 ? hi : got;
     }
 }
 
@@ -582,11 +596,13 @@ __device__ __forceinline__ void dropout_words_cols(uint32_t (&words)[NB], int I0
                                         static_cast<uint32_t>(I0 + 4 * r + (lane & 3)), hs, offset,
                                         k0, k1);
         // byte k of words 0..3 packed: the bytes key 4 J + k needs from this block
+        // (byte permutes: bytes k of x and y, bytes k of z and w, then the two pairs)
         uint32_t mine[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            mine[k] = ((v.x >> (8 * k)) & 0xFFu) | (((v.y >> (8 * k)) & 0xFFu) << 8) |
-                      (((v.z >> (8 * k)) & 0xFFu) << 16) | (((v.w >> (8 * k)) & 0xFFu) << 24);
+            const uint32_t xy = __byte_perm(v.x, v.y, k | ((k + 4) << 4));
+            const uint32_t zw = __byte_perm(v.z, v.w, k | ((k + 4) << 4));
+            mine[k] = __byte_perm(xy, zw, 0x5410);
         }
         uint32_t out[4];
         group_transpose4(mine, out, lane);
