@@ -1,0 +1,181 @@
+"""Pins of the fp8 (e4m3) oracle against the format's definition, brute force,
+closed forms and the bf16 oracle (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import fp8
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ------------------------------------------------------------------ e4m3
+
+def test_decode_known_codes():
+    # values fixed by the format: sign | 4-bit exponent (bias 7) | 3-bit mantissa
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x30: 0.5, 0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x44: 3.0,
+             0x78: 256.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = fp8.e4m3_decode(np.array(list(known), np.uint8))
+    assert np.array_equal(got, np.array(list(known.values())))
+    assert np.isnan(fp8.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_decode_monotone_and_symmetric():
+    pos = fp8.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)
+    neg = fp8.e4m3_decode(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.array_equal(neg, -pos)
+
+
+def _brute_encode(x: float) -> int:
+    """Nearest finite e4m3 value by exhaustive search; ties to the even code."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = fp8.e4m3_decode(codes)
+    if abs(x) > 448.0:
+        return 0x7E | (0x80 if x < 0 else 0)
+    dist = np.abs(vals - x)
+    best = np.flatnonzero(dist == dist.min())
+    cand = [int(codes[i]) for i in best]
+    # the same magnitude twice (+-0) or a tie between neighbours: keep the sign of x, even mantissa
+    cand = [c for c in cand if (c >> 7) == (1 if np.signbit(x) else 0)] or cand
+    even = [c for c in cand if (c & 1) == 0]
+    return (even or cand)[0]
+
+
+def test_encode_matches_brute_force():
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([rng.standard_normal(300) * 3, rng.standard_normal(200) * 0.01,
+                         rng.uniform(-500, 500, 100),
+                         # exact ties: midpoints between neighbouring values
+                         (fp8.e4m3_decode(np.arange(0, 0x7E, dtype=np.uint8)) +
+                          fp8.e4m3_decode(np.arange(1, 0x7F, dtype=np.uint8))) / 2])
+    got = fp8.e4m3_encode(xs)
+    want = np.array([_brute_encode(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_encode_round_trip_and_specials():
+    c = np.arange(256, dtype=np.uint8)
+    v = fp8.e4m3_decode(c)
+    ok = ~np.isnan(v)
+    assert np.array_equal(fp8.e4m3_encode(v[ok]), c[ok])
+    assert fp8.e4m3_encode([np.nan])[0] == 0x7F
+    assert list(fp8.e4m3_encode([464.0, 1e9, -1e9])) == [0x7E, 0x7E, 0xFE]
+
+
+# --------------------------------------------------------------- quantise
+
+def _bf16(x):
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_quantize_qk_block_properties():
+    rng = np.random.default_rng(1)
+    B, N, H, d = 2, 300, 3, 16
+    x = _bf16(rng.standard_normal((B, N, H, d)) * 2)
+    codes, scales = fp8.quantize_qk(x, B, N)
+    xf = oracle.to_f64(x)
+    nb = -(-N // 128)
+    assert scales.shape == (H, B * nb)
+    for b in range(B):
+        for kb in range(nb):
+            r = slice(kb * 128, min(N, kb * 128 + 128))
+            for h in range(H):
+                blk, s = xf[b, r, h], float(scales[h, b * nb + kb])
+                assert s == float(np.float32(np.abs(blk).max()) / np.float32(448.0))
+                dq = fp8.e4m3_decode(codes[b, r, h]) * s
+                # the largest magnitude maps to +-448; every value within half a step
+                assert np.max(np.abs(fp8.e4m3_decode(codes[b, r, h]))) == 448.0
+                step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(np.abs(blk) / s, 1e-30))), -6) - 3)
+                assert np.all(np.abs(dq - blk) <= 0.5 * step * s * (1 + 1e-6) + 1e-30)
+
+
+def test_quantize_qk_varlen_offsets_and_zero_block():
+    cu = [0, 5, 5 + 130, 5 + 130 + 128]                  # lengths 5, 130, 128
+    T, H, d = cu[-1], 2, 8
+    x = np.zeros((T, H, d), np.float32)
+    x[0:5] = 1.5                                         # sequence 0, one block
+    x[5:133] = -3.0                                      # sequence 1, block 0
+    # sequence 1 block 1 (2 tokens) stays zero; sequence 2 (one block)
+    x[135:] = 0.25
+    codes, scales = fp8.quantize_qk(_bf16(x), 3, 0, cu_seqlens=cu, nb=6)
+    offs, total = fp8.block_offsets(3, 0, cu)
+    assert offs == [0, 1, 3] and total == 4
+    assert scales.shape == (H, 6)
+    assert np.allclose(scales[:, 0], np.float32(1.5) / np.float32(448))
+    assert np.allclose(scales[:, 1], np.float32(3.0) / np.float32(448))
+    assert np.all(scales[:, 2] == 1.0) and np.all(codes[133:135] == 0)   # all-zero block
+    assert np.allclose(scales[:, 3], np.float32(0.25) / np.float32(448))
+    assert np.all(scales[:, 4:] == 1.0)                  # columns past the blocks untouched
+
+
+def test_quantize_v_transposed_padded():
+    rng = np.random.default_rng(2)
+    cu = [0, 3, 3 + 129]
+    T, H, d = cu[-1], 2, 8
+    v = _bf16(rng.standard_normal((T, H, d)))
+    vt, scales = fp8.quantize_v(v, 2, 0, cu_seqlens=cu)
+    offs, total = fp8.vt_offsets(2, 0, cu)
+    assert offs == [0, 128] and total == 128 + 256 and vt.shape == (H, d, total)
+    assert np.all(vt[:, :, 3:128] == 0) and np.all(vt[:, :, 128 + 129:] == 0)
+    vf = oracle.to_f64(v)
+    for b, (s0, L) in enumerate([(0, 3), (3, 129)]):
+        for h in range(H):
+            assert scales[h, b] == np.float32(np.abs(vf[s0:s0 + L, h]).max()) / np.float32(448)
+            code_rows = vt[h, :, offs[b]:offs[b] + L].T           # [L, d]
+            want = fp8.e4m3_encode((vf[s0:s0 + L, h].astype(np.float32) /
+                                    np.float32(scales[h, b])).astype(np.float64))
+            assert np.array_equal(code_rows, want)
+    back = fp8.dequantize_v(vt, scales, 2, 0, cu_seqlens=cu)
+    assert np.max(np.abs(back - vf)) <= 2.0 ** -4 * np.abs(vf).max() + 1e-12
+
+
+# ---------------------------------------------------------------- forward
+
+def test_fp8_forward_reduces_to_bf16_oracle_on_representable_inputs():
+    # every block contains +-448 and only e4m3 values, so every scale is 1 and the
+    # dequantised inputs equal the inputs: the fp8 oracle must equal the plain one
+    rng = np.random.default_rng(3)
+    B, N, H, d = 1, 200, 2, 16
+    grid = fp8.e4m3_decode(np.arange(0x30, 0x48, dtype=np.uint8))   # 0.5 .. 3.75
+    def draw(shape):
+        x = rng.choice(grid, size=shape) * rng.choice([-1.0, 1.0], size=shape)
+        x[:, ::128, :, 0] = 448.0
+        return x
+    q, k, v = draw((B, N, H, d)), draw((B, N, H, d)), draw((B, N, H, d))
+    v[:, 0, :, 0] = 448.0
+    q8, qs = fp8.quantize_qk(q, B, N)
+    k8, ks = fp8.quantize_qk(k, B, N)
+    vt8, vs = fp8.quantize_v(v, B, N)
+    assert np.all(qs == 1.0) and np.all(ks == 1.0) and np.all(vs == 1.0)
+    scale = 1.0 / 448.0
+    o8, l8 = fp8.attention_fwd(q8, qs, k8, ks, vt8, vs, B=B, N=N, causal=True, window=0, scale=scale)
+    o, l = oracle.attention_fwd(q, k, v, causal=True, window=0, scale=scale)
+    assert np.array_equal(o8, o) and np.array_equal(l8, l)
+
+
+def _simulated_kernel_o(q, k, v, causal, scale, shift):
+    """O as the kernel forms it: p = exp(S - m + shift) (a reference below the max),
+    p rounded to e4m3 for P V, divided by the unrounded sum."""
+    L = k.shape[0]
+    s = scale * q @ k.T
+    vis = np.tril(np.ones((L, L), bool)) if causal else np.ones((L, L), bool)
+    s = np.where(vis, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m + shift)
+    pq = fp8.e4m3_decode(fp8.e4m3_encode(p))
+    return (pq @ v) / p.sum(axis=1, keepdims=True)
+
+
+def test_o_error_bound_covers_simulated_rounding():
+    rng = np.random.default_rng(4)
+    L, d = 96, 16
+    q, k, v = (rng.standard_normal((L, d)) * 1.5 for _ in range(3))
+    scale = d ** -0.5
+    o, lse = oracle.fwd_group(q[None], k, v, True, 0, scale)
+    bound = fp8.o_error_bound(q, k, v, lse[0], causal=True, window=0, scale=scale, rows=np.arange(L))
+    for shift in (0.0, 2.0, 5.5):            # the kernel's reference sits up to 8 log2 units low
+        err = np.abs(_simulated_kernel_o(q, k, v, True, scale, shift) - o[0])
+        assert np.all(err <= bound)
+        assert err.max() > 0                 # the rounding is visible, the bound not vacuous
