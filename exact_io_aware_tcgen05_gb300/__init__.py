@@ -20,6 +20,8 @@ __all__ = [
     "FAError", "load", "fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
     "fa_bwd_dropout", "fa_bwd_workspace_size",
     "fa_bwd_static_workspace", "FA_DTYPE_BF16", "FA_DTYPE_F16",
+    "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
+    "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
     "library_path",
@@ -72,6 +74,17 @@ def load(path: str | None = None):
     lib.fa_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
                                             _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
     lib.fa_bwd_static_workspace.restype = _i
+    lib.fa_fp8_scale_blocks.argtypes = [_i, _i, _i, _i]
+    lib.fa_fp8_scale_blocks.restype = _i
+    lib.fa_fp8_vt_tokens.argtypes = [_i, _i, _i, _i]
+    lib.fa_fp8_vt_tokens.restype = _i
+    lib.fa_fp8_quantize_qk.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]
+    lib.fa_fp8_quantize_qk.restype = _i
+    lib.fa_fp8_quantize_v.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]
+    lib.fa_fp8_quantize_v.restype = _i
+    lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _i, _i,
+                               _i, _i, _vp, _i, _f, _vp]
+    lib.fa_fwd_fp8.restype = _i
     lib.fa_device_status.argtypes = [_vp]
     lib.fa_device_status.restype = _i
     lib.fa_set_wait_limit_cycles.argtypes = [_ll]
@@ -231,6 +244,49 @@ def fa_set_wait_limit_cycles(cycles: int) -> None:
 
 # ------------------------------------------------------------ conveniences
 
+def fa_fp8_scale_blocks(B, N, total_tokens, packed) -> int:
+    """Columns of the fp8 block-scale arrays (see include/fa.h)."""
+    return int(load().fa_fp8_scale_blocks(B, N, int(total_tokens), int(bool(packed))))
+
+
+def fa_fp8_vt_tokens(B, N, total_tokens, packed) -> int:
+    """Columns of the transposed fp8 V (see include/fa.h)."""
+    return int(load().fa_fp8_vt_tokens(B, N, int(total_tokens), int(bool(packed))))
+
+
+def fa_fp8_quantize_qk(x, x8, scales, nb, B, H, N, d, cu_seqlens, total_tokens, stream=None,
+                       check: bool = True) -> int:
+    """bf16 Q or K -> e4m3 codes and per-block scales."""
+    st = load().fa_fp8_quantize_qk(_ptr(x), _ptr(x8), _ptr(scales), int(nb), B, H, N, d,
+                                   _ptr(cu_seqlens), int(total_tokens), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_fp8_quantize_v(v, vt8, scales, vt_tokens, B, H, N, d, cu_seqlens, total_tokens, stream=None,
+                      check: bool = True) -> int:
+    """bf16 V -> transposed e4m3 codes and per-(sequence, head) scales."""
+    st = load().fa_fp8_quantize_v(_ptr(v), _ptr(vt8), _ptr(scales), int(vt_tokens), B, H, N, d,
+                                  _ptr(cu_seqlens), int(total_tokens), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def fa_fwd_fp8(q8, q_scale, k8, k_scale, vt8, v_scale, nb, vt_tokens, o, lse, B, Hq, Hkv, N, d,
+               causal, window, cu_seqlens, total_tokens, scale, stream=None,
+               check: bool = True) -> int:
+    """The fp8 forward (see include/fa.h)."""
+    st = load().fa_fwd_fp8(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(vt8),
+                           _ptr(v_scale), int(nb), int(vt_tokens), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                           N, d, int(bool(causal)), int(window), _ptr(cu_seqlens),
+                           int(total_tokens), float(scale), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
 def _geometry(q, k, cu_seqlens, max_seqlen):
     if cu_seqlens is None:
         B, N, Hq, d = q.shape
@@ -271,6 +327,54 @@ def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens
     else:
         fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T,
                      scale, stream)
+    return o, lse
+
+
+class Fp8Operands(tuple):
+    """(q8, q_scale, k8, k_scale, vt8, v_scale, nb, vt_tokens) of :func:`quantize_fp8`."""
+    __slots__ = ()
+    _fields = ("q8", "q_scale", "k8", "k_scale", "vt8", "v_scale", "nb", "vt_tokens")
+
+    def __getattr__(self, name):
+        return self[self._fields.index(name)]
+
+
+def quantize_fp8(q, k, v, *, cu_seqlens=None, max_seqlen=None, stream=None) -> Fp8Operands:
+    """e4m3 operands of the fp8 forward from bf16 CUDA tensors q, k, v (allocates them)."""
+    import torch
+    if {q.dtype, k.dtype, v.dtype} != {torch.bfloat16}:
+        raise TypeError("quantize_fp8 takes bfloat16 q, k, v")
+    B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
+    packed = cu_seqlens is not None
+    nb = fa_fp8_scale_blocks(B, N, T, packed)
+    vt_tokens = fa_fp8_vt_tokens(B, N, T, packed)
+    dev = q.device
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    vt8 = torch.empty((Hkv, d, vt_tokens), dtype=torch.uint8, device=dev)
+    qs = torch.empty((Hq, nb), dtype=torch.float32, device=dev)
+    ks = torch.empty((Hkv, nb), dtype=torch.float32, device=dev)
+    vs = torch.empty((Hkv, B), dtype=torch.float32, device=dev)
+    stream = stream if stream is not None else torch.cuda.current_stream(dev)
+    fa_fp8_quantize_qk(q, q8, qs, nb, B, Hq, N, d, cu_seqlens, T, stream)
+    fa_fp8_quantize_qk(k, k8, ks, nb, B, Hkv, N, d, cu_seqlens, T, stream)
+    fa_fp8_quantize_v(v, vt8, vs, vt_tokens, B, Hkv, N, d, cu_seqlens, T, stream)
+    return Fp8Operands((q8, qs, k8, ks, vt8, vs, nb, vt_tokens))
+
+
+def attention_forward_fp8(ops: Fp8Operands, *, causal=False, window=0, scale=None,
+                          cu_seqlens=None, max_seqlen=None, stream=None):
+    """O (bf16), LSE of the fp8 forward on :func:`quantize_fp8` operands (allocates outputs)."""
+    import torch
+    q8, qs, k8, ks, vt8, vs, nb, vt_tokens = ops
+    B, N, Hq, Hkv, d, T = _geometry(q8, k8, cu_seqlens, max_seqlen)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((Hq, T) if cu_seqlens is not None else (B, Hq, N), dtype=torch.float32,
+                      device=q8.device)
+    stream = stream if stream is not None else torch.cuda.current_stream(q8.device)
+    fa_fwd_fp8(q8, qs, k8, ks, vt8, vs, nb, vt_tokens, o, lse, B, Hq, Hkv, N, d, causal, window,
+               cu_seqlens, T, scale, stream)
     return o, lse
 
 

@@ -456,3 +456,194 @@ fa_status fa_device_status(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ fp8 forward
+
+namespace fa {
+namespace {
+
+// [tokens, heads, d] e4m3 viewed as (d, heads, tokens); the box is one 128-byte row
+// of d (d = 128) x 1 head x 128 tokens.
+fa_status make_u8_token_map(CUtensorMap* map, const void* base, int tokens, int heads, int d,
+                            const char* name) {
+    auto enc = encode_fn();
+    if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads) * d};
+    cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(kBlockM)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                    static_cast<int>(r));
+    return FA_OK;
+}
+
+// V^T [heads, d, vt_tokens] e4m3 viewed as (vt_tokens, d, heads); the box is 128 keys
+// (one 128-byte row) x 128 rows of d x 1 head.
+fa_status make_vt_map(CUtensorMap* map, const void* base, int vt_tokens, int d, int heads) {
+    auto enc = encode_fn();
+    if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(vt_tokens), static_cast<cuuint64_t>(d),
+                          static_cast<cuuint64_t>(heads)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(vt_tokens),
+                             static_cast<cuuint64_t>(d) * vt_tokens};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(d), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(vt) failed with CUresult %d",
+                    static_cast<int>(r));
+    return FA_OK;
+}
+
+// Upper bound on the 128-token blocks of all sequences: exact for dense batches;
+// packed: sum_b ceil(len_b / 128) <= ceil(T / 128) + B and <= B ceil(N / 128).
+long long fp8_blocks(int B, int N, int total_tokens, bool packed) {
+    const long long dense = static_cast<long long>(B) * ((static_cast<long long>(N) + 127) / 128);
+    if (!packed) return dense;
+    const long long bound = (static_cast<long long>(total_tokens) + 127) / 128 + B;
+    return bound < dense ? bound : dense;
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+fa_status fp8_geometry(int B, int H, int N, int d, const int* cu_seqlens, int total_tokens,
+                       const char* who, Geometry* g) {
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: head dim %d not in {64, 128}", who, d);
+    return check_common(B, H, H, N, d, 0, 0, cu_seqlens, total_tokens, 1.f, g);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fp8_scale_blocks(int B, int N, int total_tokens, int packed) {
+    if (B < 1 || N < 1 || total_tokens < 0) return 0;
+    const long long nb = fa::fp8_blocks(B, N, total_tokens, packed != 0);
+    return nb > INT_MAX ? 0 : static_cast<int>(nb);
+}
+
+int fa_fp8_vt_tokens(int B, int N, int total_tokens, int packed) {
+    if (B < 1 || N < 1 || total_tokens < 0) return 0;
+    const long long t = 128 * fa::fp8_blocks(B, N, total_tokens, packed != 0);
+    return t > INT_MAX / 2 ? 0 : static_cast<int>(t);
+}
+
+fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scales, int nb, int B, int H, int N,
+                             int d, const int* cu_seqlens, int total_tokens, cudaStream_t stream) {
+    using namespace fa;
+    t_last_error[0] = '\0';
+    if (!x || !x8 || !scales)
+        return fail(FA_ERR_INVALID_ARG, "fa_fp8_quantize_qk: x, x8 and scales must be non-null");
+    if (!aligned16(x) || !aligned16(x8) || !aligned4(scales))
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_fp8_quantize_qk: x and x8 must be 16-byte aligned, scales 4-byte aligned");
+    Geometry g;
+    fa_status st = fp8_geometry(B, H, N, d, cu_seqlens, total_tokens, "fa_fp8_quantize_qk", &g);
+    if (st != FA_OK) return st;
+    if (nb < fp8_blocks(B, N, g.tokens, cu_seqlens != nullptr))
+        return fail(FA_ERR_INVALID_ARG, "fa_fp8_quantize_qk: nb = %d below fa_fp8_scale_blocks", nb);
+    if (g.tokens == 0) return FA_OK;
+    Fp8QuantParams p{};
+    p.seq = g.seq;
+    p.x = x;
+    p.out = x8;
+    p.scales = scales;
+    p.heads = H;
+    p.nb = nb;
+    const cudaError_t e = launch_fp8_quant_qk(p, d, num_blocks(g, kBlockM, H), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_qk launch");
+    return FA_OK;
+}
+
+fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_tokens, int B, int H,
+                            int N, int d, const int* cu_seqlens, int total_tokens,
+                            cudaStream_t stream) {
+    using namespace fa;
+    t_last_error[0] = '\0';
+    if (!v || !vt8 || !scales)
+        return fail(FA_ERR_INVALID_ARG, "fa_fp8_quantize_v: v, vt8 and scales must be non-null");
+    if (!aligned16(v) || !aligned16(vt8) || !aligned4(scales))
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_fp8_quantize_v: v and vt8 must be 16-byte aligned, scales 4-byte aligned");
+    Geometry g;
+    fa_status st = fp8_geometry(B, H, N, d, cu_seqlens, total_tokens, "fa_fp8_quantize_v", &g);
+    if (st != FA_OK) return st;
+    if (vt_tokens % 128 != 0 || vt_tokens < 128 * fp8_blocks(B, N, g.tokens, cu_seqlens != nullptr))
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_fp8_quantize_v: vt_tokens = %d must be a multiple of 128 and at least "
+                    "fa_fp8_vt_tokens", vt_tokens);
+    if (g.tokens == 0) return FA_OK;
+    Fp8QuantParams p{};
+    p.seq = g.seq;
+    p.x = v;
+    p.out = vt8;
+    p.scales = scales;
+    p.heads = H;
+    p.vt_tokens = vt_tokens;
+    const cudaError_t e = launch_fp8_quant_v(p, d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_v launch");
+    return FA_OK;
+}
+
+fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                     const void* vt8, const float* v_scale, int nb, int vt_tokens, void* o,
+                     float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                     const int* cu_seqlens, int total_tokens, float scale, cudaStream_t stream) {
+    using namespace fa;
+    t_last_error[0] = '\0';
+    const cudaEvent_t* ev = nullptr;
+    if (take_events(1, &ev) != FA_OK)
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd_fp8: fa_set_launch_events needs >= 2 events");
+    if (!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse)
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd_fp8: every pointer must be non-null");
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse) ||
+        !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_fwd_fp8: tensors must be 16-byte aligned, scales 4-byte aligned");
+    if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8: head dim %d (only 128)", d);
+    Geometry g;
+    fa_status st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale, &g);
+    if (st != FA_OK) return st;
+    const long long blocks = fp8_blocks(B, N, g.tokens, cu_seqlens != nullptr);
+    if (nb < blocks) return fail(FA_ERR_INVALID_ARG, "fa_fwd_fp8: nb = %d below fa_fp8_scale_blocks", nb);
+    if (vt_tokens % 128 != 0 || vt_tokens < 128 * blocks)
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_fwd_fp8: vt_tokens = %d must be a multiple of 128 and at least "
+                    "fa_fp8_vt_tokens", vt_tokens);
+    if (g.tokens == 0) return FA_OK;
+
+    FwdParams p;
+    if ((st = make_u8_token_map(&p.tm_q, q8, g.tokens, Hq, d, "q8")) != FA_OK) return st;
+    if ((st = make_u8_token_map(&p.tm_k, k8, g.tokens, Hkv, d, "k8")) != FA_OK) return st;
+    if ((st = make_vt_map(&p.tm_v, vt8, vt_tokens, d, Hkv)) != FA_OK) return st;
+    if ((st = make_token_map(&p.tm_o, o, g.tokens, Hq, d, FA_DTYPE_BF16, "o")) != FA_OK) return st;
+    p.elem = kElemFp8Code;
+    p.drop = DropoutParams{};
+    p.q_scale = q_scale;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.nb = nb;
+    p.seq = g.seq;
+    p.o = o;
+    p.lse = lse;
+    p.scale_log2 = scale * kLog2e;
+    p.num_work = num_blocks(g, kFwdQTiles * kBlockM, Hq);
+    p.timeout_cycles = g_wait_limit.load();
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fa_fwd_fp8: cannot resolve the device status word");
+    cudaError_t e = record(ev, 0, stream);
+    if (e == cudaSuccess) e = launch_fwd(p, d, stream);
+    if (e == cudaSuccess) e = record(ev, 1, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
+    return FA_OK;
+}
+
+}  // extern "C"

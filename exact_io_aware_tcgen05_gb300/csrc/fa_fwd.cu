@@ -41,15 +41,24 @@
 
 
 namespace fa {
-static_assert(kElemBf16 == kElemBf16Code && kElemF16 == kElemF16Code, "element-type codes");
+static_assert(kElemBf16 == kElemBf16Code && kElemF16 == kElemF16Code && kElemFp8 == kElemFp8Code,
+              "element-type codes");
 namespace {
 
-template <int D>
+// E: element type of the operands (kElemBf16, kElemF16, or kElemFp8: e4m3 Q, K and
+// transposed V, bf16 O)
+template <int D, int E>
 struct FwdCfg {
-    static constexpr int kChunks = D / 64;                 // 128-byte swizzle column blocks
-    static constexpr int kChunkBytes = kBlockM * 128;      // 128 rows x 64 16-bit elements
-    static constexpr int kTileBytes = kBlockM * D * 2;
-    static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring depth
+    static constexpr bool kF8 = (E == kElemFp8);
+    static constexpr int kElemBytes = kF8 ? 1 : 2;
+    static constexpr int kChunks = D * kElemBytes / 128;   // 128-byte swizzle column blocks
+    static constexpr int kChunkElems = 128 / kElemBytes;
+    static constexpr int kChunkBytes = kBlockM * 128;      // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kBlockM * D * kElemBytes;
+    static constexpr int kOTileBytes = kBlockM * D * 2;    // a 16-bit output tile
+    static constexpr int kOChunks = D / 64;
+    static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;   // K/V ring depth
+    static_assert(2 * kOTileBytes <= kStages * kTileBytes, "output staging in the ring");
     static constexpr int kThreads = 384;
     static constexpr int kTmemCols = 512;
     static constexpr int kColS = 0;                        // S_t at kColS + 128 t
@@ -98,9 +107,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // E: element type of q, k, v and o (kElemBf16 or kElemF16); DROP: dropout of P
 template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, E>;
+    constexpr bool F8 = C::kF8;
+    constexpr int EO = F8 ? kElemBf16 : E;   // element type of O
+    static_assert(!(F8 && (DROP || D != 128)), "the fp8 forward: d = 128, no dropout");
     constexpr uint32_t kIdescQK = idesc_f32acc(kBlockM, kBlockN, false, false, E);
-    constexpr uint32_t kIdescPV = idesc_f32acc(kBlockM, D, false, true, E);
+    // fp8: V^T tiles, K-major like K; 16-bit: V tiles read MN-major
+    constexpr uint32_t kIdescPV = idesc_f32acc(kBlockM, D, false, !F8, E);
     const SeqInfo& s = p.seq;
 
     int b, h, qblk;
@@ -160,7 +173,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             for (int t = 0; t < kFwdQTiles; ++t)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem_addr(sQ + t * C::kTileBytes + c * C::kChunkBytes), &p.tm_q,
-                                qbar, c * 64, h, seq_start + q0 + t * kBlockM);
+                                qbar, c * C::kChunkElems, h, seq_start + q0 + t * kBlockM);
+            // fp8: V^T rows are the d dimension, columns this sequence's keys from
+            // its padded start (a multiple of 128, so the TMA x coordinate is aligned)
+            const int vt_col = F8 ? 128 * seq_block_col(s, b) : 0;
             int issued = 0;
             for (int i = 0; i < 2 * nkv; ++i) {
                 const int st = i % C::kStages, use = i / C::kStages;
@@ -171,9 +187,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 mbar_arrive_expect_tx(fb, C::kTileBytes);
                 const CUtensorMap* map = (i & 1) ? &p.tm_v : &p.tm_k;
                 const int row = seq_start + (kv_first + i / 2) * kBlockN;
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes), map,
-                                     fb, c * 64, g, row, keep);
+                if (F8 && (i & 1))
+                    tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes), map, fb,
+                                     vt_col + (kv_first + i / 2) * kBlockN, 0, g, keep);
+                else
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes),
+                                         map, fb, c * C::kChunkElems, g, row, keep);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -196,19 +216,35 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             // descriptor of the tile base; a k-step adds its byte offset >> 4
             const uint64_t qd = sdesc_sw128(smem_addr(sQ + t * C::kTileBytes), 16, 1024);
             const uint64_t kd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes), 16, 1024);
+            if constexpr (F8) {
+                // one 128-byte chunk per row; K = 32 e4m3 (32 bytes) per product
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, kIdescQK, kk > 0);
+                for (int kk = 0; kk < D / 32; ++kk)
+                    mma_ss_f8(tmem + C::kColS + t * kBlockN, qd + 2 * kk, kd + 2 * kk, kIdescQK, kk > 0);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+                    mma_ss(tmem + C::kColS + t * kBlockN, qd + off, kd + off, kIdescQK, kk > 0);
+                }
             }
         };
         auto issue_pv = [&](int t, int st, bool acc) {
-            const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes),
-                                            C::kChunkBytes, 1024);
+            if constexpr (F8) {
+                // P_t: 4 e4m3 per TMEM column, 32 keys (8 columns) per product; V^T K-major
+                const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes), 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
-                       vd + ((kk * 2048) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBlockN / 32; ++kk)
+                    mma_ts_f8(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
+                              vd + 2 * kk, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+            } else {
+                const uint64_t vd = sdesc_sw128(smem_addr(sKV + st * C::kTileBytes),
+                                                C::kChunkBytes, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kBlockN + kk * 8,
+                           vd + ((kk * 2048) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
             }
         };
         if (lane == 0) {
@@ -270,6 +306,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int full_lo = key_lo(s, tile_q_last);            // keys >= this are >= every row's lo
         const int full_hi = key_hi(s, tile_q_first, len);      // keys <= this are <= every row's hi
         const float sl2 = p.scale_log2;
+        // fp8: the scores of key block j are (Q8 K8^T) s_q s_k with s_q the scale of this
+        // query tile and s_k that of the key block; both fold into the exponent scale
+        const int blk_col = F8 ? seq_block_col(s, b) : 0;
+        // (a tile wholly past the sequence end reads its last block's scale; its rows
+        // are never stored)
+        const float sq = F8 ? __ldg(p.q_scale + static_cast<long long>(h) * p.nb + blk_col +
+                                    min(q0 / kBlockM + t, ceil_div(len, kBlockM) - 1))
+                            : 1.f;
+        const float* ks_row = F8 ? p.k_scale + static_cast<long long>(g) * p.nb + blk_col : nullptr;
         const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h);   // dropout counter word
 
         // Dropout: the Philox words of a key block do not depend on the scores, so each
@@ -317,15 +362,21 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     for (int c = 0; c < kBlockN; ++c)
                         if (c < clo || c > chi) sv[c] = kNegInf;
                 }
-                // row max as a tree (8 independent chains) to keep the latency short
+                // row max in 8 independent chains (short latency) of three-input maxima
+                // (half the instructions of two-input ones)
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-                for (int c = 8; c < kBlockN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                const float m_blk = mx * sl2;
+                for (int c = 8; c + 16 <= kBlockN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kBlockN - 8 + i]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                const float sl2b = F8 ? sl2 * sq * __ldg(ks_row + kv_first + j) : sl2;
+                const float m_blk = mx * sl2b;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (m_blk > m_ref + kRescaleThreshold) {
@@ -335,13 +386,29 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     l *= alpha;
                 }
                 const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
-                const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(neg_ref, neg_ref);
+                const uint64_t sl2x2 = f2_pack(sl2b, sl2b), nref2 = f2_pack(neg_ref, neg_ref);
                 uint64_t rs2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
                                    f2_pack(0.f, 0.f)};
                 // P (16-bit pairs) goes to the first 64 columns of S_t in two halves; every
-                // S value is already in registers, so the overwrite is safe.
+                // S value is already in registers, so the overwrite is safe.  fp8: P as
+                // e4m3, four keys per column, the first 32 columns.
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < 2 && F8; ++half) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int kc = 64 * half + 4 * c;
+                        const float2 a = f2_unpack(f2_fma(f2_pack(sv[kc], sv[kc + 1]), sl2x2, nref2));
+                        const float2 e = f2_unpack(f2_fma(f2_pack(sv[kc + 2], sv[kc + 3]), sl2x2, nref2));
+                        const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                        const float p2 = ex2_approx(e.x), p3 = ex2_approx(e.y);
+                        rs2[c & 3] = f2_add(rs2[c & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+                        pk[c] = pack4_e4m3(p0, p1, p2, p3);
+                    }
+                    tmem_st16(tS + 16 * half, pk);
+                }
+#pragma unroll
+                for (int half = 0; half < 2 && !F8; ++half) {
                     uint32_t pk[32];
                     // dropout: the random bytes of keys kb + 64 half .. + 63 of this row;
                     // l sums the probabilities before dropout, the product takes the kept
@@ -406,15 +473,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         // tile cut by the sequence end is stored row by row.  The choice is made
         // uniform over the warpgroup.
         const bool valid = q < len;
-        const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) / l : 0.f;
+        // fp8: O carries the scale of V (per sequence and key/value head)
+        const float vs = F8 ? __ldg(p.v_scale + static_cast<long long>(g) * s.B + b) : 1.f;
+        const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) * vs / l : 0.f;
         if (named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
             tc_fence_after();
-            uint8_t* stage = sKV + t * C::kTileBytes;
-            stage_acc_row<D, E>(tO, inv_l, stage, C::kChunkBytes, r, 0);
+            uint8_t* stage = sKV + t * C::kOTileBytes;
+            stage_acc_row<D, EO>(tO, inv_l, stage, C::kChunkBytes, r, 0);
             fence_proxy_async_smem();
             named_bar_sync(kFwdBarEpi + t, kBlockM);
             if (quad == 0 && lane == 0) {
-                for (int c = 0; c < C::kChunks; ++c)
+                for (int c = 0; c < C::kOChunks; ++c)
                     tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
                                  seq_start + tile_q_first);
                 bulk_commit_group();
@@ -433,8 +502,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<E>(__uint_as_float(orow[2 * i]) * inv_l,
-                                    __uint_as_float(orow[2 * i + 1]) * inv_l);
+                    w[i] = pack2<EO>(__uint_as_float(orow[2 * i]) * inv_l,
+                                     __uint_as_float(orow[2 * i + 1]) * inv_l);
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
 #pragma unroll
@@ -463,7 +532,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
 template <int D, int E, bool DROP>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, E>;
     auto kern = fa_fwd_kernel<D, E, DROP>;
     // the register split needs the launch's full 168 registers per thread: a
     // build that gave the kernel fewer would make the softmax warps wait forever
@@ -485,6 +554,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
     if (p.num_work <= 0) return cudaSuccess;
+    if (p.elem == kElemFp8) return d == 128 ? launch_fwd_d<128, kElemFp8, false>(p, stream) : cudaErrorInvalidValue;
     const bool f16 = p.elem == kElemF16, drop = p.drop.thresh != 0;
     if (drop) {
         if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, true>(p, stream) : launch_fwd_d<64, kElemF16, true>(p, stream);

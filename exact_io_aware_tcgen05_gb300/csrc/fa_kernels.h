@@ -18,6 +18,7 @@ constexpr int kFwdQTiles = 2;  // query tiles per forward CTA (ping-pong)
 // the kernels name them kElemBf16 / kElemF16)
 constexpr int kElemBf16Code = 0;
 constexpr int kElemF16Code = 1;
+constexpr int kElemFp8Code = 2;   // the fp8 forward: e4m3 Q, K, V^T and bf16 O
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 // Token / sequence geometry common to all kernels.  Dense batches are the
@@ -50,8 +51,15 @@ struct FwdParams {
     float* lse;         // fp32 dense [B, Hq, N]; packed [Hq, total_tokens]
     float scale_log2;   // softmax scale * log2(e)
     int num_work;       // launched CTAs (upper bound on work items)
-    int elem;           // element type of q, k, v, o (kElemBf16Code / kElemF16Code)
+    int elem;           // element type of q, k, v, o (kElemBf16Code / kElemF16Code), or
+                        // kElemFp8Code: e4m3 q, k and transposed v (tm_v over [Hkv, d,
+                        // vt_tokens]), bf16 o
     DropoutParams drop;
+    // fp8 only: block scales of q [Hq, nb] and k [Hkv, nb], per-sequence scales of v [Hkv, B]
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    int nb;
     long long timeout_cycles;
     int* status;        // device status word
 };
@@ -76,12 +84,25 @@ struct BwdParams {
     int* status;
 };
 
+// Quantisation of one attention operand to e4m3 (fa_fp8.cu).
+struct Fp8QuantParams {
+    SeqInfo seq;        // only B, N, total_tokens and cu_seqlens are used
+    const void* x;      // bf16 [tokens, heads, d]
+    void* out;          // Q/K: e4m3 [tokens, heads, d]; V: e4m3 V^T [heads, d, vt_tokens]
+    float* scales;      // Q/K: [heads, nb]; V: [heads, B]
+    int heads;
+    int nb;             // Q/K: columns of the scale array
+    long long vt_tokens;  // V: columns of V^T
+};
+
 // Launchers (defined in the kernel translation units).  They only enqueue on
 // `stream` and return the launch error.
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_fp8_quant_qk(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream);
+cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, cudaStream_t stream);
 
 int* device_status_word();  // library-owned device status word (fa_api.cu)
 

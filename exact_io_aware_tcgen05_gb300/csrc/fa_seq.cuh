@@ -45,6 +45,21 @@ __device__ __forceinline__ long long row_stat_index(const SeqInfo& s, int b, int
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// fp8 layouts: the column of sequence b's first 128-token block in a [heads, nb]
+// block-scale array (the blocks of the earlier sequences, ceil(len / 128) each);
+// 128 times it is the column of its first key in the transposed V layout, where
+// every sequence is padded to a multiple of 128 keys.
+__device__ __forceinline__ int seq_block_col(const SeqInfo& s, int b) {
+    if (!s.cu_seqlens) return b * ceil_div(s.N, 128);
+    int acc = 0;
+    for (int i = 0; i < b; ++i) {
+        int st, len;
+        seq_bounds(s, i, st, len);
+        acc += ceil_div(len, 128);
+    }
+    return acc;
+}
+
 // Heads per scheduling chunk (see map_work).
 constexpr int kHeadChunk = 8;
 

@@ -30,7 +30,8 @@ class Workload:
     window: int            # 0: none; else keys visible per query, including itself
     backward: bool         # whether the workload includes the backward pass
     lengths: Optional[Tuple[int, ...]] = None   # packed batch: per-sequence lengths
-    dtype: str = "bf16"    # element type of the 16-bit tensors: "bf16" or "f16"
+    dtype: str = "bf16"    # element type of the 16-bit tensors: "bf16" or "f16"; "fp8": the
+                           # fp8 forward on e4m3 operands quantised from bf16 inputs
     p_drop: float = 0.0    # dropout probability of the attention probabilities (0: none)
 
     @property
@@ -73,8 +74,11 @@ class Workload:
         return 10 * self.d * self.Hq * self.visible_pairs_per_head()
 
     def fwd_io_bytes(self) -> int:
-        """Algorithmic HBM bytes of one forward: read Q, K, V; write O and LSE once."""
+        """Algorithmic HBM bytes of one forward: read Q, K, V; write O and LSE once
+        (fp8: one-byte Q, K, V, two-byte O)."""
         T = self.total_tokens
+        if self.dtype == "fp8":
+            return T * self.d * (self.Hq + 2 * self.Hkv) + 2 * T * self.d * self.Hq + 4 * T * self.Hq
         return 2 * T * self.d * (2 * self.Hq + 2 * self.Hkv) + 4 * T * self.Hq
 
     def bwd_io_bytes(self) -> int:
@@ -111,6 +115,8 @@ WORKLOADS = {
                  dtype="f16"),
         Workload("fwdbwd_b2_h16_n8192_d128_causal_dropout10", 2, 16, 16, 8192, 128, True, 0, True,
                  p_drop=0.1),
+        Workload("fwd_b2_h16_n8192_d128_causal_fp8", 2, 16, 16, 8192, 128, True, 0, False,
+                 dtype="fp8"),
         _varlen(128),
         _varlen(64),
     ]

@@ -164,6 +164,58 @@ fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * FP8 (e4m3) forward.  "FlashAttention: How IO-Aware Tiling and Online Softmax
+ * Solved Transformer Memory Bottlenecks" ("FlashAttention-3" bullets) names
+ * FP8 with block quantisation of the inputs but gives no format, block or scale
+ * rule; this library defines them.
+ *
+ * e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+ * largest finite value 448; a code is a value rounded to nearest (ties to even)
+ * and saturated to +-448.
+ *
+ * Layouts (tokens as in fa_fwd: dense b * N + i, packed cu_seqlens[b] + i):
+ *   q8, k8   e4m3 [tokens, Hq or Hkv, d], scales [heads, nb]: one per (head,
+ *            128-token block of a sequence); block kb of sequence b is column
+ *            (blocks of sequences 0..b-1) + kb, the blocks of a sequence of
+ *            length L being ceil(L / 128).  nb >= fa_fp8_scale_blocks(...).
+ *   vt8      e4m3 V^T [Hkv, d, vt_tokens]: key i of sequence b (and channel c)
+ *            at column 128 * (blocks of sequences 0..b-1) + i, row c; the
+ *            columns past a sequence's length up to its next multiple of 128 hold
+ *            zero codes.  vt_tokens >= fa_fp8_vt_tokens(...), a multiple of 128.
+ *   v_scale  [Hkv, B]: one per (key/value head, sequence).
+ * The values are code * scale.  fa_fp8_quantize_qk / fa_fp8_quantize_v write
+ * these from bf16 tensors in the layouts of fa_fwd: per block (Q, K) or per
+ * (sequence, head) (V), scale = amax / 448 in float (1 for an all-zero block)
+ * and code = e4m3(x / scale) with the division rounded to nearest in float.
+ *
+ * fa_fwd_fp8 computes O (bf16, layout of fa_fwd) and LSE (fp32, layout of
+ * fa_fwd) of exact attention on those values, with the arguments and masks of
+ * fa_fwd.  The products run on e4m3 operands with fp32 accumulation; the
+ * probabilities are rounded to e4m3 for the P V product (the row sums use them
+ * unrounded), so each O element is within 2^-4 sum_j P_ij |V_jc| plus 2^-10 per
+ * key with P_ij < 2^-6 of the exact value (plus the bf16 rounding of O); LSE is
+ * as accurate as fa_fwd's.  Only d = 128 (FA_ERR_UNSUPPORTED otherwise); no
+ * dropout.  Pointers: tensors 16-byte aligned, scale arrays 4-byte aligned.
+ * Errors otherwise as fa_fwd.  The quantisers take d in {64, 128} and the
+ * geometry arguments of fa_fwd (H heads); they only enqueue work.
+ *
+ * fa_fp8_scale_blocks / fa_fp8_vt_tokens return the minimum nb / vt_tokens for
+ * a batch (exact for dense batches, packed != 0: an upper bound from
+ * total_tokens and B), or 0 for invalid arguments.
+ */
+int fa_fp8_scale_blocks(int B, int N, int total_tokens, int packed);
+int fa_fp8_vt_tokens(int B, int N, int total_tokens, int packed);
+fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scales, int nb, int B, int H, int N,
+                             int d, const int* cu_seqlens, int total_tokens, cudaStream_t stream);
+fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_tokens, int B, int H,
+                            int N, int d, const int* cu_seqlens, int total_tokens,
+                            cudaStream_t stream);
+fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                     const void* vt8, const float* v_scale, int nb, int vt_tokens, void* o,
+                     float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                     const int* cu_seqlens, int total_tokens, float scale, cudaStream_t stream);
+
+/*
  * Backward pass of fa_fwd for the loss gradient dO, recomputing S and P from
  * the saved logsumexp ("3. Recomputation in the Backward Pass"):
  *   D_i = dO_i . O_i,  P_ij = exp(S_ij - LSE_i),  dP_ij = dO_i . v_j,

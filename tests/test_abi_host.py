@@ -126,3 +126,30 @@ def test_dropout_entry_points_reject_bad_probabilities(lib):
     st = fa.fa_bwd_dropout(fa.FA_DTYPE_BF16, 1.5, 1, 0, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 1,
                            128, 128, 1, 0, None, 0, 0.125, 256, need, None, check=False)
     assert st == 1
+
+
+def test_fp8_sizes_and_argument_checks(lib):
+    fa, _ = lib
+    # dense: exact block counts; packed: the bound ceil(T / 128) + B (capped by the dense count)
+    assert fa.fa_fp8_scale_blocks(2, 300, 0, 0) == 6 and fa.fa_fp8_vt_tokens(2, 300, 0, 0) == 768
+    assert fa.fa_fp8_scale_blocks(16, 8192, 68143, 1) == 533 + 16
+    assert fa.fa_fp8_vt_tokens(16, 8192, 68143, 1) == 128 * (533 + 16)
+    assert fa.fa_fp8_scale_blocks(3, 100, 300, 1) == 3          # capped at B * ceil(N / 128)
+    assert fa.fa_fp8_scale_blocks(0, 100, 0, 0) == 0
+    def fwd(**over):
+        a = dict(nb=3, vt=384, d=128, N=300, q=16)
+        a.update(over)
+        return fa.fa_fwd_fp8(a["q"], 16, 16, 16, 16, 16, a["nb"], a["vt"], 16, 16, 1, 1, 1, a["N"],
+                             a["d"], 0, 0, None, 0, 0.1, None, check=False)
+    assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(nb=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd(vt=256) == fa.FA_ERR_INVALID_ARG
+    assert fwd(vt=400) == fa.FA_ERR_INVALID_ARG                  # not a multiple of 128
+    assert fwd(q=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd(q=8) == fa.FA_ERR_INVALID_ARG                     # misaligned
+    assert fa.fa_fp8_quantize_qk(16, 16, 16, 2, 1, 1, 300, 128, None, 0, None,
+                                 check=False) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fp8_quantize_qk(16, 16, 16, 3, 1, 1, 300, 96, None, 0, None,
+                                 check=False) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fp8_quantize_v(16, 16, 16, 256, 1, 1, 300, 128, None, 0, None,
+                                check=False) == fa.FA_ERR_INVALID_ARG

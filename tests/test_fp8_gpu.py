@@ -1,0 +1,148 @@
+"""The fp8 (e4m3) forward (fa_fp8_quantize_qk / fa_fp8_quantize_v / fa_fwd_fp8)
+against the fp8 oracle.
+
+Both sides start from the same seeded bf16 inputs and quantise them on their own;
+the codes and scales must agree bit for bit (float32 division and e4m3 rounding
+to nearest even on both sides).  The forward is then compared with exact
+attention on the dequantised values: LSE within the bf16 path's 1e-3, O within
+the per-element bound of oracle.fp8.o_error_bound (the kernel rounds P to e4m3
+for the P V product).
+"""
+import numpy as np
+import pytest
+
+from helpers import LSE_MAX_ABS, cu_dev, make_case, scale_of, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+# (B, Hq, Hkv, N, causal, window, lengths); d = 128
+CASES = [
+    (1, 1, 1, 128, False, 0, None),
+    (2, 4, 2, 300, True, 0, None),
+    (1, 8, 1, 700, True, 200, None),
+    (6, 4, 2, 513, True, 0, (1, 127, 128, 129, 300, 513)),
+    (3, 2, 1, 900, False, 0, (900, 5, 256)),
+]
+D = 128
+
+
+def _ids(c):
+    return f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}c{int(c[4])}w{c[5]}{'p' if c[6] else ''}"
+
+
+def _gpu(fa, x, N, causal, window):
+    import torch
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    cu = cu_dev(x["cu"])
+    ops = fa.quantize_fp8(q, k, v, cu_seqlens=cu, max_seqlen=N)
+    o, lse = fa.attention_forward_fp8(ops, causal=causal, window=window, scale=scale_of(D),
+                                      cu_seqlens=cu, max_seqlen=N)
+    fa.fa_device_status(torch.cuda.current_stream())
+    assert o.dtype == torch.bfloat16
+    return ops, o, lse
+
+
+def _oracle_ops(fp8, x, B, N, nb, vt_tokens):
+    cu = None if x["cu"] is None else [int(c) for c in x["cu"]]
+    q8, qs = fp8.quantize_qk(x["q"], B, N, cu, nb=nb)
+    k8, ks = fp8.quantize_qk(x["k"], B, N, cu, nb=nb)
+    vt8, vs = fp8.quantize_v(x["v"], B, N, cu, vt_tokens=vt_tokens)
+    return cu, (q8, qs, k8, ks, vt8, vs)
+
+
+def _check_quantisation(fp8, ops, ref, B, N, cu):
+    q8, qs, k8, ks, vt8, vs = (t.cpu().numpy() for t in ops[:6])
+    rq8, rqs, rk8, rks, rvt8, rvs = ref
+    _, blocks = fp8.block_offsets(B, N, cu)
+    assert np.array_equal(q8, rq8) and np.array_equal(k8, rk8)
+    assert np.array_equal(qs[:, :blocks], rqs[:, :blocks])
+    assert np.array_equal(ks[:, :blocks], rks[:, :blocks])
+    assert np.array_equal(vs, rvs)
+    _, cols = fp8.vt_offsets(B, N, cu)          # the written columns: padding included
+    assert np.array_equal(vt8[:, :, :cols], rvt8[:, :, :cols])
+
+
+def _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, causal, window, cu, rows_per_seq=None):
+    q8, qs, k8, ks, vt8, vs = ref
+    qd = fp8.dequantize_qk(q8, qs, B, N, cu)
+    kd = fp8.dequantize_qk(k8, ks, B, N, cu)
+    vd = fp8.dequantize_v(vt8, vs, B, N, cu)
+    og, lg = to_f64(o), lse.cpu().numpy().astype(np.float64)
+    G = Hq // Hkv
+    import oracle
+    worst, err2, ref2 = -np.inf, 0.0, 0.0
+    for b, (start, L) in enumerate(fp8.seq_lengths(B, N, cu)):
+        rows = np.arange(L) if rows_per_seq is None else np.unique(np.clip(rows_per_seq, 0, L - 1))
+        qs_, ks_, vs_ = ((qd[b], kd[b], vd[b]) if cu is None else
+                         (qd[start:start + L], kd[start:start + L], vd[start:start + L]))
+        for h in range(Hq):
+            qh, kg, vg = qs_[:, h], ks_[:, h // G], vs_[:, h // G]
+            o_ref, l_ref = oracle.fwd_group(qh[None], kg, vg, causal, window, scale_of(D), rows=rows)
+            o_ref, l_ref = o_ref[0], l_ref[0]
+            if cu is None:
+                o_got, l_got = og[b, rows, h], lg[b, h, rows]
+            else:
+                o_got, l_got = og[start + rows, h], lg[h, start + rows]
+            assert np.max(np.abs(l_got - l_ref)) <= LSE_MAX_ABS
+            lse_full = np.zeros(L)
+            lse_full[rows] = l_ref
+            bound = fp8.o_error_bound(qh, kg, vg, lse_full, causal=causal, window=window,
+                                      scale=scale_of(D), rows=rows)
+            worst = max(worst, float(np.max(np.abs(o_got - o_ref) - bound)))
+            err2 += float(np.sum((o_got - o_ref) ** 2))
+            ref2 += float(np.sum(o_ref ** 2))
+    assert worst <= 0.0, f"O outside the e4m3 bound by {worst}"
+    # statistical check on N(0,1) inputs.  Rounding a value spread over a binade to e4m3
+    # (spacing 2^-3 of the binade's base) leaves an RMS relative error of about
+    # 2^-3 ln 2 / sqrt(12) ~ 2.5%; with diffuse attention O and its error both shrink
+    # like 1 / sqrt(keys seen), so the relative Frobenius error of O sits near that
+    # figure.  4% leaves room for the sampling spread and catches a doubled error.
+    assert np.sqrt(err2 / ref2) <= 4e-2
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_fp8_quantisation_and_forward_match_oracle(fa, oracle_mod, case):
+    from oracle import fp8
+    B, Hq, Hkv, N, causal, window, lengths = case
+    x = make_case(B, Hq, Hkv, N, D, seed=31, lengths=lengths, with_dout=False)
+    ops, o, lse = _gpu(fa, x, N, causal, window)
+    cu, ref = _oracle_ops(fp8, x, B if lengths is None else len(lengths), N, ops.nb, ops.vt_tokens)
+    Bn = B if lengths is None else len(lengths)
+    _check_quantisation(fp8, ops, ref, Bn, N, cu)
+    _check_forward(fp8, x, ref, o, lse, Bn, Hq, Hkv, N, causal, window, cu)
+
+
+def test_fp8_fullsize_sampled_rows(fa, oracle_mod):
+    """B2 H16 N8192 d128 causal (the bench shape): quantisation checked everywhere,
+    the forward on sampled rows of every head."""
+    from oracle import fp8
+    B, Hq, Hkv, N = 2, 16, 16, 8192
+    x = make_case(B, Hq, Hkv, N, D, seed=0, with_dout=False)
+    ops, o, lse = _gpu(fa, x, N, True, 0)
+    cu, ref = _oracle_ops(fp8, x, B, N, ops.nb, ops.vt_tokens)
+    _check_quantisation(fp8, ops, ref, B, N, cu)
+    rows = np.array([0, 1, 127, 128, 255, 256, 4095, 4096, 8190, 8191])
+    _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, True, 0, cu, rows_per_seq=rows)
+
+
+def test_fp8_rejects_d64_and_short_buffers(fa):
+    import torch
+    dev = "cuda"
+    q8 = torch.zeros((1, 128, 1, 64), dtype=torch.uint8, device=dev)
+    sc = torch.ones((1, 1), dtype=torch.float32, device=dev)
+    vt = torch.zeros((1, 64, 128), dtype=torch.uint8, device=dev)
+    o = torch.empty((1, 128, 1, 64), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, 1, 128), dtype=torch.float32, device=dev)
+    st = fa.fa_fwd_fp8(q8, sc, q8, sc, vt, sc, 1, 128, o, lse, 1, 1, 1, 128, 64, 0, 0, None, 0,
+                       0.125, check=False)
+    assert st == fa.FA_ERR_UNSUPPORTED
+    q8 = torch.zeros((1, 300, 1, 128), dtype=torch.uint8, device=dev)
+    o = torch.empty((1, 300, 1, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, 1, 300), dtype=torch.float32, device=dev)
+    vt = torch.zeros((1, 128, 384), dtype=torch.uint8, device=dev)
+    sc3 = torch.ones((1, 3), dtype=torch.float32, device=dev)
+    # nb = 2 < 3 blocks; vt_tokens = 256 < 384
+    assert fa.fa_fwd_fp8(q8, sc3, q8, sc3, vt, sc, 2, 384, o, lse, 1, 1, 1, 300, 128, 0, 0, None, 0,
+                         0.1, check=False) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_fp8(q8, sc3, q8, sc3, vt, sc, 3, 256, o, lse, 1, 1, 1, 300, 128, 0, 0, None, 0,
+                         0.1, check=False) == fa.FA_ERR_INVALID_ARG
