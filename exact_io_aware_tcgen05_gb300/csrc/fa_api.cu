@@ -588,7 +588,7 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_toke
     p.scales = scales;
     p.heads = H;
     p.vt_tokens = vt_tokens;
-    const cudaError_t e = launch_fp8_quant_v(p, d, stream);
+    const cudaError_t e = launch_fp8_quant_v(p, d, num_blocks(g, kBlockN, H), stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_v launch");
     return FA_OK;
 }

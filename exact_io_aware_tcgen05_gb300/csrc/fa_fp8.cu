@@ -58,91 +58,125 @@ __device__ __forceinline__ float block_scale(float amax) {
     return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
 }
 
-// Q or K: thread r of a 128-thread CTA owns token row r of the block.
+constexpr int kQuantThreads = 256;
+
+// The 128 x D block of (sequence b, head h, 128-token block blk) as 16-byte units:
+// thread t takes units u = t % (D / 8) of rows t / (D / 8) + k * (256 / (D / 8)),
+// so a warp reads whole rows (coalesced).  Returns the block's largest magnitude
+// over the CTA; `v` holds this thread's units (zero past the sequence end).
 template <int D>
-__global__ void __launch_bounds__(128) fp8_quant_qk_kernel(const __grid_constant__ Fp8QuantParams p) {
-    __shared__ float red[4];
+__device__ __forceinline__ float load_block(const uint16_t* x, int heads, int start, int len, int h,
+                                            int blk, uint4 (&v)[kBlockM * D / 8 / kQuantThreads],
+                                            float* red) {
+    constexpr int kU = D / 8, kRows = kQuantThreads / kU, kN = kBlockM / kRows;
+    const int u = threadIdx.x % kU, r0 = threadIdx.x / kU;
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+        const int row = blk * kBlockM + r0 + k * kRows;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < len) {
+            v[k] = *reinterpret_cast<const uint4*>(
+                x + (static_cast<long long>(start + row) * heads + h) * D + 8 * u);
+            m = fmaxf(m, amax8(v[k]));
+        }
+    }
+    return cta_max(m, red);
+}
+
+// Q or K: one CTA per (sequence, 128-token block, head).
+template <int D>
+__global__ void __launch_bounds__(kQuantThreads) fp8_quant_qk_kernel(const __grid_constant__ Fp8QuantParams p) {
+    __shared__ float red[kQuantThreads / 32];
     int b, h, blk;
     if (!map_work(p.seq, blockIdx.x, kBlockM, p.heads, false, b, h, blk)) return;
     int start, len;
     seq_bounds(p.seq, b, start, len);
-    const int row = blk * kBlockM + threadIdx.x;
-    const bool valid = row < len;
-    const long long base = (static_cast<long long>(start + row) * p.heads + h) * D;
-    uint4 v[D / 8];
-    float m = 0.f;
-    if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + base);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            v[i] = src[i];
-            m = fmaxf(m, amax8(v[i]));
-        }
-    }
-    const float scale = block_scale(cta_max(m, red));
+    constexpr int kU = D / 8, kRows = kQuantThreads / kU, kN = kBlockM / kRows;
+    uint4 v[kN];
+    const float scale = block_scale(load_block<D>(static_cast<const uint16_t*>(p.x), p.heads, start,
+                                                  len, h, blk, v, red));
     if (threadIdx.x == 0)
         p.scales[static_cast<long long>(h) * p.nb + seq_block_col(p.seq, b) + blk] = scale;
-    if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + base);
+    const int u = threadIdx.x % kU, r0 = threadIdx.x / kU;
+    uint8_t* out = static_cast<uint8_t*>(p.out);
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            const uint2 lo = quant8(v[2 * i], scale), hi = quant8(v[2 * i + 1], scale);
-            dst[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        }
+    for (int k = 0; k < kN; ++k) {
+        const int row = blk * kBlockM + r0 + k * kRows;
+        if (row < len)
+            *reinterpret_cast<uint2*>(out + (static_cast<long long>(start + row) * p.heads + h) * D +
+                                      8 * u) = quant8(v[k], scale);
     }
 }
 
-// V: one CTA of 256 threads per (sequence, head): the sequence's amax, then per
-// 128-token block the codes into shared memory [token][d] and out transposed, a
-// row of 128 keys (128 bytes) per d.
+// V, in three passes over (sequence, 128-token block, head) CTAs and a fourth over
+// (sequence, head): the scale slots start at zero, take the atomic max of the
+// blocks' largest magnitudes (float bits compare like ints for non-negative
+// values), then every block quantises with amax / 448, and last the slots turn
+// from amax into the scale.
+__global__ void fp8_v_slots_kernel(float* slots, int n, bool to_scale) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) slots[i] = to_scale ? block_scale(slots[i]) : 0.f;
+}
+
 template <int D>
-__global__ void __launch_bounds__(256) fp8_quant_v_kernel(const __grid_constant__ Fp8QuantParams p) {
-    __shared__ float red[8];
-    __shared__ __align__(16) uint8_t tile[kBlockN][D];
-    const int b = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
-    if (b >= p.seq.B) return;
+__global__ void __launch_bounds__(kQuantThreads) fp8_v_amax_kernel(const __grid_constant__ Fp8QuantParams p) {
+    __shared__ float red[kQuantThreads / 32];
+    int b, h, blk;
+    if (!map_work(p.seq, blockIdx.x, kBlockN, p.heads, false, b, h, blk)) return;
     int start, len;
     seq_bounds(p.seq, b, start, len);
+    uint4 v[kBlockM * D / 8 / kQuantThreads];
+    const float m = load_block<D>(static_cast<const uint16_t*>(p.x), p.heads, start, len, h, blk, v, red);
+    if (threadIdx.x == 0)
+        atomicMax(reinterpret_cast<int*>(p.scales + static_cast<long long>(h) * p.seq.B + b),
+                  __float_as_int(m));
+}
+
+// Quantise one block of V and write it transposed: thread i takes channels
+// 8 (i % (D / 8)) .. + 7 of the block's tokens (i / (D / 8)) * kT .. + kT - 1 (one
+// 16-byte load per token, a warp reading whole rows), and after the quantisation
+// regroups the bytes per channel in registers (byte permutes) into kT keys of one
+// V^T row, stored as one piece.
+template <int D>
+__global__ void __launch_bounds__(128) fp8_v_quant_kernel(const __grid_constant__ Fp8QuantParams p) {
+    constexpr int kU = D / 8;              // channel groups
+    constexpr int kT = kBlockN * kU / 128; // tokens per thread: 16 (d = 128) or 8 (d = 64)
+    static_assert(kT % 4 == 0, "whole words of keys");
+    int b, h, blk;
+    if (!map_work(p.seq, blockIdx.x, kBlockN, p.heads, false, b, h, blk)) return;
+    int start, len;
+    seq_bounds(p.seq, b, start, len);
+    const float scale = block_scale(p.scales[static_cast<long long>(h) * p.seq.B + b]);
+    const int u = threadIdx.x % kU, t0 = (threadIdx.x / kU) * kT;
     const uint16_t* x = static_cast<const uint16_t*>(p.x);
-    constexpr int kU = D / 8;   // 16-byte units per token row
-    float m = 0.f;
-    for (int i = threadIdx.x; i < len * kU; i += blockDim.x) {
-        const int t = i / kU, u = i % kU;
-        m = fmaxf(m, amax8(*reinterpret_cast<const uint4*>(
-                         x + (static_cast<long long>(start + t) * p.heads + h) * D + 8 * u)));
-    }
-    const float scale = block_scale(cta_max(m, red));
-    if (threadIdx.x == 0) p.scales[static_cast<long long>(h) * p.seq.B + b] = scale;
-    uint8_t* out = static_cast<uint8_t*>(p.out);
-    const long long col0 = 128LL * seq_block_col(p.seq, b);
-    const int nblk = ceil_div(len, kBlockN);
-    for (int kb = 0; kb < nblk; ++kb) {
-        for (int i = threadIdx.x; i < kBlockN * kU; i += blockDim.x) {
-            const int t = i / kU, u = i % kU;
-            const int tok = kb * kBlockN + t;
-            uint2 c = make_uint2(0u, 0u);   // padding keys: zero codes
-            if (tok < len)
-                c = quant8(*reinterpret_cast<const uint4*>(
-                               x + (static_cast<long long>(start + tok) * p.heads + h) * D + 8 * u),
-                           scale);
-            *reinterpret_cast<uint2*>(&tile[t][8 * u]) = c;
-        }
-        __syncthreads();
-        // d rows of 128 keys: 8 units of 16 keys each
-        for (int i = threadIdx.x; i < D * 8; i += blockDim.x) {
-            const int dd = i / 8, k16 = i % 8;
-            uint32_t w[4];
+    uint2 c[kT];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int t0 = 16 * k16 + 4 * q;
-                w[q] = static_cast<uint32_t>(tile[t0][dd]) | (static_cast<uint32_t>(tile[t0 + 1][dd]) << 8) |
-                       (static_cast<uint32_t>(tile[t0 + 2][dd]) << 16) |
-                       (static_cast<uint32_t>(tile[t0 + 3][dd]) << 24);
-            }
-            *reinterpret_cast<uint4*>(out + (static_cast<long long>(h) * D + dd) * p.vt_tokens + col0 +
-                                      kb * kBlockN + 16 * k16) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int t = 0; t < kT; ++t) {
+        const int tok = blk * kBlockN + t0 + t;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);   // padding keys: zero values, zero codes
+        if (tok < len)
+            v = *reinterpret_cast<const uint4*>(x + (static_cast<long long>(start + tok) * p.heads + h) * D +
+                                                8 * u);
+        c[t] = quant8(v, scale);
+    }
+    uint8_t* out = static_cast<uint8_t*>(p.out);
+    const long long col = 128LL * seq_block_col(p.seq, b) + static_cast<long long>(blk) * kBlockN + t0;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t sel = (ch & 3) | (((ch & 3) + 4) << 4);   // byte ch of two words
+        uint32_t w[kT / 4];
+#pragma unroll
+        for (int q = 0; q < kT / 4; ++q) {
+            const uint32_t a0 = ch < 4 ? c[4 * q].x : c[4 * q].y, a1 = ch < 4 ? c[4 * q + 1].x : c[4 * q + 1].y;
+            const uint32_t a2 = ch < 4 ? c[4 * q + 2].x : c[4 * q + 2].y, a3 = ch < 4 ? c[4 * q + 3].x : c[4 * q + 3].y;
+            w[q] = __byte_perm(__byte_perm(a0, a1, sel), __byte_perm(a2, a3, sel), 0x5410);
         }
-        __syncthreads();
+        uint8_t* dst = out + (static_cast<long long>(h) * D + 8 * u + ch) * p.vt_tokens + col;
+        if constexpr (kT == 16)
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1 % (kT / 4)], w[2 % (kT / 4)], w[3 % (kT / 4)]);
+        else
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1 % (kT / 4)]);
     }
 }
 
@@ -150,16 +184,23 @@ __global__ void __launch_bounds__(256) fp8_quant_v_kernel(const __grid_constant_
 
 cudaError_t launch_fp8_quant_qk(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    if (d == 128) fp8_quant_qk_kernel<128><<<grid, 128, 0, stream>>>(p);
-    else fp8_quant_qk_kernel<64><<<grid, 128, 0, stream>>>(p);
+    if (d == 128) fp8_quant_qk_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
+    else fp8_quant_qk_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, cudaStream_t stream) {
-    const int grid = p.seq.B * p.heads;
-    if (grid <= 0) return cudaSuccess;
-    if (d == 128) fp8_quant_v_kernel<128><<<grid, 256, 0, stream>>>(p);
-    else fp8_quant_v_kernel<64><<<grid, 256, 0, stream>>>(p);
+cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream) {
+    const int n = p.seq.B * p.heads;
+    if (grid <= 0 || n <= 0) return cudaSuccess;
+    fp8_v_slots_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.scales, n, false);
+    if (d == 128) {
+        fp8_v_amax_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
+        fp8_v_quant_kernel<128><<<grid, 128, 0, stream>>>(p);
+    } else {
+        fp8_v_amax_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
+        fp8_v_quant_kernel<64><<<grid, 128, 0, stream>>>(p);
+    }
+    fp8_v_slots_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.scales, n, true);
     return cudaGetLastError();
 }
 

@@ -102,7 +102,7 @@ cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_fp8_quant_qk(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream);
-cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, cudaStream_t stream);
+cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream);
 
 int* device_status_word();  // library-owned device status word (fa_api.cu)
 
