@@ -19,8 +19,11 @@
 //   warps 4..7    softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8..11   softmax + epilogue of query tile 1
 // TMEM (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 and O_1 (D columns each)
-// from 256.  P_t (bf16 or fp16, the input type) overwrites the first 64 columns of S_t and feeds the
-// P.V product straight from TMEM.  The issuer interleaves the two tiles so the
+// from 256.  P_t (bf16 or fp16, the input type; e4m3 in the fp8 instance, four
+// keys per column) overwrites the first 64 (32) columns of S_t and feeds the
+// P.V product straight from TMEM.  The fp8 instance runs both products as
+// kind::f8f6f4 on e4m3 Q, K and transposed V, with the Q and K block scales
+// folded into the exponent scale and V's scale into 1/l.  The issuer interleaves the two tiles so the
 // tensor cores work on one tile while the softmax warps work on the other:
 //   S0=Q0K0 S1=Q1K0 | O0+=P0V0 S0=Q0K1 | O1+=P1V0 S1=Q1K1 | O0+=P0V1 ...
 // Scores are kept in log2 units (scale * log2 e folded in) and exponentiated
