@@ -2,7 +2,7 @@
 
 Every translation unit is compiled for sm_103a only, in parallel, then linked
 into one shared object next to this file.  The CUDA runtime is linked
-statically, so the library loads without a GPU; the driver's tensor-map
+statically, so the library loads without a GPU; the CUDA driver's tensor-map
 encoder is resolved at run time.
 """
 from __future__ import annotations
