@@ -31,7 +31,9 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
-              "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status"):
+              "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status",
+              "fa_fwd_fp8", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fp8_scale_blocks",
+              "fa_fp8_vt_tokens"):
         assert n in names
 
 
