@@ -60,28 +60,30 @@ __device__ __forceinline__ int seq_block_col(const SeqInfo& s, int b) {
     return acc;
 }
 
-// Heads per scheduling chunk (see map_work).
+// Heads per scheduling chunk (see map_work) unless the launcher picks another.
 constexpr int kHeadChunk = 8;
 
 // Maps CTA index w to (sequence b, head h, block index blk of `rows` rows).
-// Heads are taken in chunks of kHeadChunk: all work items of a chunk are
-// launched before the next chunk's, so the CTAs in flight touch few heads and
-// the tiles they share stay in L2.  Within a chunk the order is by "level":
-// level 0 is the most expensive block of every head of the chunk, level 1 the
-// next, and so on (longest first); the most expensive block is the last one
-// for query blocks under a causal mask (`from_end`), the first for key blocks.
-// Returns false for CTAs beyond the real work (packed batches launch an upper
-// bound).
+// Heads are taken in chunks of `chunk`: all work items of a chunk are launched
+// before the next chunk's, so the CTAs in flight touch few heads and the tiles
+// they share stay in L2.  Within a chunk the order is by "level": level 0 is the
+// most expensive block of every head of the chunk, level 1 the next, and so on
+// (longest first); the most expensive block is the last one for query blocks
+// under a causal mask (`from_end`), the first for key blocks.  A wider chunk
+// shortens the tail (the last chunk's long items start earlier) at the price of
+// a larger working set.  Returns false for CTAs beyond the real work (packed
+// batches launch an upper bound).
 __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int heads,
-                                         bool from_end, int& b, int& h, int& blk) {
+                                         bool from_end, int& b, int& h, int& blk,
+                                         int chunk = kHeadChunk) {
     int n, first_bh, nbh, r;   // blocks per head, first (seq, head) pair of the range, pairs, index
     if (!s.cu_seqlens) {
         n = ceil_div(s.N, rows);
         const int pairs = s.B * heads;
         if (w >= n * pairs) return false;
-        const int chunk = w / (n * kHeadChunk);
-        first_bh = chunk * kHeadChunk;
-        nbh = min(kHeadChunk, pairs - first_bh);
+        const int c = w / (n * chunk);
+        first_bh = c * chunk;
+        nbh = min(chunk, pairs - first_bh);
         r = w - first_bh * n;
     } else {
         // sequences in order; within a sequence its heads in chunks
@@ -95,10 +97,10 @@ __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int 
         }
         if (b >= s.B) return false;
         const int idx = w - base;
-        const int chunk = idx / (n * kHeadChunk);
-        first_bh = b * heads + chunk * kHeadChunk;
-        nbh = min(kHeadChunk, heads - chunk * kHeadChunk);
-        r = idx - chunk * kHeadChunk * n;
+        const int c = idx / (n * chunk);
+        first_bh = b * heads + c * chunk;
+        nbh = min(chunk, heads - c * chunk);
+        r = idx - c * chunk * n;
     }
     const int level = r / nbh;
     const int bh = first_bh + r % nbh;
