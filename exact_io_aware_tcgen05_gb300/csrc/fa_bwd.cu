@@ -41,19 +41,41 @@ constexpr float kPosInf = __builtin_huge_valf();
 // ------------------------------------------------------------- preprocess
 
 // D_i = sum_c dO_ic O_ic in fp32 for every (token, query head).  A group of
-// D/8 lanes handles one row, 8 elements (16 bytes) per lane.  E: element type.
+// D/8 lanes handles one row, 8 elements (16 bytes) per lane; a CTA takes
+// kPrePasses passes of 256 / (D/8) consecutive rows, all of whose loads are
+// issued before the first sum, so that every thread keeps 2 kPrePasses
+// 16-byte loads in flight.  E: element type.
+constexpr int kPrePasses = 4;
+constexpr int kPreThreads = 256;
+
+template <int D>
+constexpr int pre_rows_per_cta() { return kPrePasses * (kPreThreads / (D / 8)); }
+
 template <int D, int E>
-__global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const __grid_constant__ BwdParams p) {
     constexpr int kLanesPerRow = D / 8;
+    constexpr int kRowsPerPass = kPreThreads / kLanesPerRow;
     const SeqInfo& s = p.seq;
     const long long rows = static_cast<long long>(s.total_tokens) * s.Hq;
-    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kLanesPerRow;
+    const long long row0 = static_cast<long long>(blockIdx.x) * pre_rows_per_cta<D>() +
+                           threadIdx.x / kLanesPerRow;
     const int sub = threadIdx.x % kLanesPerRow;
-    float acc = 0.f;
-    if (row < rows) {
-        const uint4 o4 = reinterpret_cast<const uint4*>(p.o)[row * kLanesPerRow + sub];
-        const uint4 d4 = reinterpret_cast<const uint4*>(p.dout)[row * kLanesPerRow + sub];
-        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+    uint4 o4[kPrePasses], d4[kPrePasses];
+#pragma unroll
+    for (int k = 0; k < kPrePasses; ++k) {
+        const long long row = row0 + k * kRowsPerPass;
+        o4[k] = d4[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < rows) {
+            o4[k] = reinterpret_cast<const uint4*>(p.o)[row * kLanesPerRow + sub];
+            d4[k] = reinterpret_cast<const uint4*>(p.dout)[row * kLanesPerRow + sub];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPrePasses; ++k) {
+        const long long row = row0 + k * kRowsPerPass;
+        const uint32_t ow[4] = {o4[k].x, o4[k].y, o4[k].z, o4[k].w};
+        const uint32_t dw[4] = {d4[k].x, d4[k].y, d4[k].z, d4[k].w};
+        float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 a = unpack2<E>(ow[i]);
@@ -61,16 +83,16 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const __grid_con
             acc = fmaf(a.x, c.x, acc);
             acc = fmaf(a.y, c.y, acc);
         }
-    }
 #pragma unroll
-    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanesPerRow);
-    if (row < rows && sub == 0) {
-        const int token = static_cast<int>(row / s.Hq), h = static_cast<int>(row % s.Hq);
-        long long idx;
-        if (s.cu_seqlens) idx = static_cast<long long>(h) * s.total_tokens + token;
-        else idx = (static_cast<long long>(token / s.N) * s.Hq + h) * s.N + token % s.N;
-        p.delta[idx] = acc;
+        for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanesPerRow);
+        if (row < rows && sub == 0) {
+            const int token = static_cast<int>(row / s.Hq), h = static_cast<int>(row % s.Hq);
+            long long idx;
+            if (s.cu_seqlens) idx = static_cast<long long>(h) * s.total_tokens + token;
+            else idx = (static_cast<long long>(token / s.N) * s.Hq + h) * s.N + token % s.N;
+            p.delta[idx] = acc;
+        }
     }
 }
 
@@ -927,17 +949,16 @@ cudaError_t launch_tc(K kern, int grid, int threads, int smem, const BwdParams& 
 
 cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.seq.total_tokens) * p.seq.Hq;
-    const int lanes = d / 8;
-    const long long threads = rows * lanes;
-    const int grid = static_cast<int>((threads + 255) / 256);
+    const int per_cta = d == 128 ? pre_rows_per_cta<128>() : pre_rows_per_cta<64>();
+    const int grid = static_cast<int>((rows + per_cta - 1) / per_cta);
     if (grid <= 0) return cudaSuccess;
     const bool f16 = p.elem == kElemF16;
     if (d == 128) {
-        if (f16) fa_bwd_preprocess_kernel<128, kElemF16><<<grid, 256, 0, stream>>>(p);
-        else fa_bwd_preprocess_kernel<128, kElemBf16><<<grid, 256, 0, stream>>>(p);
+        if (f16) fa_bwd_preprocess_kernel<128, kElemF16><<<grid, kPreThreads, 0, stream>>>(p);
+        else fa_bwd_preprocess_kernel<128, kElemBf16><<<grid, kPreThreads, 0, stream>>>(p);
     } else {
-        if (f16) fa_bwd_preprocess_kernel<64, kElemF16><<<grid, 256, 0, stream>>>(p);
-        else fa_bwd_preprocess_kernel<64, kElemBf16><<<grid, 256, 0, stream>>>(p);
+        if (f16) fa_bwd_preprocess_kernel<64, kElemF16><<<grid, kPreThreads, 0, stream>>>(p);
+        else fa_bwd_preprocess_kernel<64, kElemBf16><<<grid, kPreThreads, 0, stream>>>(p);
     }
     return cudaGetLastError();
 }
