@@ -19,6 +19,11 @@ SMALL = [
     (6, 4, 2, 513, 64, True, 0, (1, 127, 128, 129, 300, 513)),
     (3, 2, 1, 900, 128, False, 0, (900, 5, 256)),
     (4, 4, 1, 700, 128, True, 100, (700, 33, 256, 1)),
+    # the backward's work order takes heads in chunks of 8: 18 query-head pairs (dQ:
+    # 8 + 8 + 2) and 9 key/value-head pairs (dK/dV: 8 + 1); packed, 12 query heads
+    # per sequence (8 + 4)
+    (3, 6, 3, 300, 128, True, 0, None),
+    (2, 12, 4, 300, 64, True, 0, (300, 77)),
 ]
 
 

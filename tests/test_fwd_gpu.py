@@ -20,6 +20,13 @@ SMALL = [
     (6, 4, 2, 513, 64, True, 0, (1, 127, 128, 129, 300, 513)),
     (3, 2, 1, 900, 128, False, 0, (900, 5, 256)),
     (4, 4, 1, 700, 128, True, 100, (700, 33, 256, 1)),
+    # 2 MB of K and V per head: the work order takes heads in chunks of 8, so 10
+    # (sequence, head) pairs make a full chunk and a partial one; packed, 12 query
+    # heads per sequence do the same within each sequence
+    (1, 10, 5, 4096, 128, True, 0, None),
+    (2, 12, 4, 4096, 128, True, 0, (4096, 300)),
+    # 1 MB per head: chunks of 16, so 20 pairs make 16 + 4
+    (2, 10, 10, 2048, 128, True, 0, None),
 ]
 
 
