@@ -404,6 +404,7 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.elem = static_cast<int>(dtype);
     p.drop = drop;
     p.seq = g.seq;
+    p.q = q;
     p.o = o;
     p.dout = dout;
     p.lse = lse;

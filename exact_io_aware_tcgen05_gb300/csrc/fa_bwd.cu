@@ -110,7 +110,11 @@ struct BwdCfg {
     // steps; odd items (dO_n, V_j) about half a step.  Separate rings give each
     // kind a prefetch distance of its own.
     static constexpr int kSlotsOdd = (D == 128) ? 2 : 3;
-    static constexpr int kSlotsEven = kSlots - kSlotsOdd;
+    // The dQ kernel keeps Q and dO in TMEM (below), so every tile of shared memory
+    // belongs to its ring: 7 (d = 128) or 10 (d = 64) slots, of which V_j takes
+    // kSlotsOddDq.
+    static constexpr int kSlotsDq = kSlots + 2;
+    static constexpr int kSlotsOddDq = (D == 128) ? 2 : 3;
     // element-wise warpgroups, each owning kEwCols of the 128 tile columns: d = 64 has
     // half the tensor work per tile of d = 128 and the same element-wise work, so it
     // gets twice the element-wise warps
@@ -131,7 +135,11 @@ struct BwdCfg {
     static constexpr int kColS = 0;          // S (or S^T), 128 fp32 columns
     static constexpr int kColDP = 128;       // dP (or dP^T), 128 fp32 columns
     static constexpr int kColAcc = 256;      // accumulators: dQ, or dV then dK (D each)
-    static constexpr int kColDP1 = 384;      // dQ kernel only: second dP buffer
+    // dQ kernel: Q and dO of the query tile, the A operands of S and dP, packed two
+    // elements per 32-bit column (D/2 columns each) after the dQ accumulator
+    static constexpr int kColQ = kColAcc + D;
+    static constexpr int kColDO = kColQ + D / 2;
+    static_assert(kColDO + D / 2 <= kTmemCols, "TMEM columns");
     // [barriers 512 B][row statistics: warpgroups x 2 buffers x 2 kEwCols fp32][pad] then
     // tiles: resident pair (K,V or Q,dO) followed by the slot ring
     static constexpr int kBarBytes = 512;
@@ -146,8 +154,8 @@ static_assert(BwdCfg<64>::kSmemBytes <= 232448, "shared memory budget");
 // named barrier ids (0 is __syncthreads): element-wise results (and streamed
 // tiles) ready for the issuer's next products
 constexpr int kBarP = 1;     // P (P^T) written / S read
-constexpr int kBarDS0 = 2;   // dS (dS^T) written; the dQ kernel alternates kBarDS0 / kBarDS1
-constexpr int kBarDS1 = 3;
+constexpr int kBarDS0 = 2;   // dS (dS^T) written
+constexpr int kBarOperands = 3;  // dQ kernel: Q and dO copied into TMEM
 constexpr int kBarEpi = 4;   // element-wise warps among themselves: the epilogue
 constexpr int kBarStat = 5;  // + warpgroup: a dK/dV element-wise warpgroup's row statistics staged
 
@@ -156,8 +164,8 @@ struct BwdBars {
     uint64_t s_full;          // S (S^T) tile computed
     uint64_t dp_full[2];      // dP (dP^T) tile computed, per dP buffer
     uint64_t acc_full;        // all accumulation done
-    uint64_t slot_full[8];    // streamed tile landed in slot
-    uint64_t slot_empty[8];   // streamed tile consumed
+    uint64_t slot_full[10];   // streamed tile landed in slot
+    uint64_t slot_empty[10];  // streamed tile consumed
     uint32_t tmem_base;
     int abort;
 };
@@ -195,6 +203,30 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_region, uin
         mma_ts(d_tmem, a_region + (16 * kk / C::kEwCols) * C::kEwCols + (16 * kk % C::kEwCols) / 2,
                bd + ((kk * 2048) >> 4),
                kIdescTS, (acc || kk > 0) ? 1u : 0u);
+}
+
+// N consecutive 32-bit TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[N]) {
+    static_assert(N == 8 || N == 16 || N == 32, "TMEM store width");
+    if constexpr (N == 32) tmem_st32(taddr, w);
+    else if constexpr (N == 16) tmem_st16(taddr, w);
+    else tmem_st8(taddr, w);
+}
+
+// A = 16-bit operand held whole in TMEM (128 rows x D, packed two per 32-bit
+// column, D/2 contiguous columns) . b[smem rows: K-major 128 x D]^T -> tmem
+// (128 x 128 fp32): the dQ kernel's S = Q K^T and dP = dO V^T.
+template <int D, int E>
+__device__ __forceinline__ void issue_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t b) {
+    using C = BwdCfg<D>;
+    constexpr uint32_t kIdesc = idesc_f32acc(kBlockM, kBlockN, false, false, E);
+    const uint64_t bd = sdesc_sw128(b, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+        mma_ts(d_tmem, a_tmem + 8 * kk, bd + off, kIdesc, kk > 0 ? 1u : 0u);
+    }
 }
 
 // NC fp32 columns of a TMEM accumulator row * mul -> element type E in global memory.
@@ -287,7 +319,7 @@ __device__ __forceinline__ bool smem_base_ok(const uint8_t* base, int* status) {
 }
 
 template <int D>
-__device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
+__device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp, int slots) {
     if (threadIdx.x == 0) {
         bars->abort = 0;
         mbar_init(smem_addr(&bars->res_full), 1);
@@ -296,7 +328,7 @@ __device__ __forceinline__ void init_bwd_cta(BwdBars* bars, int warp) {
             mbar_init(smem_addr(&bars->dp_full[i]), 1);
         }
         mbar_init(smem_addr(&bars->acc_full), 1);
-        for (int i = 0; i < BwdCfg<D>::kSlots; ++i) {
+        for (int i = 0; i < slots; ++i) {
             mbar_init(smem_addr(&bars->slot_full[i]), 1);
             mbar_init(smem_addr(&bars->slot_empty[i]), 1);
         }
@@ -323,20 +355,25 @@ __device__ __forceinline__ void teardown_bwd_cta(BwdBars* bars, int warp) {
     }
 }
 
-// Slot ring of streamed item i: physical slot, and use count of that slot.
-template <int D>
-__device__ __forceinline__ int slot_index(int i) {
-    using C = BwdCfg<D>;
-    const int k = i >> 1;
-    return (i & 1) ? C::kSlotsEven + k % C::kSlotsOdd : k % C::kSlotsEven;
-}
-
-template <int D>
-__device__ __forceinline__ int slot_use(int i) {
-    using C = BwdCfg<D>;
-    const int k = i >> 1;
-    return (i & 1) ? k / C::kSlotsOdd : k / C::kSlotsEven;
-}
+// Slot ring of SLOTS tiles for a stream of items that alternate between two
+// kinds: the odd items take ODD slots, the even ones the rest.  index(i) is item
+// i's slot, use(i) how many items used that slot before it.  Each kind gets at
+// least two slots: with one, a wait for item i + 2 on the slot's mbarrier could
+// complete on the phase of item i if that item had not landed yet.
+template <int SLOTS, int ODD>
+struct Ring {
+    static constexpr int kSlots = SLOTS;
+    static constexpr int kEven = SLOTS - ODD;
+    static_assert(ODD >= 2 && kEven >= 2, "two slots per kind of item");
+    __device__ static __forceinline__ int index(int i) {
+        const int k = i >> 1;
+        return (i & 1) ? kEven + k % ODD : k % kEven;
+    }
+    __device__ static __forceinline__ int use(int i) {
+        const int k = i >> 1;
+        return (i & 1) ? k / ODD : k / kEven;
+    }
+};
 
 // Warp-uniform bounded wait (the TMEM accesses that follow are warp-collective).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -345,18 +382,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Producer loop shared by both kernels: streams `items` tiles through the slot
-// ring (item i from map (i & 1) ? odd : even); `coords(i, head, row)` gives the
-// head and token row of item i.
-template <int D, typename Coords>
+// ring R (item i from map (i & 1) ? odd : even); `coords(i, head, row)` gives the
+// head and token row of item i.  `resident`: the CTA also loaded a resident pair
+// on res_full, which an abort has to wait for too.
+template <int D, typename R, typename Coords>
 __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int items,
                                              const CUtensorMap* even, const CUtensorMap* odd,
                                              Coords coords, volatile int* abort_flag,
-                                             const BwdParams& p) {
+                                             const BwdParams& p, bool resident) {
     using C = BwdCfg<D>;
     const uint64_t keep = make_l2_policy_evict_last();
     int issued = 0;
     for (int i = 0; i < items; ++i) {
-        const int sl = slot_index<D>(i), use = slot_use<D>(i);
+        const int sl = R::index(i), use = R::use(i);
         if (use > 0 && !mbar_wait(smem_addr(&bars->slot_empty[sl]), (use - 1) & 1, abort_flag,
                                   p.timeout_cycles, p.status))
             break;
@@ -371,14 +409,14 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
         issued = i + 1;
     }
     if (*abort_flag) {
-        mbar_wait_drain(smem_addr(&bars->res_full), 0, kDrainCycles);
+        if (resident) mbar_wait_drain(smem_addr(&bars->res_full), 0, kDrainCycles);
         // the last item issued into each slot
         unsigned seen = 0;
-        for (int i = issued - 1; i >= 0 && i >= issued - 2 * C::kSlots; --i) {
-            const int sl = slot_index<D>(i);
+        for (int i = issued - 1; i >= 0 && i >= issued - 2 * R::kSlots; --i) {
+            const int sl = R::index(i);
             if (seen & (1u << sl)) continue;
             seen |= 1u << sl;
-            mbar_wait_drain(smem_addr(&bars->slot_full[sl]), slot_use<D>(i) & 1, kDrainCycles);
+            mbar_wait_drain(smem_addr(&bars->slot_full[sl]), R::use(i) & 1, kDrainCycles);
         }
     }
 }
@@ -406,6 +444,7 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
 template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    using R = Ring<C::kSlots, C::kSlotsOdd>;   // Q_n (even) and dO_n (odd)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the dQ kernel reads nothing this kernel writes: let it start on SMs this
     // grid's last CTAs leave idle
@@ -431,7 +470,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    init_bwd_cta<D>(bars, warp);
+    init_bwd_cta<D>(bars, warp, C::kSlots);
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
@@ -444,13 +483,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                 tma_load_3d(smem_addr(sK + c * C::kChunkBytes), &p.tm_k, rb, c * 64, g, seq_start + kb);
                 tma_load_3d(smem_addr(sV + c * C::kChunkBytes), &p.tm_v, rb, c * 64, g, seq_start + kb);
             }
-            stream_tiles<D>(bars, sSlots, 2 * nsteps, &p.tm_q, &p.tm_do,
+            stream_tiles<D, R>(bars, sSlots, 2 * nsteps, &p.tm_q, &p.tm_do,
                             [&](int i, int& head, int& row) {
                                 const int n = i / 2;
                                 head = g * s.group + n / nq;
                                 row = seq_start + (qt_first + n % nq) * kBlockM;
                             },
-                            abort_flag, p);
+                            abort_flag, p, true);
         }
     } else if (warp == 1) {
         regs_lower<C::kRegsCtl>();
@@ -459,15 +498,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
         // warp-collective); lane 0 issues.  It never waits on an mbarrier inside
         // the loop and does not look at the abort flag: after an abort it keeps
         // issuing (on stale data) so that every barrier phase still completes.
-        auto slot = [&](int i) { return smem_addr(sSlots + slot_index<D>(i) * C::kTileBytes); };
-        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[slot_index<D>(i)])); };
+        auto slot = [&](int i) { return smem_addr(sSlots + R::index(i) * C::kTileBytes); };
+        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[R::index(i)])); };
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
         if (lane == 0) {
             auto wait = [&](uint64_t& bar, int parity) {
                 return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
             };
-            if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
-                wait(bars->slot_full[slot_index<D>(1)], 0)) {}
+            if (wait(bars->res_full, 0) && wait(bars->slot_full[R::index(0)], 0) &&
+                wait(bars->slot_full[R::index(1)], 0)) {}
             tc_fence_after();
             issue_ss<D, E>(tmem + C::kColS, aK, slot(0));      // S^T_0 = K Q_0^T
             mma_commit(smem_addr(&bars->s_full));
@@ -509,13 +548,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
         for (int n = 0; n < nsteps; ++n) {
             const bool more = n + 1 < nsteps;
             if (lane == 0 && more)
-                mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(2 * n + 2)]),
-                          slot_use<D>(2 * n + 2) & 1, abort_flag, p.timeout_cycles, p.status);
+                mbar_wait(smem_addr(&bars->slot_full[R::index(2 * n + 2)]),
+                          R::use(2 * n + 2) & 1, abort_flag, p.timeout_cycles, p.status);
             __syncwarp();
             named_bar_sync(kBarP, C::kBarCount);
             if (lane == 0 && more)
-                mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(2 * n + 3)]),
-                          slot_use<D>(2 * n + 3) & 1, abort_flag, p.timeout_cycles, p.status);
+                mbar_wait(smem_addr(&bars->slot_full[R::index(2 * n + 3)]),
+                          R::use(2 * n + 3) & 1, abort_flag, p.timeout_cycles, p.status);
             __syncwarp();
             named_bar_sync(kBarDS0, C::kBarCount);
         }
@@ -689,19 +728,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 
 // ---------------------------------------------------------------------- dQ
 //
-// Per key tile j the issuer runs S_j and dP_j; as soon as the element-wise
-// warps have read S_j into registers it issues S_{j+1} and dP_{j+1} (dP
-// alternates between two TMEM buffers), and when dS_j is back in TMEM (over
-// dP_j) it issues dQ += dS_j K_j.  The tensor cores thus compute the next
-// tile's S and dP while the element-wise warps turn dP_j into dS_j.  K_j and
-// V_j stream through the slot ring as items 2j and 2j+1; V_j's slot is
-// released as soon as dP_j is done, K_j's after dQ_j.  dp_full has one
-// mbarrier per dP buffer and "dS_j written" alternates between two named
-// barriers, so no signal can run two phases ahead of its waiter.
+// Q and dO of the CTA's query tile live in TMEM, copied there row by row by the
+// element-wise warps at the start, as the A operands of S_j = Q K_j^T and dP_j =
+// dO V_j^T; shared memory holds only the K/V slot ring (7 slots at d = 128: 5 for
+// K_j, 2 for V_j; K_j is held from S_j to dQ_j, about one and a half steps, and
+// the deeper ring lets its load start well before it is needed).  Per key tile j:
+// as soon as the element-wise warps have read S_j into registers the issuer runs
+// S_{j+1}; when dS_j is back in TMEM (over dP_j) it runs dQ += dS_j K_j and then
+// dP_{j+1} into the same columns (tcgen05 ops of one thread execute in issue
+// order, so dQ_j has read dS_j first).  K_j and V_j stream through the ring as
+// items 2j and 2j+1; V_j's slot is released after dP_j, K_j's after dQ_j.  Every
+// signal waits for its waiter's previous phase: S_{j+1} needs S_j read, dP_{j+1}
+// needs dS_j written, so no mbarrier or named barrier runs two phases ahead.
 
 template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    using R = Ring<C::kSlotsDq, C::kSlotsOddDq>;   // K_j (even) and V_j (odd)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Launched as a programmatic dependent of the dK/dV kernel: it may start while
     // that grid finishes.  Before exiting, every CTA waits for that grid, so the
@@ -723,72 +766,63 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     const int nk = kt_last - kt_first + 1;
 
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
-    uint8_t* sQ = smem_raw + C::kHeadBytes;
-    uint8_t* sDO = sQ + C::kTileBytes;
-    uint8_t* sSlots = sDO + C::kTileBytes;
+    uint8_t* sSlots = smem_raw + C::kHeadBytes;
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    init_bwd_cta<D>(bars, warp);
+    init_bwd_cta<D>(bars, warp, C::kSlotsDq);
     const uint32_t tmem = bars->tmem_base;
+    constexpr int kOperandBar = C::kEwThreads + 32;   // element-wise warps + the issuer
 
     if (warp == 0) {
         regs_lower<C::kRegsCtl>();
-        if (lane == 0) {
-            const uint32_t rb = smem_addr(&bars->res_full);
-            mbar_arrive_expect_tx(rb, 2 * C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(smem_addr(sQ + c * C::kChunkBytes), &p.tm_q, rb, c * 64, h, seq_start + q0);
-                tma_load_3d(smem_addr(sDO + c * C::kChunkBytes), &p.tm_do, rb, c * 64, h, seq_start + q0);
-            }
-            stream_tiles<D>(bars, sSlots, 2 * nk, &p.tm_k, &p.tm_v,
-                            [&](int i, int& head, int& row) {
-                                head = g;
-                                row = seq_start + (kt_first + i / 2) * kBlockN;
-                            },
-                            abort_flag, p);
-        }
+        if (lane == 0)
+            stream_tiles<D, R>(bars, sSlots, 2 * nk, &p.tm_k, &p.tm_v,
+                               [&](int i, int& head, int& row) {
+                                   head = g;
+                                   row = seq_start + (kt_first + i / 2) * kBlockN;
+                               },
+                               abort_flag, p, false);
     } else if (warp == 1) {
         regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ MMA issuer
         // (whole warp walks the tiles, lane 0 issues; as in the dK/dV kernel it
         // never waits on an mbarrier inside the loop)
-        auto slot = [&](int i) { return smem_addr(sSlots + slot_index<D>(i) * C::kTileBytes); };
-        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[slot_index<D>(i)])); };
-        auto dp_col = [&](int j) { return tmem + ((j & 1) ? C::kColDP1 : C::kColDP); };
-        const uint32_t aQ = smem_addr(sQ), aDO = smem_addr(sDO);
+        auto slot = [&](int i) { return smem_addr(sSlots + R::index(i) * C::kTileBytes); };
+        auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[R::index(i)])); };
+        const uint32_t tQ = tmem + C::kColQ, tDO = tmem + C::kColDO, tDP = tmem + C::kColDP;
+        named_bar_sync(kBarOperands, kOperandBar);        // Q and dO are in TMEM
         if (lane == 0) {
             auto wait = [&](uint64_t& bar, int parity) {
                 return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
             };
-            if (wait(bars->res_full, 0) && wait(bars->slot_full[slot_index<D>(0)], 0) &&
-                wait(bars->slot_full[slot_index<D>(1)], 0)) {}
+            if (wait(bars->slot_full[R::index(0)], 0) && wait(bars->slot_full[R::index(1)], 0)) {}
             tc_fence_after();
-            issue_ss<D, E>(tmem + C::kColS, aQ, slot(0));       // S_0 = Q K_0^T
+            issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(0));    // S_0 = Q K_0^T
             mma_commit(smem_addr(&bars->s_full));
-            issue_ss<D, E>(dp_col(0), aDO, slot(1));            // dP_0 = dO V_0^T
+            issue_ts_k<D, E>(tDP, tDO, slot(1));               // dP_0 = dO V_0^T
             mma_commit(smem_addr(&bars->dp_full[0]));
             free_slot(1);
         }
         __syncwarp();
         for (int j = 0; j < nk; ++j) {
-            named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} and V_{j+1} landed
+            named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} landed
             if (lane == 0 && j + 1 < nk) {
-                // S_{j+1} once S_j is in registers; dP_{j+1} into the other buffer,
-                // whose dS_{j-1} the already issued dQ_{j-1} reads first
                 tc_fence_after();
-                issue_ss<D, E>(tmem + C::kColS, aQ, slot(2 * j + 2));
+                issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * j + 2));   // S_{j+1}
                 mma_commit(smem_addr(&bars->s_full));
-                issue_ss<D, E>(dp_col(j + 1), aDO, slot(2 * j + 3));
-                mma_commit(smem_addr(&bars->dp_full[(j + 1) & 1]));
-                free_slot(2 * j + 3);
             }
             __syncwarp();
-            named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);   // dS_j written
+            named_bar_sync(kBarDS0, C::kBarCount);          // dS_j written, V_{j+1} landed
             if (lane == 0) {
                 tc_fence_after();
-                issue_ts<D, E>(tmem + C::kColAcc, dp_col(j), slot(2 * j), j > 0);   // dQ += dS K
+                issue_ts<D, E>(tmem + C::kColAcc, tDP, slot(2 * j), j > 0);   // dQ += dS_j K_j
                 free_slot(2 * j);
+                if (j + 1 < nk) {
+                    issue_ts_k<D, E>(tDP, tDO, slot(2 * j + 3));   // dP_{j+1}, after dQ_j read dS_j
+                    mma_commit(smem_addr(&bars->dp_full[0]));
+                    free_slot(2 * j + 3);
+                }
             }
             __syncwarp();
         }
@@ -796,15 +830,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     } else if (warp == 2) {
         regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ slot relay
+        auto wait_item = [&](int i) {
+            mbar_wait(smem_addr(&bars->slot_full[R::index(i)]), R::use(i) & 1, abort_flag,
+                      p.timeout_cycles, p.status);
+        };
         for (int j = 0; j < nk; ++j) {
-            if (lane == 0 && j + 1 < nk) {
-                for (int i = 2 * j + 2; i <= 2 * j + 3; ++i)
-                    mbar_wait(smem_addr(&bars->slot_full[slot_index<D>(i)]), slot_use<D>(i) & 1,
-                              abort_flag, p.timeout_cycles, p.status);
-            }
+            if (lane == 0 && j + 1 < nk) wait_item(2 * j + 2);   // K_{j+1}
             __syncwarp();
             named_bar_sync(kBarP, C::kBarCount);
-            named_bar_sync((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount);
+            if (lane == 0 && j + 1 < nk) wait_item(2 * j + 3);   // V_{j+1}
+            __syncwarp();
+            named_bar_sync(kBarDS0, C::kBarCount);
         }
     } else if (warp == 3) {
         regs_lower<C::kRegsCtl>();   // idle; its warpgroup gives registers away
@@ -816,10 +852,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         const int r = quad * 32 + lane;     // query row within the tile = TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_addr + C::kColS + W * wg;
-        const uint32_t tDP0 = tmem + lane_addr + C::kColDP + W * wg;
-        const uint32_t tDP1 = tmem + lane_addr + C::kColDP1 + W * wg;
+        const uint32_t tDP = tmem + lane_addr + C::kColDP + W * wg;
         const int q = q0 + r;
         const bool valid = q < len;
+        {
+            // Q and dO of row q into TMEM, two elements per 32-bit column as they lie in
+            // memory (the A-operand layout of S and dP): each warpgroup copies kQW of
+            // the D/2 columns; rows past the sequence end are zero
+            constexpr int kQW = D / 2 / C::kEwWG;   // 32 (d = 128) or 8 (d = 64)
+            uint32_t wq[kQW], wd[kQW];
+#pragma unroll
+            for (int i = 0; i < kQW; ++i) wq[i] = wd[i] = 0u;
+            if (valid) {
+                const long long off = (static_cast<long long>(seq_start + q) * s.Hq + h) * D +
+                                      2 * kQW * wg;
+                const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + off);
+                const uint4* gd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
+#pragma unroll
+                for (int i = 0; i < kQW / 4; ++i) {
+                    const uint4 a = __ldg(gq + i), c = __ldg(gd + i);
+                    wq[4 * i] = a.x; wq[4 * i + 1] = a.y; wq[4 * i + 2] = a.z; wq[4 * i + 3] = a.w;
+                    wd[4 * i] = c.x; wd[4 * i + 1] = c.y; wd[4 * i + 2] = c.z; wd[4 * i + 3] = c.w;
+                }
+            }
+            tmem_st_words<kQW>(tmem + lane_addr + C::kColQ + kQW * wg, wq);
+            tmem_st_words<kQW>(tmem + lane_addr + C::kColDO + kQW * wg, wd);
+            tmem_st_wait();
+            tc_fence_before();
+            named_bar_arrive(kBarOperands, kOperandBar);
+        }
         float lse2 = kPosInf, dlt = 0.f;
         if (valid) {
             const long long idx = row_stat_index(s, b, h, seq_start, q);
@@ -866,12 +927,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                     for (int c = 0; c < W; ++c)
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
-                ok = warp_wait(smem_addr(&bars->dp_full[j & 1]), (j >> 1) & 1, abort_flag,
-                               p.timeout_cycles, p.status);
+                ok = warp_wait(smem_addr(&bars->dp_full[0]), j & 1, abort_flag, p.timeout_cycles,
+                               p.status);
             }
             if (ok) {
                 tc_fence_after();
-                const uint32_t tDP = (j & 1) ? tDP1 : tDP0;
                 float dp[W];
                 tmem_ldw<W>(tDP, dp);
                 if (DROP) {
@@ -891,7 +951,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 tmem_st_wait();
                 tc_fence_before();
             }
-            named_bar_signal((j & 1) ? kBarDS1 : kBarDS0, C::kBarCount, ok);
+            named_bar_signal(kBarDS0, C::kBarCount, ok);
             if (DROP && ok && j + 1 < nk) draw(j + 1);
         }
         if (ok)

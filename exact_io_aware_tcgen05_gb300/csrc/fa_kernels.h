@@ -69,6 +69,7 @@ struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as in FwdParams; dO like Q
     CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs (stores of whole tiles)
     SeqInfo seq;
+    const void* q;      // Q (the dQ kernel copies its query tile's rows into TMEM)
     const void* o;      // forward output (for the preprocess)
     const void* dout;   // dO (for the preprocess)
     const float* lse;   // forward logsumexp, layout as FwdParams::lse
