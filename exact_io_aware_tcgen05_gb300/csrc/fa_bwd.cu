@@ -20,8 +20,9 @@
 //                      TMEM with keys on the TMEM lanes, P^T and dS^T go back
 //                      to TMEM as bf16 and feed dV += P^T dO and dK += dS^T Q
 //   fa_bwd_dq          one CTA per (sequence, query head, 128-row tile); loops
-//                      over the key tiles; S and dP in TMEM, dS (bf16) back to
-//                      TMEM feeds dQ += dS K
+//                      over the key tiles; Q and dO held in TMEM as the A
+//                      operands of S and dP, dS (bf16) back to TMEM feeds
+//                      dQ += dS K
 // Warp roles in both tensor-core kernels: warp 0 TMA producer, warp 1 tcgen05
 // issuer (one thread, owns TMEM), warps 4.. element-wise work + epilogue as two
 // (d = 128) or four (d = 64) warpgroups, each owning 64 or 32 of the 128 tile
@@ -103,7 +104,7 @@ struct BwdCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = kBlockM * 128;
     static constexpr int kTileBytes = kBlockM * D * 2;
-    // ring of single-tile slots for the streamed operands (Q/dO, or K/V)
+    // dK/dV kernel: ring of single-tile slots for the streamed Q_n and dO_n
     static constexpr int kSlots = (D == 128) ? 5 : 8;
     // The streamed items alternate between two rings of slots: even items (Q_n,
     // K_j) are held from their first product to their last, about one and a half
@@ -141,7 +142,8 @@ struct BwdCfg {
     static constexpr int kColDO = kColQ + D / 2;
     static_assert(kColDO + D / 2 <= kTmemCols, "TMEM columns");
     // [barriers 512 B][row statistics: warpgroups x 2 buffers x 2 kEwCols fp32][pad] then
-    // tiles: resident pair (K,V or Q,dO) followed by the slot ring
+    // tiles: dK/dV kernel, the resident pair (K, V) followed by its slot ring; dQ
+    // kernel, all of them its slot ring
     static constexpr int kBarBytes = 512;
     static constexpr int kStatOffset = kBarBytes;
     static constexpr int kHeadBytes = 3072;
