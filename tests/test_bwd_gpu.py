@@ -24,6 +24,12 @@ SMALL = [
     # per sequence (8 + 4)
     (3, 6, 3, 300, 128, True, 0, None),
     (2, 12, 4, 300, 64, True, 0, (300, 77)),
+    # degenerate masks: a window of one key (each query sees only itself), a window
+    # wider than the sequence (plain causal), and a packed batch of 1- to 3-token
+    # sequences
+    (1, 2, 1, 300, 64, True, 1, None),
+    (2, 2, 2, 260, 128, True, 5000, None),
+    (5, 2, 1, 3, 64, True, 0, (1, 2, 3, 1, 1)),
 ]
 
 

@@ -27,6 +27,12 @@ SMALL = [
     (2, 12, 4, 4096, 128, True, 0, (4096, 300)),
     # 1 MB per head: chunks of 16, so 20 pairs make 16 + 4
     (2, 10, 10, 2048, 128, True, 0, None),
+    # degenerate masks: a window of one key (each query sees only itself), a window
+    # wider than the sequence (plain causal), and a packed batch of 1- to 3-token
+    # sequences
+    (1, 2, 1, 300, 64, True, 1, None),
+    (2, 2, 2, 260, 128, True, 5000, None),
+    (5, 2, 1, 3, 64, True, 0, (1, 2, 3, 1, 1)),
 ]
 
 
