@@ -1,0 +1,56 @@
+"""The algorithmic FLOP counts every TFLOP/s figure rests on (CPU only).
+
+workloads.visible_pairs gives the number of (query, key) pairs a sequence's mask
+lets through, in closed form.  Here it is checked against a direct count of the
+mask's definition: key j is visible to query i iff j <= i (causal) and i - j <
+window (window > 0), in one sequence; on small lengths pair by pair, and on every
+benchmarked workload's own lengths with a vectorised count.
+"""
+import numpy as np
+import pytest
+
+from exact_io_aware_tcgen05_gb300.workloads import WORKLOADS, visible_pairs
+
+
+def count_visible(L: int, causal: bool, window: int) -> int:
+    total = 0
+    j = np.arange(L)
+    for i0 in range(0, L, 1024):
+        i = np.arange(i0, min(L, i0 + 1024))[:, None]
+        vis = np.ones((i.shape[0], L), bool)
+        if causal:
+            vis &= j[None, :] <= i
+        if window > 0:
+            vis &= (i - j[None, :]) < window
+        total += int(vis.sum())
+    return total
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_visible_pairs_against_the_mask_pair_by_pair(causal):
+    for L in list(range(1, 41)) + [127, 128, 129, 300]:
+        for window in (0, 1, 2, 5, L - 1, L, L + 3):
+            if window > 0 and not causal:
+                continue        # a window needs the causal mask (rejected by the library)
+            want = sum(1 for i in range(L) for jj in range(L)
+                       if (not causal or jj <= i) and (window <= 0 or i - jj < window))
+            assert visible_pairs(L, causal, window) == want, (L, causal, window)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_workload_pairs_and_flops(name):
+    w = WORKLOADS[name]
+    pairs = sum(count_visible(L, w.causal, w.window) for L in w.seq_lengths())
+    assert w.visible_pairs_per_head() == pairs
+    # forward: S = Q K^T and O = P V, 2 d FLOPs per visible pair each; backward: the
+    # five products S, dP, dV, dK, dQ (the dQ kernel's recomputed S and dP not counted)
+    assert w.fwd_flops() == 4 * w.d * w.Hq * pairs
+    assert w.bwd_flops() == 10 * w.d * w.Hq * pairs
+
+
+def test_closed_forms_of_the_dense_workloads():
+    # causal N(N+1)/2; causal with window W < N: W(W+1)/2 + (N - W) W
+    assert WORKLOADS["fwdbwd_b2_h16_n8192_d128_causal"].visible_pairs_per_head() == 2 * 8192 * 8193 // 2
+    assert WORKLOADS["fwdbwd_b1_h32kv8_n16384_d128_causal_w4096"].visible_pairs_per_head() == \
+        4096 * 4097 // 2 + (16384 - 4096) * 4096
+    assert WORKLOADS["fwd_b1_h1_n128_d64"].visible_pairs_per_head() == 128 * 128
