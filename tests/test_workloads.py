@@ -54,3 +54,18 @@ def test_closed_forms_of_the_dense_workloads():
     assert WORKLOADS["fwdbwd_b1_h32kv8_n16384_d128_causal_w4096"].visible_pairs_per_head() == \
         4096 * 4097 // 2 + (16384 - 4096) * 4096
     assert WORKLOADS["fwd_b1_h1_n128_d64"].visible_pairs_per_head() == 128 * 128
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_io_bytes_are_the_tensors_read_and_written_once(name):
+    """The algorithmic HBM bytes equal the sizes of the tensors each pass reads and
+    writes once, taken from their shapes: the forward reads Q, K, V and writes O and
+    LSE; the backward reads Q, K, V, O, dO and LSE and writes dQ, dK and dV."""
+    w = WORKLOADS[name]
+    n = lambda shape: int(np.prod(shape))
+    q, kv, lse = n(w.q_shape), n(w.kv_shape), n(w.lse_shape)
+    if w.dtype == "fp8":
+        assert w.fwd_io_bytes() == 1 * (q + 2 * kv) + 2 * q + 4 * lse
+    else:
+        assert w.fwd_io_bytes() == 2 * (q + 2 * kv) + 2 * q + 4 * lse
+        assert w.bwd_io_bytes() == 2 * (3 * q + 2 * kv) + 4 * lse + 2 * (q + 2 * kv)
