@@ -155,3 +155,29 @@ def test_fp8_sizes_and_argument_checks(lib):
                                  check=False) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fp8_quantize_v(16, 16, 16, 256, 1, 1, 300, 128, None, 0, None,
                                 check=False) == fa.FA_ERR_INVALID_ARG
+
+
+def _bwd(fa, **over):
+    need = fa.fa_bwd_workspace_size(1, 2, 1, 128, 128, 0)
+    a = dict(q=16, k=16, v=16, o=16, lse=16, dout=16, dq=16, dk=16, dv=16, B=1, Hq=2, Hkv=1,
+             N=128, d=128, causal=1, window=0, cu_seqlens=None, total_tokens=0, scale=0.125,
+             ws=256, ws_bytes=need)
+    a.update(over)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"],
+                     a["dv"], a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["causal"], a["window"],
+                     a["cu_seqlens"], a["total_tokens"], a["scale"], a["ws"], a["ws_bytes"], None,
+                     check=False)
+
+
+@pytest.mark.parametrize("over,status", [
+    *[(dict(**{n: None}), 1) for n in ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv")],
+    *[(dict(**{n: 8}), 1) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")],
+    (dict(d=96), 2), (dict(Hkv=3), 1), (dict(B=0), 1), (dict(N=0), 1),
+    (dict(window=4, causal=0), 1), (dict(scale=0.0), 1),
+])
+def test_backward_rejects_bad_arguments(lib, over, status):
+    """The backward checks every pointer (null, 16-byte alignment), the head grouping,
+    the sizes and the mask flags before anything is enqueued, as the forward does."""
+    fa, _ = lib
+    assert _bwd(fa, **over) == status
+    assert fa.fa_last_error() != ""
