@@ -162,7 +162,9 @@ def quantize_v(v, B: int, N: int, cu_seqlens=None, vt_tokens=None):
     for b, (start, L) in enumerate(seqs):
         for h in range(H):
             blk = vf[start:start + L, h]
-            s = _f32_scale(np.max(np.abs(blk)))
+            # an empty sequence has amax 0 (the max over no magnitudes), so scale 1,
+            # as for an all-zero block
+            s = _f32_scale(np.max(np.abs(blk)) if blk.size else 0.0)
             scales[h, b] = s
             vt[h, :, offs[b]:offs[b] + L] = _encode_scaled(blk, s).T
     return vt, scales

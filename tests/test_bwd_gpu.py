@@ -30,6 +30,8 @@ SMALL = [
     (1, 2, 1, 300, 64, True, 1, None),
     (2, 2, 2, 260, 128, True, 5000, None),
     (5, 2, 1, 3, 64, True, 0, (1, 2, 3, 1, 1)),
+    # empty sequences in a packed batch (no work items; the others unaffected)
+    (4, 4, 2, 130, 64, True, 0, (5, 0, 130, 0)),
 ]
 
 
