@@ -185,9 +185,9 @@ fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
  *   v_scale  [Hkv, B]: one per (key/value head, sequence).
  * The values are code * scale.  fa_fp8_quantize_qk / fa_fp8_quantize_v write
  * these from bf16 tensors in the layouts of fa_fwd: per block (Q, K) or per
- * (sequence, head) (V), scale = amax / 448 in float (1 for an all-zero block, and
- * for the V of an empty sequence)
- * and code = e4m3(x / scale) with the division rounded to nearest in float.
+ * (sequence, head) (V), scale = amax / 448 in float (1 for an all-zero block,
+ * and for the V of an empty sequence) and code = e4m3(x / scale) with the
+ * division rounded to nearest in float.
  *
  * fa_fwd_fp8 computes O (bf16, layout of fa_fwd) and LSE (fp32, layout of
  * fa_fwd) of exact attention on those values, with the arguments and masks of
