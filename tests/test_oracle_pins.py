@@ -267,9 +267,10 @@ def test_gqa_equals_repeated_heads(oracle_mod):
     np.testing.assert_allclose(dv, dv2.reshape(B, N, Hkv, Hq // Hkv, d).sum(3), atol=1e-13)
 
 
-def test_packed_batch_equals_independent_sequences(oracle_mod):
-    """A packed batch equals one call per sequence (no attention across sequences)."""
-    lengths = [5, 1, 17, 9]
+@pytest.mark.parametrize("lengths", [[5, 1, 17, 9], [5, 0, 1, 17, 0, 9, 0]])
+def test_packed_batch_equals_independent_sequences(oracle_mod, lengths):
+    """A packed batch equals one call per sequence (no attention across sequences);
+    empty sequences add nothing and leave the others unchanged."""
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     T, Hq, Hkv, d = int(cu[-1]), 4, 2, 8
     rng = np.random.default_rng(41)
@@ -279,6 +280,8 @@ def test_packed_batch_equals_independent_sequences(oracle_mod):
     o, lse = oracle_mod.attention_fwd(q, k, v, cu_seqlens=cu, **kw)
     dq, dk, dv = oracle_mod.attention_bwd(q, k, v, do, cu_seqlens=cu, **kw)
     for b, L in enumerate(lengths):
+        if L == 0:
+            continue
         s = slice(cu[b], cu[b + 1])
         ob, lb = oracle_mod.attention_fwd(q[s][None], k[s][None], v[s][None], **kw)
         np.testing.assert_allclose(o[s], ob[0], atol=1e-14)
