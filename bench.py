@@ -48,11 +48,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # Algorithmic FLOPs per visible pair and query head, split by kernel: the
 # forward's two products; of the backward's five products (S recomputed, dP,
-# dV, dK, dQ) the dK/dV kernel performs four and the dQ kernel contributes dQ
-# (its second S and dP are recomputation and not counted).
-KERNEL_FLOPS_PER_PAIR_D = {"fa_fwd": 4, "fa_bwd_dkdv": 8, "fa_bwd_dq": 2}
-KERNEL_SOURCES = {"fa_fwd": "fa_fwd.cu", "fa_bwd_dkdv": "fa_bwd.cu", "fa_bwd_dq": "fa_bwd.cu",
-                  "fa_bwd_preprocess": "fa_bwd.cu"}
+# dV, dK, dQ) the fused kernel performs all five; on the split path the dK/dV
+# kernel performs four and the dQ kernel contributes dQ (its second S and dP
+# are recomputation and not counted).
+KERNEL_FLOPS_PER_PAIR_D = {"fa_fwd": 4, "fa_bwd_fused": 10, "fa_bwd_dkdv": 8, "fa_bwd_dq": 2}
+HBM_KERNELS = ("fa_bwd_preprocess", "fa_bwd_dq_convert")
+KERNEL_SOURCES = {"fa_fwd": ("fa_fwd.cu",), "fa_bwd_fused": ("fa_bwd_fused.cu", "fa_bwd_common.cuh"),
+                  "fa_bwd_dkdv": ("fa_bwd.cu", "fa_bwd_common.cuh"),
+                  "fa_bwd_dq": ("fa_bwd.cu", "fa_bwd_common.cuh"),
+                  "fa_bwd_preprocess": ("fa_bwd.cu", "fa_bwd_common.cuh"),
+                  "fa_bwd_dq_convert": ("fa_bwd_fused.cu", "fa_bwd_common.cuh")}
 
 
 def parse_args():
@@ -69,6 +74,9 @@ def parse_args():
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="skip the second timed region with per-kernel events (no roofline)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--bwd-path", choices=["auto", "split", "fused"], default="auto",
+                    help="backward path (fa_bwd_set_path): auto, the library's default choice; "
+                         "split (dK/dV and dQ kernels); fused (one kernel, causal masks)")
     return ap.parse_args()
 
 
@@ -111,7 +119,7 @@ SHARED_SOURCES = ("fa_ptx.cuh", "fa_seq.cuh", "fa_kernels.h")
 def source_sha(kernel: str) -> str:
     """SHA-256 (first 16 hex digits) of the kernel's source file and the shared headers."""
     h = hashlib.sha256()
-    for name in (KERNEL_SOURCES[kernel],) + SHARED_SOURCES:
+    for name in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
         with open(os.path.join(ROOT, "exact_io_aware_tcgen05_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -348,8 +356,15 @@ def run_ours(args, w):
     lse = torch.empty(w.lse_shape, dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(d_in["q"]), torch.empty_like(d_in["k"]),
                   torch.empty_like(d_in["v"]))
-    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
+    ws_size = {"auto": fa.fa_bwd_workspace_size, "split": fa.fa_bwd_workspace_size_min,
+               "fused": fa.fa_bwd_workspace_size_fused}[args.bwd_path]
+    ws_bytes = ws_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    fa.fa_bwd_set_path({"auto": fa.FA_BWD_AUTO, "split": fa.FA_BWD_SPLIT,
+                        "fused": fa.FA_BWD_FUSED}[args.bwd_path])
+    fused = bwd and fa.fa_bwd_path(w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, T,
+                                   ws_bytes) == fa.FA_BWD_FUSED
+    bwd_kernels = 3
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     geo = (w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, cu, T, w.scale)
@@ -454,17 +469,21 @@ def run_ours(args, w):
     elapsed = timed_region(False)
     # Region 2 (per-kernel durations for the roofline): K more steps with the
     # library recording caller-owned CUDA events around each of its launches on
-    # the launching stream.  Events between the backward's launches keep its
-    # dQ kernel from overlapping the end of the dK/dV kernel, so this region is
-    # not used for the step time.
+    # the launching stream.  On the split path, events between the backward's
+    # launches keep its dQ kernel from overlapping the end of the dK/dV kernel, so
+    # this region is not used for the step time.
     kern_ms = None
     if not args.no_kernel_events:
         timed_region(True)
         kern_ms = {"fa_fwd": [a.elapsed_time(b) for a, b in ev_f]}
         if bwd:
             kern_ms["fa_bwd_preprocess"] = [e[0].elapsed_time(e[1]) for e in ev_b]
-            kern_ms["fa_bwd_dkdv"] = [e[1].elapsed_time(e[2]) for e in ev_b]
-            kern_ms["fa_bwd_dq"] = [e[2].elapsed_time(e[3]) for e in ev_b]
+            if fused:
+                kern_ms["fa_bwd_fused"] = [e[1].elapsed_time(e[2]) for e in ev_b]
+                kern_ms["fa_bwd_dq_convert"] = [e[2].elapsed_time(e[3]) for e in ev_b]
+            else:
+                kern_ms["fa_bwd_dkdv"] = [e[1].elapsed_time(e[2]) for e in ev_b]
+                kern_ms["fa_bwd_dq"] = [e[2].elapsed_time(e[3]) for e in ev_b]
     clocks = sampler.stop()
     elapsed = max_over_ranks(elapsed, dev)
     ms_per_step = elapsed / K
@@ -547,7 +566,16 @@ def run_ours(args, w):
                     entry["algorithmic_bytes_per_launch"] = w.fwd_io_bytes()
                     entry["gbs"] = w.fwd_io_bytes() / (mean / 1e3) / 1e9
             else:
-                by = 2 * w.total_tokens * w.Hq * w.d * 2 + 4 * w.total_tokens * w.Hq
+                T_, Hq_, Hkv_, d_ = w.total_tokens, w.Hq, w.Hkv, w.d
+                if name == "fa_bwd_dq_convert":
+                    # int32 sums and row scales in, dQ out
+                    by = 4 * T_ * Hq_ * d_ + 4 * T_ * Hq_ + 2 * T_ * Hq_ * d_
+                else:
+                    # O and dO in, D out; fused: also the row scales out, the int32 sums
+                    # zeroed and K, V read for their bounds
+                    by = 2 * T_ * Hq_ * d_ * 2 + 4 * T_ * Hq_
+                    if fused:
+                        by += 4 * T_ * Hq_ + 4 * T_ * Hq_ * d_ + 2 * T_ * Hkv_ * d_ * 2
                 entry["algorithmic_bytes_per_launch"] = by
                 entry["gbs"] = by / (mean / 1e3) / 1e9
             kernels[name] = entry
@@ -585,7 +613,8 @@ def run_ours(args, w):
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E},
-            "gpu_launches": world * K * (4 if bwd else 1), "clocks": clocks,
+            "gpu_launches": world * K * (1 + (bwd_kernels if bwd else 0)), "clocks": clocks,
+            "bwd_path": ("fused" if fused else "split") if bwd else None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

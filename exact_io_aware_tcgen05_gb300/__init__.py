@@ -18,8 +18,10 @@ import os
 
 __all__ = [
     "FAError", "load", "fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
-    "fa_bwd_dropout", "fa_bwd_workspace_size",
-    "fa_bwd_static_workspace", "FA_DTYPE_BF16", "FA_DTYPE_F16",
+    "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_bwd_workspace_size_min",
+    "fa_bwd_workspace_size_fused", "fa_bwd_set_path", "fa_bwd_path", "FA_BWD_AUTO", "FA_BWD_SPLIT",
+    "FA_BWD_FUSED",
+    "fa_bwd_static_workspace", "FA_STATIC_WORKSPACE_BYTES", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
@@ -35,6 +37,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3:
                 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 
 FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1   # fa_dtype
+FA_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024   # the array of fa_bwd_static_workspace
+FA_BWD_AUTO, FA_BWD_SPLIT, FA_BWD_FUSED = -1, 0, 1   # fa_bwd_path_kind
 
 _lib = None
 _vp, _i, _f, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
@@ -59,6 +63,14 @@ def load(path: str | None = None):
     lib.fa_fwd.restype = _i
     lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
     lib.fa_bwd_workspace_size.restype = _sz
+    lib.fa_bwd_workspace_size_min.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.fa_bwd_workspace_size_min.restype = _sz
+    lib.fa_bwd_workspace_size_fused.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.fa_bwd_workspace_size_fused.restype = _sz
+    lib.fa_bwd_set_path.argtypes = [_i]
+    lib.fa_bwd_set_path.restype = None
+    lib.fa_bwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _sz]
+    lib.fa_bwd_path.restype = _i
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                            _vp, _i, _f, _vp, _sz, _vp]
     lib.fa_bwd.restype = _i
@@ -133,7 +145,30 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_
 
 
 def fa_bwd_workspace_size(B, Hq, Hkv, N, d, total_tokens) -> int:
+    """Workspace bytes of fa_bwd's default choice for this head dimension."""
     return int(load().fa_bwd_workspace_size(B, Hq, Hkv, N, d, int(total_tokens)))
+
+
+def fa_bwd_workspace_size_min(B, Hq, Hkv, N, d, total_tokens) -> int:
+    """The split backward's workspace, the least fa_bwd accepts."""
+    return int(load().fa_bwd_workspace_size_min(B, Hq, Hkv, N, d, int(total_tokens)))
+
+
+def fa_bwd_workspace_size_fused(B, Hq, Hkv, N, d, total_tokens) -> int:
+    """The fused backward's workspace."""
+    return int(load().fa_bwd_workspace_size_fused(B, Hq, Hkv, N, d, int(total_tokens)))
+
+
+def fa_bwd_set_path(path) -> None:
+    """Backward path of this thread's fa_bwd calls: FA_BWD_AUTO, FA_BWD_SPLIT or FA_BWD_FUSED."""
+    load().fa_bwd_set_path(int(path))
+
+
+def fa_bwd_path(B, Hq, Hkv, N, d, causal, window, total_tokens, workspace_bytes) -> int:
+    """FA_BWD_FUSED or FA_BWD_SPLIT: the backward fa_bwd would run on this thread for
+    these arguments (-1: it would fail)."""
+    return int(load().fa_bwd_path(B, Hq, Hkv, N, d, int(bool(causal)), int(window),
+                                  int(total_tokens), int(workspace_bytes)))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
@@ -378,25 +413,37 @@ def attention_forward_fp8(ops: Fp8Operands, *, causal=False, window=0, scale=Non
     return o, lse
 
 
+_PATHS = {"auto": FA_BWD_AUTO, "split": FA_BWD_SPLIT, "fused": FA_BWD_FUSED}
+
+
 def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=None,
                        cu_seqlens=None, max_seqlen=None, stream=None, workspace=None,
-                       dropout=None):
-    """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace)."""
+                       dropout=None, path="auto"):
+    """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace
+    that ``path`` -- "auto", "split" or "fused" -- needs; the path is this thread's
+    preference for the call)."""
     import torch
     dtype = _dtype_code(q, k, v, o, dout)
     B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d, T)
+    size = {"auto": fa_bwd_workspace_size, "split": fa_bwd_workspace_size_min,
+            "fused": fa_bwd_workspace_size_fused}[path]
+    ws_bytes = size(B, Hq, Hkv, N, d, T)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
     ws_given = workspace.numel() * workspace.element_size()
-    if dropout is not None:
-        p_drop, seed, offset = dropout
-        fa_bwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv,
-                       N, d, causal, window, cu_seqlens, T, scale, workspace, ws_given, stream)
-    else:
-        fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, window,
-                     cu_seqlens, T, scale, workspace, ws_given, stream)
+    fa_bwd_set_path(_PATHS[path])
+    try:
+        if dropout is not None:
+            p_drop, seed, offset = dropout
+            fa_bwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, dout, dq, dk, dv, B, Hq,
+                           Hkv, N, d, causal, window, cu_seqlens, T, scale, workspace, ws_given,
+                           stream)
+        else:
+            fa_bwd_typed(dtype, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal,
+                         window, cu_seqlens, T, scale, workspace, ws_given, stream)
+    finally:
+        fa_bwd_set_path(FA_BWD_AUTO)
     return dq, dk, dv

@@ -24,13 +24,20 @@ namespace {
 thread_local char t_last_error[512] = "";
 thread_local const cudaEvent_t* t_events = nullptr;  // armed by fa_set_launch_events
 thread_local int t_event_count = 0;
+thread_local int t_bwd_path = FA_BWD_AUTO;          // fa_bwd_set_path
+
+// Takes (and disarms) the events armed for this call, with their count.
+void take_events_any(const cudaEvent_t** out, int* count) {
+    *out = t_events;
+    *count = t_event_count;
+    t_events = nullptr;
+    t_event_count = 0;
+}
 
 // Takes (and disarms) the events armed for this call; fails if too few.
 fa_status take_events(int kernels, const cudaEvent_t** out) {
-    *out = t_events;
-    const int count = t_event_count;
-    t_events = nullptr;
-    t_event_count = 0;
+    int count = 0;
+    take_events_any(out, &count);
     if (*out && count < kernels + 1) {
         *out = nullptr;
         return FA_ERR_INVALID_ARG;
@@ -95,17 +102,50 @@ fa_status make_token_map(CUtensorMap* map, const void* base, int tokens, int hea
     return FA_OK;
 }
 
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+}  // namespace
+
+unsigned long long current_context_id() {
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PfnCtxGetId>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+namespace {
+
 int* status_word_ptr() {
-    // one address per device; looked up once per device
+    // one address per device and context: looked up again when the device's
+    // context has changed (after cudaDeviceReset the old address is stale)
     static std::mutex mu;
     static int* ptrs[64] = {nullptr};
+    static unsigned long long ctx_ids[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
+    const unsigned long long id = current_context_id();
+    if (!ptrs[dev] || id == 0 || id != ctx_ids[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
         ptrs[dev] = static_cast<int*>(p);
+        ctx_ids[dev] = current_context_id();
     }
     return ptrs[dev];
 }
@@ -223,6 +263,27 @@ fa_status report_error(fa_status st, const char* fmt, ...) {
     return st;
 }
 
+// Workspace of the backward pass for these sizes (false for invalid ones): the
+// fp32 row statistics D, then (fused backward only) the fp32 row scales, the
+// K/V bound slots and the int32 dQ accumulator; each part padded to 256 bytes.
+bool bwd_workspace(int B, int Hq, int Hkv, int N, int d, int total_tokens, BwdWorkspace* w) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128) || total_tokens < 0)
+        return false;
+    auto pad = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    // rows of the token dimension: packed T (total_tokens > 0); dense B * N
+    const long long rows = total_tokens > 0 ? total_tokens : static_cast<long long>(B) * N;
+    w->delta = pad(static_cast<size_t>(rows) * Hq * sizeof(float));
+    w->scale_offset = w->delta;
+    w->bound_offset = w->scale_offset + w->delta;
+    w->acc_offset = w->bound_offset + pad(static_cast<size_t>(Hkv) * kBoundSlots * (d + 1) * sizeof(float));
+    w->full = w->acc_offset + pad(static_cast<size_t>(rows) * Hq * d * sizeof(int));
+    return true;
+}
+
+// The backward fa_bwd runs by default for head dimension d when the mask and the
+// workspace allow the fused one (the path measured faster on GB300).
+bool prefer_fused(int d) { return d == 64; }
+
 }  // namespace fa
 
 using namespace fa;
@@ -320,13 +381,35 @@ fa_status fwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
 extern "C" {
 
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128) || total_tokens < 0)
-        return 0;
-    (void)Hkv;
-    // delta rows: packed [Hq, T] (total_tokens > 0); dense [B, Hq, N]
-    const long long rows = total_tokens > 0 ? total_tokens : static_cast<long long>(B) * N;
-    size_t bytes = static_cast<size_t>(rows) * Hq * sizeof(float);
-    return (bytes + 255) & ~static_cast<size_t>(255);
+    fa::BwdWorkspace w;
+    if (!fa::bwd_workspace(B, Hq, Hkv, N, d, total_tokens, &w)) return 0;
+    return fa::prefer_fused(d) ? w.full : w.delta;
+}
+
+size_t fa_bwd_workspace_size_min(int B, int Hq, int Hkv, int N, int d, int total_tokens) {
+    fa::BwdWorkspace w;
+    return fa::bwd_workspace(B, Hq, Hkv, N, d, total_tokens, &w) ? w.delta : 0;
+}
+
+size_t fa_bwd_workspace_size_fused(int B, int Hq, int Hkv, int N, int d, int total_tokens) {
+    fa::BwdWorkspace w;
+    return fa::bwd_workspace(B, Hq, Hkv, N, d, total_tokens, &w) ? w.full : 0;
+}
+
+void fa_bwd_set_path(int path) {
+    t_bwd_path = (path == FA_BWD_SPLIT || path == FA_BWD_FUSED) ? path : FA_BWD_AUTO;
+}
+
+int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens,
+                size_t workspace_bytes) {
+    fa::BwdWorkspace w;
+    if (!fa::bwd_workspace(B, Hq, Hkv, N, d, total_tokens, &w) || workspace_bytes < w.delta)
+        return -1;
+    (void)window;
+    const bool can_fuse = causal && workspace_bytes >= w.full;
+    if (t_bwd_path == FA_BWD_SPLIT) return FA_BWD_SPLIT;
+    if (t_bwd_path == FA_BWD_FUSED) return can_fuse ? FA_BWD_FUSED : -1;
+    return (can_fuse && fa::prefer_fused(d)) ? FA_BWD_FUSED : FA_BWD_SPLIT;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -372,9 +455,10 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
                    void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal,
                    int window, const int* cu_seqlens, int total_tokens, float scale,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    // the events armed for this call are used up by it, whatever happens
     const cudaEvent_t* ev = nullptr;
-    if (take_events(3, &ev) != FA_OK)
-        return fail(FA_ERR_INVALID_ARG, "fa_bwd: fa_set_launch_events needs >= 4 events");
+    int ev_count = 0;
+    take_events_any(&ev, &ev_count);
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: tensor pointers must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -385,12 +469,28 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     Geometry g;
     st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale, &g);
     if (st != FA_OK) return st;
-    const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, N, d, cu_seqlens ? total_tokens : 0);
-    if (!workspace || workspace_bytes < need)
-        return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace of %zu bytes needed, got %zu%s", need,
-                    workspace_bytes, workspace ? "" : " (null)");
+    BwdWorkspace wl;
+    bwd_workspace(B, Hq, Hkv, N, d, cu_seqlens ? total_tokens : 0, &wl);
+    if (!workspace || workspace_bytes < wl.delta)
+        return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace of at least %zu bytes needed (%zu for the "
+                    "fused backward), got %zu%s", wl.delta, wl.full, workspace_bytes,
+                    workspace ? "" : " (null)");
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace must be 256-byte aligned");
+    // the fused backward (one tensor-core kernel) for causal masks when the workspace
+    // holds its dQ accumulator and the thread's preference allows it; otherwise the
+    // split backward (dK/dV, then dQ)
+    const bool can_fuse = causal && workspace_bytes >= wl.full;
+    if (t_bwd_path == FA_BWD_FUSED && !causal)
+        return fail(FA_ERR_UNSUPPORTED, "fa_bwd: the fused backward serves causal masks only");
+    if (t_bwd_path == FA_BWD_FUSED && !can_fuse)
+        return fail(FA_ERR_WORKSPACE, "fa_bwd: the fused backward needs a workspace of %zu bytes, got %zu",
+                    wl.full, workspace_bytes);
+    const bool fused = t_bwd_path == FA_BWD_FUSED ||
+                       (t_bwd_path == FA_BWD_AUTO && can_fuse && prefer_fused(d));
+    const int kernels = 3;
+    if (ev && ev_count < kernels + 1)
+        return fail(FA_ERR_INVALID_ARG, "fa_bwd: fa_set_launch_events needs >= %d events", kernels + 1);
     if (g.tokens == 0) return FA_OK;
 
     BwdParams p;
@@ -409,6 +509,17 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.dout = dout;
     p.lse = lse;
     p.delta = static_cast<float*>(workspace);
+    p.k_ptr = k;
+    p.v_ptr = v;
+    p.dq_acc = nullptr;
+    p.row_scale = nullptr;
+    p.kv_bound = nullptr;
+    if (fused) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.row_scale = reinterpret_cast<float*>(ws + wl.scale_offset);
+        p.kv_bound = reinterpret_cast<float*>(ws + wl.bound_offset);
+        p.dq_acc = reinterpret_cast<int*>(ws + wl.acc_offset);
+    }
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -419,10 +530,20 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();
     if (!p.status) return fail(FA_ERR_CUDA, "fa_bwd: cannot resolve the device status word");
+    p.pre_row_ctas = bwd_preprocess_row_ctas(p, d);
     cudaError_t e = record(ev, 0, stream);
     if (e == cudaSuccess) e = launch_bwd_preprocess(p, d, stream);
     if (e == cudaSuccess) e = record(ev, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd preprocess launch");
+    if (fused) {
+        e = launch_bwd_fused(p, d, stream);
+        if (e == cudaSuccess) e = record(ev, 2, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "fa_bwd fused launch");
+        e = launch_bwd_dq_convert(p, d, stream);
+        if (e == cudaSuccess) e = record(ev, 3, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dq conversion launch");
+        return FA_OK;
+    }
     e = launch_bwd_dkdv(p, d, stream);
     if (e == cudaSuccess) e = record(ev, 2, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd dk/dv launch");

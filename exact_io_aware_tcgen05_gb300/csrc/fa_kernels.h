@@ -70,10 +70,23 @@ struct BwdParams {
     CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs (stores of whole tiles)
     SeqInfo seq;
     const void* q;      // Q (the dQ kernel copies its query tile's rows into TMEM)
+    const void* k_ptr;  // K, V (the fused backward's preprocess bounds them)
+    const void* v_ptr;
     const void* o;      // forward output (for the preprocess)
     const void* dout;   // dO (for the preprocess)
     const float* lse;   // forward logsumexp, layout as FwdParams::lse
     float* delta;       // fp32 D_i = rowsum(dO * O), same layout as lse
+    // fused backward only (null for the split one).  dQ is summed across CTAs as
+    // fixed-point int32: element (i, c) of every contribution is rounded to a
+    // multiple of 2^-F_ic with F_ic = Fr_i + Fc_gc, where 2^Fr_i = row_scale (from
+    // ||dO_i||) and 2^Fc_gc comes from the K and V bounds (kBoundSlots slots of
+    // tokens per key/value head: max_j |k_jc| for c < d, max_j ||v_j||_2 at d), so
+    // that every partial sum of row i stays below 2^30 in magnitude; integer sums
+    // do not depend on the order of the additions.
+    int* dq_acc;        // d = 128: [Hq, tokens, d]; d = 64: [Hq, d, tokens]
+    float* row_scale;   // 2^Fr_i, layout of lse
+    float* kv_bound;    // [Hkv, kBoundSlots, d + 1]
+    int pre_row_ctas;   // preprocess CTAs over the rows (the bound CTAs follow them)
     void* dq;           // outputs, element type of q
     void* dk;
     void* dv;
@@ -100,13 +113,36 @@ struct Fp8QuantParams {
 // Launchers (defined in the kernel translation units).  They only enqueue on
 // `stream` and return the launch error.
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+int bwd_preprocess_row_ctas(const BwdParams& p, int d);
 cudaError_t launch_bwd_preprocess(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_fused(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert(const BwdParams& p, int d, cudaStream_t stream);
+
+// Slots of tokens per key/value head over which the preprocess takes the maxima
+// of |k_jc| and ||v_j||_2 for the fused backward's fixed-point scales.
+constexpr int kBoundSlots = 32;
 cudaError_t launch_fp8_quant_qk(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream);
 cudaError_t launch_fp8_quant_v(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream);
 
 int* device_status_word();  // library-owned device status word (fa_api.cu)
+
+// Byte layout of the backward workspace (fa_api.cu): D at 0 (`delta` bytes; all
+// the split backward needs), then for the fused backward the row scales, the
+// K/V bound slots and the int32 dQ accumulator; `full` bytes in all.
+struct BwdWorkspace {
+    size_t delta;                     // row statistics D (all the split backward needs)
+    size_t scale_offset, bound_offset, acc_offset;
+    size_t full;                      // + row scales, K/V bound slots, int32 dQ accumulator
+};
+bool bwd_workspace(int B, int Hq, int Hkv, int N, int d, int total_tokens, BwdWorkspace* w);
+
+// Identifier of the calling thread's current CUDA context, unique for the life
+// of the process (0 if no context is current or the driver cannot say).  Device
+// addresses of the library's own __device__ arrays are cached per device and
+// looked up again when this changes, e.g. after cudaDeviceReset.
+unsigned long long current_context_id();
 
 // Records `fmt` as the calling thread's fa_last_error() message; returns st.
 fa_status report_error(fa_status st, const char* fmt, ...);

@@ -383,6 +383,13 @@ __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ------------------------------------------------------- global reductions
+
+// *p += v in L2 (32-bit integer), no return value
+__device__ __forceinline__ void red_add_s32(int* p, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (the

@@ -81,7 +81,7 @@ typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size or flag          */
     FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not in {64, 128})  */
-    FA_ERR_WORKSPACE = 3,    /* workspace null or smaller than fa_bwd_workspace_size  */
+    FA_ERR_WORKSPACE = 3,    /* workspace null, misaligned or below fa_bwd_workspace_size_min */
     FA_ERR_CUDA = 4,         /* a CUDA call failed; see fa_last_error()               */
     FA_ERR_TIMEOUT = 5       /* a kernel's bounded wait gave up (fa_device_status)    */
 } fa_status;
@@ -102,12 +102,50 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int total_tokens, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for these sizes (fp32 row
- * statistics D_i = sum_c dO_ic O_ic, one per query row and head, padded to
- * 256 bytes).  total_tokens: T for a packed batch, 0 for a dense one (whose
- * B * N rows are used).  Returns 0 for invalid sizes.
+ * Backward paths.  fa_bwd runs one of two:
+ *   split  the row statistics D_i = sum_c dO_ic O_ic, a dK/dV kernel, then a dQ
+ *          kernel that rebuilds S and dP a second time (any mask);
+ *   fused  causal masks only: D_i and the fixed-point scales, ONE kernel that
+ *          forms dQ, dK and dV from a single rebuild of each score tile, then a
+ *          kernel that converts the dQ sums.  Several CTAs add into each dQ row;
+ *          each contribution is rounded to fixed point (an int32 multiple of
+ *          2^-F for an F chosen per row and channel from ||dO_i||_2, max_j ||v_j||_2
+ *          and max_j |k_jc|, so that no partial sum exceeds 2^30), and integer sums
+ *          do not depend on the order of the additions.  The rounding adds at most
+ *          (contributing 128-key tiles / 2) 2^-F to an element: about 1e-7 of the
+ *          bound 2 ||dO_i|| max||v_j|| max|k_jc| on |dQ_ic| / scale per tile.
+ * Both are deterministic (the same inputs, workspace size and path give the same
+ * bits); their dQ differ in the last bits.
+ *
+ * Workspace (total_tokens: T for a packed batch, 0 for a dense one, whose B * N
+ * rows are used; 0 for invalid sizes):
+ *   fa_bwd_workspace_size_min    the split backward's: D, one fp32 per query row
+ *                                and head, padded to 256 bytes;
+ *   fa_bwd_workspace_size_fused  the fused backward's: D, the row scales (one
+ *                                fp32 per row and head), the K/V bounds (32 x
+ *                                (d + 1) fp32 per key/value head) and the int32
+ *                                dQ sums (d per row and head), each padded;
+ *   fa_bwd_workspace_size        what the default choice below needs for this d.
+ *
+ * Choice (per calling thread, fa_bwd_set_path): FA_BWD_AUTO, the default, runs
+ * the fused backward where it measured faster on GB300 (d = 64), given a causal
+ * mask and at least fa_bwd_workspace_size_fused bytes, and the split one
+ * otherwise; FA_BWD_SPLIT always runs the split one; FA_BWD_FUSED always runs
+ * the fused one and fails (FA_ERR_UNSUPPORTED without a causal mask,
+ * FA_ERR_WORKSPACE with a smaller workspace).  fa_bwd_path tells which one
+ * fa_bwd would run on the calling thread (-1: it would fail).
  */
+typedef enum fa_bwd_path_kind {
+    FA_BWD_AUTO = -1,
+    FA_BWD_SPLIT = 0,        /* row statistics; dK/dV kernel; dQ kernel (3 kernels) */
+    FA_BWD_FUSED = 1         /* row statistics; fused kernel; dQ conversion (3 kernels) */
+} fa_bwd_path_kind;
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d, int total_tokens);
+size_t fa_bwd_workspace_size_min(int B, int Hq, int Hkv, int N, int d, int total_tokens);
+size_t fa_bwd_workspace_size_fused(int B, int Hq, int Hkv, int N, int d, int total_tokens);
+void fa_bwd_set_path(int path);
+int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens,
+                size_t workspace_bytes);
 
 /*
  * fa_fwd and fa_bwd for an explicit element type: `dtype` gives the type of
@@ -227,11 +265,13 @@ fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const
  * (The pages give no backward formulas; these are the calculus of softmax.)
  *   q, k, v, o, lse, dout   device, read only; o and lse as written by fa_fwd
  *   dq, dk, dv              device, written (bf16, layouts of q, k, v)
- *   workspace               device, >= fa_bwd_workspace_size(...) bytes,
+ *   workspace               device, >= fa_bwd_workspace_size_min(...) bytes
+ *                           (see "Backward paths" for the fused backward's),
  *                           256-byte aligned, contents on entry ignored; it
  *                           must not be shared by calls in flight together
- * dQ, dK and dV are deterministic: the same inputs give the same bits.
- * Enqueues three kernels on `stream`; returns without waiting.
+ * dQ, dK and dV are deterministic: the same inputs, workspace size and path
+ * give the same bits.  Enqueues three kernels on `stream` (either path);
+ * returns without waiting.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
@@ -242,8 +282,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * Backward pass with a built-in workspace, for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point.
  *
- * fa_bwd needs fa_bwd_workspace_size() bytes of device scratch, normally
- * allocated by the caller.  Some callers cannot call cudaMalloc where they
+ * fa_bwd needs device scratch (fa_bwd_workspace_size() bytes for its fused
+ * backward, at least fa_bwd_workspace_size_min()), normally allocated by the
+ * caller.  Some callers cannot call cudaMalloc where they
  * run the backward pass (a framework whose allocator owns all device memory,
  * a plugin that may not allocate behind its host, code that must not
  * allocate because allocation synchronises or may fail mid-step).  This
@@ -252,13 +293,22 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * places in device memory (every GPU that loads the library holds it until
  * the process exits).  It calls no allocating routine.
  *
- *   - Sizes whose workspace exceeds FA_STATIC_WORKSPACE_BYTES (Hq * tokens
- *     fp32 row statistics, i.e. Hq * T <= 4,194,304 rows) are rejected with
- *     FA_ERR_WORKSPACE and a message, before anything is enqueued; other
- *     argument errors are those of fa_bwd.
+ *   - The array is fa_bwd's workspace: a call runs exactly what fa_bwd runs
+ *     on the calling thread with a caller workspace of
+ *     FA_STATIC_WORKSPACE_BYTES bytes (so the fused backward only where its
+ *     workspace fits in the array) and gives the same bits.
+ *   - Sizes whose least workspace exceeds the array (fa_bwd_workspace_size_min:
+ *     Hq * tokens fp32 row statistics, i.e. Hq * T <= 4,194,304 rows) are
+ *     rejected with FA_ERR_WORKSPACE and a message, before anything is
+ *     enqueued; other argument errors are those of fa_bwd.
  *   - The first call on a device looks up the array's device address on
  *     that device (cudaGetSymbolAddress, with that device current); make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is looked up
+ *     again on the first call after the device's context has changed (for
+ *     instance after cudaDeviceReset); that call, too, belongs before any
+ *     capture.
+ *   - A call rejected for its size uses up the timing events armed for it
+ *     by fa_set_launch_events, as fa_bwd's own argument errors do.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose work
  *     overlaps on the GPU race on it: serialise them.
@@ -290,7 +340,8 @@ void fa_set_wait_limit_cycles(long long cycles);
  * call (one call, then it disarms itself): events[i] is recorded on that
  * call's stream just before the call enqueues its i-th kernel, and events[L]
  * just after the last one, L being the number of kernels the call enqueues
- * (fa_fwd: 1; fa_bwd: 3 -- row statistics D, then dK/dV, then dQ).  The
+ * (fa_fwd: 1; fa_bwd: 3 -- row statistics D, then dK/dV and dQ on the split
+ * path, or the fused kernel and the dQ conversion on the fused one).  The
  * events are created and owned by the caller (cudaEventCreate); count must be
  * >= L + 1, otherwise that call fails with FA_ERR_INVALID_ARG before enqueuing
  * anything.  events == NULL disarms.

@@ -82,7 +82,7 @@ def test_typed_entry_points_reject_unknown_element_types(lib):
 
 def test_backward_rejects_small_workspace(lib):
     fa, _ = lib
-    need = fa.fa_bwd_workspace_size(2, 4, 2, 300, 128, 0)
+    need = fa.fa_bwd_workspace_size_min(2, 4, 2, 300, 128, 0)
     st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 4, 2, 300, 128, 1, 0, None, 0, 0.1,
                    256, need - 256, None, check=False)
     assert st == 3 and "workspace" in fa.fa_last_error()
@@ -94,14 +94,64 @@ def test_backward_rejects_small_workspace(lib):
     assert st == 3 and "aligned" in fa.fa_last_error()
 
 
+def _pad(x):
+    return (x + 255) // 256 * 256
+
+
 def test_workspace_size(lib):
     fa, _ = lib
-    # dense: B * Hq * N fp32, padded to 256 bytes
-    assert fa.fa_bwd_workspace_size(2, 16, 16, 8192, 128, 0) == 2 * 16 * 8192 * 4
-    assert fa.fa_bwd_workspace_size(1, 3, 1, 5, 64, 0) == 256
+    # split backward: B * Hq * N fp32 row statistics, padded to 256 bytes
+    assert fa.fa_bwd_workspace_size_min(2, 16, 16, 8192, 128, 0) == 2 * 16 * 8192 * 4
+    assert fa.fa_bwd_workspace_size_min(1, 3, 1, 5, 64, 0) == 256
     # packed: Hq * T
-    assert fa.fa_bwd_workspace_size(16, 32, 8, 7960, 128, 68143) == ((32 * 68143 * 4 + 255) // 256) * 256
-    assert fa.fa_bwd_workspace_size(1, 1, 1, 1, 96, 0) == 0
+    assert fa.fa_bwd_workspace_size_min(16, 32, 8, 7960, 128, 68143) == _pad(32 * 68143 * 4)
+    # fused backward: + fp32 row scales (one per row and head) + the K/V bound slots
+    # (32 x (d + 1) fp32 per key/value head) + the int32 dQ sums (d per row and head)
+    for B, Hq, Hkv, N, d, T in ((2, 16, 16, 8192, 128, 0), (1, 3, 1, 5, 64, 0),
+                                (16, 32, 8, 7960, 128, 68143), (16, 32, 8, 7960, 64, 68143)):
+        rows = T if T else B * N
+        full = 2 * _pad(rows * Hq * 4) + _pad(Hkv * 32 * (d + 1) * 4) + _pad(rows * Hq * d * 4)
+        assert fa.fa_bwd_workspace_size_fused(B, Hq, Hkv, N, d, T) == full
+        # the default choice: the fused backward at d = 64, the split one at d = 128
+        want = full if d == 64 else fa.fa_bwd_workspace_size_min(B, Hq, Hkv, N, d, T)
+        assert fa.fa_bwd_workspace_size(B, Hq, Hkv, N, d, T) == want
+    for f in (fa.fa_bwd_workspace_size, fa.fa_bwd_workspace_size_min, fa.fa_bwd_workspace_size_fused):
+        assert f(1, 1, 1, 1, 96, 0) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_path_selection(lib, d):
+    """Default: the fused backward for causal masks (with or without a window) at
+    d = 64 when the workspace holds it, the split one otherwise; a thread can force
+    either, and a forced fused call without its mask or workspace would fail."""
+    fa, _ = lib
+    args = (2, 4, 2, 300, d)
+    full = fa.fa_bwd_workspace_size_fused(*args, 0)
+    least = fa.fa_bwd_workspace_size_min(*args, 0)
+    auto_fused = fa.FA_BWD_FUSED if d == 64 else fa.FA_BWD_SPLIT
+    try:
+        fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
+        assert fa.fa_bwd_path(*args, 1, 0, 0, full) == auto_fused
+        assert fa.fa_bwd_path(*args, 1, 100, 0, full) == auto_fused
+        assert fa.fa_bwd_path(*args, 1, 0, 0, full - 1) == fa.FA_BWD_SPLIT
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == fa.FA_BWD_SPLIT
+        assert fa.fa_bwd_path(*args, 1, 0, 0, least - 1) == -1
+        assert fa.fa_bwd_path(2, 4, 2, 300, 96, 1, 0, 0, full) == -1
+        fa.fa_bwd_set_path(fa.FA_BWD_SPLIT)
+        assert fa.fa_bwd_path(*args, 1, 0, 0, full) == fa.FA_BWD_SPLIT
+        fa.fa_bwd_set_path(fa.FA_BWD_FUSED)
+        assert fa.fa_bwd_path(*args, 1, 0, 0, full) == fa.FA_BWD_FUSED
+        assert fa.fa_bwd_path(*args, 1, 0, 0, full - 1) == -1
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == -1
+        # and fa_bwd itself refuses, before touching the GPU
+        st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, *args, 0, 0, None, 0, 0.1, 256, full,
+                       None, check=False)
+        assert st == fa.FA_ERR_UNSUPPORTED and "causal" in fa.fa_last_error()
+        st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, *args, 1, 0, None, 0, 0.1, 256, least,
+                       None, check=False)
+        assert st == fa.FA_ERR_WORKSPACE and "fused" in fa.fa_last_error()
+    finally:
+        fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
@@ -181,3 +231,25 @@ def test_backward_rejects_bad_arguments(lib, over, status):
     fa, _ = lib
     assert _bwd(fa, **over) == status
     assert fa.fa_last_error() != ""
+
+
+def test_static_workspace_size_constant_matches_header(lib):
+    fa, _ = lib
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    m = re.search(r"#define\s+FA_STATIC_WORKSPACE_BYTES\s+\((\d+)\s*\*\s*(\d+)\s*\*\s*(\d+)\)", text)
+    assert m and int(m[1]) * int(m[2]) * int(m[3]) == fa.FA_STATIC_WORKSPACE_BYTES
+
+
+def test_rejected_static_workspace_call_uses_up_armed_events(lib):
+    """A size the static array cannot hold is rejected before anything is enqueued, and
+    the timing events armed for that call are used up with it (as fa_bwd's own argument
+    errors do), so they cannot time the thread's next call."""
+    fa, _ = lib
+    fa.fa_set_launch_events([1])          # one handle: too few for any call, never recorded
+    st = fa.fa_bwd_static_workspace(16, 16, 16, 16, 16, 16, 16, 16, 16, 4, 64, 8, 32768, 128,
+                                    1, 0, None, 0, 0.1, None, check=False)
+    assert st == fa.FA_ERR_WORKSPACE
+    # still armed, the next call would fail on the event count; disarmed, it reaches
+    # its own argument check
+    assert _fwd(fa, q=None) == fa.FA_ERR_INVALID_ARG
+    assert "non-null" in fa.fa_last_error()

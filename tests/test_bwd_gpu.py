@@ -35,38 +35,94 @@ SMALL = [
 ]
 
 
-def run_fwd_bwd(fa, x, N, d, causal, window):
+# the two backward paths: "fused" (causal masks with the full workspace: one kernel,
+# dQ summed across CTAs in a fixed order) and "split" (the least workspace: a dK/dV
+# kernel and a dQ kernel)
+PATHS = ["fused", "split"]
+
+
+def run_fwd_bwd(fa, x, N, d, causal, window, path="fused"):
     import torch
     q, k, v, do = (to_dev(x[n]) for n in ("q", "k", "v", "dout"))
     cu = cu_dev(x["cu"])
     kw = dict(causal=causal, window=window, scale=scale_of(d), cu_seqlens=cu, max_seqlen=N)
     o, lse = fa.attention_forward(q, k, v, **kw)
-    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, **kw)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, path=path, **kw)
     fa.fa_device_status(torch.cuda.current_stream())
     return dq, dk, dv
 
 
-@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}{'p' if c[7] else ''}")
-def test_backward_matches_oracle(fa, oracle_mod, case):
+def expected_path(fa, case, path):
     B, Hq, Hkv, N, d, causal, window, lengths = case
+    T = int(sum(lengths)) if lengths else 0
+    size = (fa.fa_bwd_workspace_size_min if path == "split" else fa.fa_bwd_workspace_size_fused)(
+        B, Hq, Hkv, N, d, T)
+    fa.fa_bwd_set_path(fa.FA_BWD_SPLIT if path == "split" else fa.FA_BWD_FUSED)
+    try:
+        return fa.fa_bwd_path(B, Hq, Hkv, N, d, causal, window, T, size)
+    finally:
+        fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
+
+
+_ORACLE = {}
+
+
+def oracle_grads(oracle_mod, x, case):
+    key = tuple(map(str, case))
+    if key not in _ORACLE:
+        B, Hq, Hkv, N, d, causal, window, lengths = case
+        _ORACLE[key] = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=causal,
+                                                window=window, scale=scale_of(d),
+                                                cu_seqlens=x["cu"])
+    return _ORACLE[key]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}{'p' if c[7] else ''}")
+def test_backward_matches_oracle(fa, oracle_mod, case, path):
+    B, Hq, Hkv, N, d, causal, window, lengths = case
+    if path == "fused" and not causal:
+        pytest.skip("the fused backward serves causal masks; others run the split one")
+    assert expected_path(fa, case, path) == (fa.FA_BWD_FUSED if path == "fused" else fa.FA_BWD_SPLIT)
     x = make_case(B, Hq, Hkv, N, d, seed=5, lengths=lengths)
-    dq, dk, dv = run_fwd_bwd(fa, x, N, d, causal, window)
-    rq, rk, rv = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=causal,
-                                          window=window, scale=scale_of(d), cu_seqlens=x["cu"])
+    dq, dk, dv = run_fwd_bwd(fa, x, N, d, causal, window, path)
+    rq, rk, rv = oracle_grads(oracle_mod, x, case)
     for name, g, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         err = rel_fro(to_f64(g), ref)
         assert err <= GRAD_REL_FRO, (name, err)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", [(1, 8, 2, 1100, 128, None), (3, 8, 2, 1100, 64, (1100, 7, 640))],
                          ids=["d128", "d64packed"])
-def test_backward_is_deterministic(fa, case):
-    """Two runs give the same bits: every gradient row is summed by one CTA in a
-    fixed order (both head dimensions; their rings and warpgroups differ)."""
+def test_backward_is_deterministic(fa, case, path):
+    """Two runs give the same bits.  Split: every gradient row is summed by one CTA in
+    a fixed order.  Fused: dK and dV as in the split path; dQ is summed across CTAs
+    as fixed-point integers, whose sum does not depend on the order of the additions
+    (both head dimensions; their accumulator layouts differ)."""
     import torch
     B, Hq, Hkv, N, d, lengths = case
     x = make_case(B, Hq, Hkv, N, d, seed=9, lengths=lengths)
-    a = run_fwd_bwd(fa, x, N, d, True, 0)
-    b = run_fwd_bwd(fa, x, N, d, True, 0)
+    a = run_fwd_bwd(fa, x, N, d, True, 0, path)
+    b = run_fwd_bwd(fa, x, N, d, True, 0, path)
     for ga, gb in zip(a, b):
         assert torch.equal(ga.view(torch.int16), gb.view(torch.int16))
+
+
+@pytest.mark.parametrize("case", [
+    (2, 16, 2, 1500, 128, True, 0, None),          # GQA 8:1, 12 key tiles: chains of up to 12
+    (1, 4, 4, 2100, 64, True, 300, None),          # window: chains of 4 over 17 tiles
+    (5, 8, 4, 900, 128, True, 0, (900, 1, 385, 0, 640)),   # packed, unaligned starts, empty
+], ids=["gqa8_chain12", "d64_window300", "packed_mixed"])
+def test_fused_backward_longer_chains(fa, oracle_mod, case):
+    """The fused backward on cases whose dQ rows collect many contributions (long
+    causal chains, a window, GQA 8:1, a packed batch with unaligned starts and an
+    empty sequence), against the oracle."""
+    B, Hq, Hkv, N, d, causal, window, lengths = case
+    assert expected_path(fa, case, "fused") == fa.FA_BWD_FUSED
+    x = make_case(B, Hq, Hkv, N, d, seed=17, lengths=lengths)
+    dq, dk, dv = run_fwd_bwd(fa, x, N, d, causal, window, "fused")
+    rq, rk, rv = oracle_grads(oracle_mod, x, case)
+    for name, g, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = rel_fro(to_f64(g), ref)
+        assert err <= GRAD_REL_FRO, (name, err)

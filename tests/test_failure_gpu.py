@@ -13,9 +13,10 @@ from helpers import GRAD_REL_FRO, O_MAX_ABS, make_case, max_abs, rel_fro, scale_
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_budget_expiry_reports_timeout_then_recovers(fa, oracle_mod):
+@pytest.mark.parametrize("path,d", [("split", 128), ("fused", 128), ("fused", 64)])
+def test_wait_budget_expiry_reports_timeout_then_recovers(fa, oracle_mod, path, d):
     import torch
-    B, Hq, Hkv, N, d = 2, 4, 2, 700, 128
+    B, Hq, Hkv, N = 2, 4, 2, 700
     x = make_case(B, Hq, Hkv, N, d, seed=13)
     q, k, v, do = (to_dev(x[n]) for n in ("q", "k", "v", "dout"))
     stream = torch.cuda.current_stream()
@@ -25,13 +26,13 @@ def test_wait_budget_expiry_reports_timeout_then_recovers(fa, oracle_mod):
     try:
         o, lse = fa.attention_forward(q, k, v, **kw)
         assert fa.fa_device_status(stream, check=False) == fa.FA_ERR_TIMEOUT
-        fa.attention_backward(q, k, v, o, lse, do, **kw)
+        fa.attention_backward(q, k, v, o, lse, do, path=path, **kw)
         assert fa.fa_device_status(stream, check=False) == fa.FA_ERR_TIMEOUT
     finally:
         fa.fa_set_wait_limit_cycles(0)              # back to the default budget
     assert fa.fa_device_status(stream, check=False) == fa.FA_OK
     o, lse = fa.attention_forward(q, k, v, **kw)
-    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, **kw)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, path=path, **kw)
     fa.fa_device_status(stream)
     o_ref, _ = oracle_mod.attention_fwd(x["q"], x["k"], x["v"], causal=True, scale=scale_of(d))
     assert max_abs(to_f64(o), o_ref) <= O_MAX_ABS

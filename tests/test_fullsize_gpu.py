@@ -35,7 +35,7 @@ def sampled_sequences(w):
     return sorted(s)
 
 
-def run_workload(fa, w, x):
+def run_workload(fa, w, x, path="split"):
     import torch
     dev = torch.device("cuda", 0)
 
@@ -58,9 +58,14 @@ def run_workload(fa, w, x):
     if w.backward:
         do = d(x["dout"])
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
+        size = fa.fa_bwd_workspace_size_fused if path == "fused" else fa.fa_bwd_workspace_size_min
+        ws_bytes = size(w.B, w.Hq, w.Hkv, w.N, w.d, T)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        fa.fa_bwd_typed(code, q, k, v, o, lse, do, dq, dk, dv, *geo, ws, ws_bytes, s)
+        fa.fa_bwd_set_path(fa.FA_BWD_FUSED if path == "fused" else fa.FA_BWD_SPLIT)
+        try:
+            fa.fa_bwd_typed(code, q, k, v, o, lse, do, dq, dk, dv, *geo, ws, ws_bytes, s)
+        finally:
+            fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
         out.update(dq=dq, dk=dk, dv=dv)
     fa.fa_device_status(s)
     return {n: t.float().cpu().numpy().astype(np.float64) for n, t in out.items()}
@@ -76,12 +81,16 @@ def token_index(w, b, rows):
 # dropout workloads are checked against the dropout oracle at smaller sizes
 # (tests/test_dropout_gpu.py): its dense per-head matrices do not scale to these;
 # the fp8 workload against the fp8 oracle (tests/test_fp8_gpu.py, same shape)
-@pytest.mark.parametrize("name", sorted(n for n, w in WORKLOADS.items()
-                                        if w.p_drop == 0 and w.dtype != "fp8"))
-def test_full_size_sampled(fa, oracle_mod, name):
+# backward workloads run both backward paths (all of them have causal masks)
+CASES = [(n, p) for n, w in sorted(WORKLOADS.items()) if w.p_drop == 0 and w.dtype != "fp8"
+         for p in (("split", "fused") if w.backward else ("split",))]
+
+
+@pytest.mark.parametrize("name,path", CASES, ids=[f"{n}-{p}" for n, p in CASES])
+def test_full_size_sampled(fa, oracle_mod, name, path):
     w = WORKLOADS[name]
     x = attention_inputs(w.q_shape, w.kv_shape, 0, with_dout=w.backward, dtype=w.dtype)
-    got = run_workload(fa, w, x)
+    got = run_workload(fa, w, x, path)
     cu = w.cu_seqlens()
     G = w.Hq // w.Hkv
     for b in sampled_sequences(w):
