@@ -196,17 +196,14 @@ fa_status check_common(int B, int Hq, int Hkv, int N, int d, int causal, int win
 }
 
 // CTAs to launch for blocks of `rows` rows per sequence and head: exact for
-// dense batches, an upper bound (sum_b ceil(len_b/rows) <= ceil(T/rows) + B)
-// for packed ones.
+// dense batches; for packed ones the slot space of map_work, ceil(T / rows) + B
+// slots per head (sequence b's blocks start at slot floor(start_b / rows) + b).
 int num_blocks(const Geometry& g, int rows, int heads) {
     long long per_head;
-    if (g.seq.cu_seqlens) {
+    if (g.seq.cu_seqlens)
         per_head = (static_cast<long long>(g.tokens) + rows - 1) / rows + g.seq.B;
-        long long dense_bound = static_cast<long long>(g.seq.B) * ((g.seq.N + rows - 1) / rows);
-        if (dense_bound < per_head) per_head = dense_bound;
-    } else {
+    else
         per_head = static_cast<long long>(g.seq.B) * ((g.seq.N + rows - 1) / rows);
-    }
     return static_cast<int>(per_head * heads);
 }
 
@@ -624,13 +621,12 @@ fa_status make_vt_map(CUtensorMap* map, const void* base, int vt_tokens, int d, 
     return FA_OK;
 }
 
-// Upper bound on the 128-token blocks of all sequences: exact for dense batches;
-// packed: sum_b ceil(len_b / 128) <= ceil(T / 128) + B and <= B ceil(N / 128).
+// Columns of the fp8 block-scale arrays: exact for dense batches (B ceil(N / 128));
+// packed, the column space of seq_block_col: ceil(T / 128) + B.
 long long fp8_blocks(int B, int N, int total_tokens, bool packed) {
-    const long long dense = static_cast<long long>(B) * ((static_cast<long long>(N) + 127) / 128);
-    if (!packed) return dense;
-    const long long bound = (static_cast<long long>(total_tokens) + 127) / 128 + B;
-    return bound < dense ? bound : dense;
+    if (!packed) return static_cast<long long>(B) * ((static_cast<long long>(N) + 127) / 128);
+    // packed: sequence b's blocks start at column floor(cu_seqlens[b] / 128) + b
+    return (static_cast<long long>(total_tokens) + 127) / 128 + B;
 }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

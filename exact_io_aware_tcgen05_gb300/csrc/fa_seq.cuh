@@ -45,19 +45,36 @@ __device__ __forceinline__ long long row_stat_index(const SeqInfo& s, int b, int
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// First block slot of sequence b of a packed batch for blocks of `rows` rows:
+// floor(start_b / rows) + b.  The slot ranges [first(b), first(b) + ceil(len_b /
+// rows)) are disjoint, increase with b and lie below ceil(T / rows) + B, so the
+// sequence that owns a slot is found by a binary search over cu_seqlens (O(log B)
+// loads) rather than a walk over all earlier sequences.
+__device__ __forceinline__ int seq_first_slot(const SeqInfo& s, int b, int rows) {
+    int st, len;
+    seq_bounds(s, b, st, len);
+    return st / rows + b;
+}
+
+// The sequence b whose slot range may hold `slot`: the last b with first(b) <= slot
+// (first() strictly increases with b).
+__device__ __forceinline__ int seq_of_slot(const SeqInfo& s, int slot, int rows) {
+    int lo = 0, hi = s.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seq_first_slot(s, mid, rows) <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 // fp8 layouts: the column of sequence b's first 128-token block in a [heads, nb]
-// block-scale array (the blocks of the earlier sequences, ceil(len / 128) each);
-// 128 times it is the column of its first key in the transposed V layout, where
-// every sequence is padded to a multiple of 128 keys.
+// block-scale array: b ceil(N / 128) for dense batches, first(b) (above) for packed
+// ones; 128 times it is the column of its first key in the transposed V layout,
+// where every sequence is padded to a multiple of 128 keys.
 __device__ __forceinline__ int seq_block_col(const SeqInfo& s, int b) {
     if (!s.cu_seqlens) return b * ceil_div(s.N, 128);
-    int acc = 0;
-    for (int i = 0; i < b; ++i) {
-        int st, len;
-        seq_bounds(s, i, st, len);
-        acc += ceil_div(len, 128);
-    }
-    return acc;
+    return seq_first_slot(s, b, 128);
 }
 
 // Heads per scheduling chunk (see map_work) unless the launcher picks another.
@@ -71,8 +88,10 @@ constexpr int kHeadChunk = 8;
 // (longest first); the most expensive block is the last one for query blocks
 // under a causal mask (`from_end`), the first for key blocks.  A wider chunk
 // shortens the tail (the last chunk's long items start earlier) at the price of
-// a larger working set.  Returns false for CTAs beyond the real work (packed
-// batches launch an upper bound).
+// a larger working set.  Packed batches: sequence b owns CTA indices
+// [first(b) heads, (first(b) + blocks) heads) (see seq_first_slot), sequences in
+// order, within a sequence its heads in chunks.  Returns false for CTAs beyond
+// the real work (packed batches launch an upper bound, with gaps).
 __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int heads,
                                          bool from_end, int& b, int& h, int& blk,
                                          int chunk = kHeadChunk) {
@@ -86,17 +105,14 @@ __device__ __forceinline__ bool map_work(const SeqInfo& s, int w, int rows, int 
         nbh = min(chunk, pairs - first_bh);
         r = w - first_bh * n;
     } else {
-        // sequences in order; within a sequence its heads in chunks
-        int base = 0;
-        for (b = 0; b < s.B; ++b) {
-            int st, len;
-            seq_bounds(s, b, st, len);
-            n = ceil_div(len, rows);
-            if (w < base + n * heads) break;
-            base += n * heads;
-        }
-        if (b >= s.B) return false;
-        const int idx = w - base;
+        const int slot = w / heads;
+        b = seq_of_slot(s, slot, rows);
+        int st, len;
+        seq_bounds(s, b, st, len);
+        n = ceil_div(len, rows);
+        const int base = seq_first_slot(s, b, rows);
+        if (slot >= base + n) return false;   // a gap between sequences
+        const int idx = w - base * heads;
         const int c = idx / (n * chunk);
         first_bh = b * heads + c * chunk;
         nbh = min(chunk, heads - c * chunk);

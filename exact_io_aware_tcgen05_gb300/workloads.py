@@ -104,6 +104,13 @@ def _varlen(d: int) -> Workload:
                     N=max(lengths), d=d, causal=True, window=0, backward=True, lengths=lengths)
 
 
+def _many_short() -> Workload:
+    # a packed batch of many short sequences: 1024 lengths drawn uniformly from [64, 512]
+    lengths = tuple(int(x) for x in varlen_lengths(0, 1024, 64, 512))
+    return Workload("fwdbwd_varlen1024_h32kv8_d128_causal", B=len(lengths), Hq=32, Hkv=8,
+                    N=max(lengths), d=128, causal=True, window=0, backward=True, lengths=lengths)
+
+
 WORKLOADS = {
     w.name: w for w in [
         Workload("fwd_b1_h1_n128_d64", 1, 1, 1, 128, 64, False, 0, False),
@@ -119,6 +126,7 @@ WORKLOADS = {
                  dtype="fp8"),
         _varlen(128),
         _varlen(64),
+        _many_short(),
     ]
 }
 

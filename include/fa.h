@@ -213,13 +213,15 @@ fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
  *
  * Layouts (tokens as in fa_fwd: dense b * N + i, packed cu_seqlens[b] + i):
  *   q8, k8   e4m3 [tokens, Hq or Hkv, d], scales [heads, nb]: one per (head,
- *            128-token block of a sequence); block kb of sequence b is column
- *            (blocks of sequences 0..b-1) + kb, the blocks of a sequence of
- *            length L being ceil(L / 128).  nb >= fa_fp8_scale_blocks(...).
+ *            128-token block of a sequence, ceil(L / 128) blocks for length L);
+ *            block kb of sequence b is column c_b + kb, with c_b = b ceil(N / 128)
+ *            for a dense batch and c_b = floor(cu_seqlens[b] / 128) + b for a
+ *            packed one (columns between sequences unused).
+ *            nb >= fa_fp8_scale_blocks(...).
  *   vt8      e4m3 V^T [Hkv, d, vt_tokens]: key i of sequence b (and channel c)
- *            at column 128 * (blocks of sequences 0..b-1) + i, row c; the
- *            columns past a sequence's length up to its next multiple of 128 hold
- *            zero codes.  vt_tokens >= fa_fp8_vt_tokens(...), a multiple of 128.
+ *            at column 128 c_b + i, row c; the columns past a sequence's length
+ *            up to its next multiple of 128 hold zero codes.
+ *            vt_tokens >= fa_fp8_vt_tokens(...), a multiple of 128.
  *   v_scale  [Hkv, B]: one per (key/value head, sequence).
  * The values are code * scale.  fa_fp8_quantize_qk / fa_fp8_quantize_v write
  * these from bf16 tensors in the layouts of fa_fwd: per block (Q, K) or per
@@ -239,8 +241,8 @@ fa_status fa_bwd_dropout(fa_dtype dtype, float p_drop, unsigned long long seed,
  * geometry arguments of fa_fwd (H heads); they only enqueue work.
  *
  * fa_fp8_scale_blocks / fa_fp8_vt_tokens return the minimum nb / vt_tokens for
- * a batch (exact for dense batches, packed != 0: an upper bound from
- * total_tokens and B), or 0 for invalid arguments.
+ * a batch (dense: B ceil(N / 128) blocks; packed != 0: ceil(total_tokens / 128)
+ * + B, the column space above), or 0 for invalid arguments.
  */
 int fa_fp8_scale_blocks(int B, int N, int total_tokens, int packed);
 int fa_fp8_vt_tokens(int B, int N, int total_tokens, int packed);

@@ -20,12 +20,13 @@ processing (a random orthogonal transform of Q and K) is not part of it.
   block of that sequence (the kernels' tile), scale = amax / 448 in float32
   (1 for an all-zero block) and code = e4m3(x / scale), the division in
   float32.  Scales are laid out [H, nb]: block kb of sequence b sits at
-  column sum_{b' < b} ceil(len_b' / 128) + kb; nb >= that sum is the caller's
-  row stride.
+  column c_b + kb, c_b = b ceil(N / 128) for a dense batch and
+  floor(start_b / 128) + b for a packed one; nb is the caller's row stride.
 * V is quantised per sequence and head (one scale; the P V product
   accumulates over all key blocks in one accumulator, so one scale per row of
   output), stored transposed as V^T [Hkv, d, vt_tokens]: key j of sequence b at
-  column sum_{b' < b} round_up(len_b', 128) + j, the padding columns zero.
+  column 128 c_b + j, the columns past the sequence up to its next multiple of
+  128 zero.
   Scales [Hkv, B].
 * The fp8 forward computes, on the dequantised inputs (code value * scale),
   the same O and LSE as the bf16 forward; the kernel rounds the probabilities
@@ -91,21 +92,21 @@ def seq_lengths(B: int, N: int, cu_seqlens=None):
 
 
 def block_offsets(B: int, N: int, cu_seqlens=None):
-    """Column of each sequence's first 128-token block in a [H, nb] scale array."""
-    offs, acc = [], 0
-    for _, L in seq_lengths(B, N, cu_seqlens):
-        offs.append(acc)
-        acc += -(-L // BLOCK)
-    return offs, acc
+    """Column c_b of each sequence's first 128-token block in a [H, nb] scale array,
+    and the columns the layout spans."""
+    seqs = seq_lengths(B, N, cu_seqlens)
+    if cu_seqlens is None:
+        offs = [b * -(-N // BLOCK) for b in range(B)]
+    else:
+        offs = [start // BLOCK + b for b, (start, _) in enumerate(seqs)]
+    end = max((o + -(-L // BLOCK) for o, (_, L) in zip(offs, seqs)), default=0)
+    return offs, end
 
 
 def vt_offsets(B: int, N: int, cu_seqlens=None):
-    """Column of each sequence's first key in the transposed V layout."""
-    offs, acc = [], 0
-    for _, L in seq_lengths(B, N, cu_seqlens):
-        offs.append(acc)
-        acc += -(-L // BLOCK) * BLOCK
-    return offs, acc
+    """Column of each sequence's first key in the transposed V layout (128 c_b)."""
+    offs, end = block_offsets(B, N, cu_seqlens)
+    return [BLOCK * o for o in offs], BLOCK * end
 
 
 def _f32_scale(amax: np.ndarray) -> np.ndarray:

@@ -182,11 +182,12 @@ def test_dropout_entry_points_reject_bad_probabilities(lib):
 
 def test_fp8_sizes_and_argument_checks(lib):
     fa, _ = lib
-    # dense: exact block counts; packed: the bound ceil(T / 128) + B (capped by the dense count)
+    # dense: exact block counts; packed: the column space ceil(T / 128) + B (sequence b
+    # starts at column floor(start_b / 128) + b)
     assert fa.fa_fp8_scale_blocks(2, 300, 0, 0) == 6 and fa.fa_fp8_vt_tokens(2, 300, 0, 0) == 768
     assert fa.fa_fp8_scale_blocks(16, 8192, 68143, 1) == 533 + 16
     assert fa.fa_fp8_vt_tokens(16, 8192, 68143, 1) == 128 * (533 + 16)
-    assert fa.fa_fp8_scale_blocks(3, 100, 300, 1) == 3          # capped at B * ceil(N / 128)
+    assert fa.fa_fp8_scale_blocks(3, 100, 300, 1) == 3 + 3      # lengths 100 each: columns 0, 1, 3
     assert fa.fa_fp8_scale_blocks(0, 100, 0, 0) == 0
     def fwd(**over):
         a = dict(nb=3, vt=384, d=128, N=300, q=16)

@@ -126,3 +126,42 @@ def test_fused_backward_longer_chains(fa, oracle_mod, case):
     for name, g, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         err = rel_fro(to_f64(g), ref)
         assert err <= GRAD_REL_FRO, (name, err)
+
+
+def _many_lengths():
+    """1100 packed sequences: seeded lengths in [0, 300) with empty, one-token and
+    tile-edge lengths mixed in."""
+    rng = np.random.default_rng(11)
+    lengths = rng.integers(0, 300, size=1100)
+    lengths[::97] = 0
+    lengths[1::89] = 1
+    lengths[2::83] = 128
+    lengths[3::79] = 129
+    return tuple(int(x) for x in lengths)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_packed_sequences(fa, oracle_mod, d):
+    """More than a thousand packed sequences (the CTAs find their sequence by a
+    binary search over cu_seqlens): forward element by element, and both backward
+    paths, against the oracle."""
+    from helpers import LSE_MAX_ABS, O_MAX_ABS, max_abs
+    lengths = _many_lengths()
+    B, Hq, Hkv, N = len(lengths), 2, 1, max(lengths)
+    x = make_case(B, Hq, Hkv, N, d, seed=23, lengths=lengths)
+    q, k, v, do = (to_dev(x[n]) for n in ("q", "k", "v", "dout"))
+    cu = cu_dev(x["cu"])
+    kw = dict(causal=True, window=0, scale=scale_of(d), cu_seqlens=cu, max_seqlen=N)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    o_ref, lse_ref = oracle_mod.attention_fwd(x["q"], x["k"], x["v"], causal=True,
+                                              scale=scale_of(d), cu_seqlens=x["cu"])
+    assert max_abs(to_f64(o), o_ref) <= O_MAX_ABS
+    assert max_abs(lse.cpu().numpy().astype(np.float64), lse_ref) <= LSE_MAX_ABS
+    refs = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=True,
+                                    scale=scale_of(d), cu_seqlens=x["cu"])
+    for path in PATHS:
+        grads = fa.attention_backward(q, k, v, o, lse, do, path=path, **kw)
+        fa.fa_device_status()
+        for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+            err = rel_fro(to_f64(g), r)
+            assert err <= GRAD_REL_FRO, (path, name, err)

@@ -54,13 +54,17 @@ def _oracle_ops(fp8, x, B, N, nb, vt_tokens):
 def _check_quantisation(fp8, ops, ref, B, N, cu):
     q8, qs, k8, ks, vt8, vs = (t.cpu().numpy() for t in ops[:6])
     rq8, rqs, rk8, rks, rvt8, rvs = ref
-    _, blocks = fp8.block_offsets(B, N, cu)
+    # the columns the layout assigns to the sequences' blocks (a packed batch leaves
+    # unused columns between sequences)
+    offs, _ = fp8.block_offsets(B, N, cu)
+    used = np.concatenate([np.arange(o, o + -(-L // 128)) for o, (_, L) in
+                           zip(offs, fp8.seq_lengths(B, N, cu))]).astype(np.int64)
     assert np.array_equal(q8, rq8) and np.array_equal(k8, rk8)
-    assert np.array_equal(qs[:, :blocks], rqs[:, :blocks])
-    assert np.array_equal(ks[:, :blocks], rks[:, :blocks])
+    assert np.array_equal(qs[:, used], rqs[:, used])
+    assert np.array_equal(ks[:, used], rks[:, used])
     assert np.array_equal(vs, rvs)
-    _, cols = fp8.vt_offsets(B, N, cu)          # the written columns: padding included
-    assert np.array_equal(vt8[:, :, :cols], rvt8[:, :, :cols])
+    cols = (128 * used[:, None] + np.arange(128)[None, :]).ravel()   # padding included
+    assert np.array_equal(vt8[:, :, cols], rvt8[:, :, cols])
 
 
 def _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, causal, window, cu, rows_per_seq=None):

@@ -133,17 +133,18 @@ def test_quantize_v_transposed_padded():
 
 def test_quantize_empty_sequences():
     # an empty sequence has no blocks and no V^T columns; its V scale is that of an
-    # all-zero block (amax 0 over no values), 1
+    # all-zero block (amax 0 over no values), 1.  Packed layout: sequence b starts at
+    # column floor(start_b / 128) + b
     cu = [0, 4, 4, 4 + 130, 4 + 130]                     # lengths 4, 0, 130, 0
     T, H, d = cu[-1], 1, 8
     x = _bf16(np.random.default_rng(6).standard_normal((T, H, d)))
     offs, total = fp8.block_offsets(4, 0, cu)
-    assert offs == [0, 1, 1, 3] and total == 3
+    assert offs == [0, 1, 2, 4] and total == 4
     codes, scales = fp8.quantize_qk(x, 4, 0, cu_seqlens=cu)
-    assert scales.shape == (H, 3)
+    assert scales.shape == (H, 4)
     vt, vs = fp8.quantize_v(x, 4, 0, cu_seqlens=cu)
     voffs, vtotal = fp8.vt_offsets(4, 0, cu)
-    assert voffs == [0, 128, 128, 384] and vtotal == 384
+    assert voffs == [0, 128, 256, 512] and vtotal == 512
     assert vs[0, 1] == 1.0 and vs[0, 3] == 1.0
     back = fp8.dequantize_v(vt, vs, 4, 0, cu_seqlens=cu)
     assert back.shape == (T, H, d)
