@@ -411,38 +411,40 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     tmem_st16(tS + 16 * half, pk);
                 }
 #pragma unroll
-                for (int half = 0; half < 2 && !F8; ++half) {
-                    uint32_t pk[32];
-                    // dropout: the random bytes of keys kb + 64 half .. + 63 of this row;
+                // (a quarter of the row per TMEM store: 32 keys, 16 packed words, keeps the
+                // live registers of the pass below the softmax warps' budget)
+                for (int qtr = 0; qtr < 4 && !F8; ++qtr) {
+                    uint32_t pk[16];
+                    // dropout: the random bytes of keys kb + 32 qtr .. + 31 of this row;
                     // l sums the probabilities before dropout, the product takes the kept
                     // ones (the 1 / keep-probability factor is applied to O in fp32 at the
                     // end, so the 16-bit P carries no extra rounding)
-                    uint32_t dw[DROP ? 16 : 1];
+                    uint32_t dw[DROP ? 8 : 1];
                     if (DROP) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 v = drop_row[(4 * half + c) ^ (r & 7)];
-                            dw[(4 * c) % (DROP ? 16 : 1)] = v.x;
-                            dw[(4 * c + 1) % (DROP ? 16 : 1)] = v.y;
-                            dw[(4 * c + 2) % (DROP ? 16 : 1)] = v.z;
-                            dw[(4 * c + 3) % (DROP ? 16 : 1)] = v.w;
+                        for (int c = 0; c < 2; ++c) {
+                            const uint4 v = drop_row[(2 * qtr + c) ^ (r & 7)];
+                            dw[(4 * c) % (DROP ? 8 : 1)] = v.x;
+                            dw[(4 * c + 1) % (DROP ? 8 : 1)] = v.y;
+                            dw[(4 * c + 2) % (DROP ? 8 : 1)] = v.z;
+                            dw[(4 * c + 3) % (DROP ? 8 : 1)] = v.w;
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int k = 64 * half + 2 * c;
+                    for (int c = 0; c < 16; ++c) {
+                        const int k = 32 * qtr + 2 * c;
                         const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
                         const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
                         rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
                         if (DROP)
-                            pk[c] = pack2<E>(p0 * keep_factor(dw[(c >> 1) % (DROP ? 16 : 1)], (2 * c) & 3,
+                            pk[c] = pack2<E>(p0 * keep_factor(dw[(c >> 1) % (DROP ? 8 : 1)], (2 * c) & 3,
                                                               p.drop.thresh, 1.f),
-                                             p1 * keep_factor(dw[(c >> 1) % (DROP ? 16 : 1)], (2 * c + 1) & 3,
+                                             p1 * keep_factor(dw[(c >> 1) % (DROP ? 8 : 1)], (2 * c + 1) & 3,
                                                               p.drop.thresh, 1.f));
                         else
                             pk[c] = pack2<E>(p0, p1);
                     }
-                    tmem_st32(tS + 32 * half, pk);
+                    tmem_st16(tS + 16 * qtr, pk);
                 }
                 const float2 rsum = f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])));
                 l += rsum.x + rsum.y;
