@@ -332,6 +332,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                                       ((qt_first + n % nq) * kBlockM + W * wg) >> 2, kpos >> 2,
                                       static_cast<uint32_t>(b * s.Hq + g * s.group + n / nq),
                                       p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
+            keep_masks(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), p.drop.thresh);
         };
         if (DROP) draw(0);
         // `ok` turns false (warp-uniformly) when a wait gives up; the warp then
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
                 if (DROP)
-                    tmem_st_pk_dropped<W, E>(tS, pv, *reinterpret_cast<const uint32_t(*)[W / 4]>(dw), p.drop);
+                    tmem_st_pk_dropped<W, E>(tS, pv, *reinterpret_cast<const uint32_t(*)[W / 4]>(dw));
                 else
                     tmem_st_pk<W, E>(tS, pv);
                 tmem_st_wait();
@@ -393,21 +394,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
                 tc_fence_after();
                 float dp[W];
                 tmem_ldw<W>(tDP, dp);
-                if (DROP) {
-                    // dS = P (keep dZ - D): dZ is the product's dP, taken through the keep factors
-#pragma unroll
-                    for (int c = 0; c < W; ++c)
-                        dp[c] *= col_keep<W>(*reinterpret_cast<const uint32_t(*)[W / 4]>(dw), c, p.drop);
-                }
+                // with dropout dS = P (r keep dZ - D), dZ the product's dP: the dropped
+                // columns cleared by their masks, r folded into the multiply-add
+                const uint32_t(&km)[W / 4] = *reinterpret_cast<const uint32_t(*)[W / 4]>(dw);
+                const uint64_t rr = f2_pack(p.drop.rscale, p.drop.rscale);
 #pragma unroll
                 for (int c4 = 0; c4 < W / 4; ++c4) {
                     const float4 nd = ndlt4[c4];
-                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[4 * c4], pv[4 * c4 + 1]),
-                                                      f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]),
-                                                             f2_pack(nd.x, nd.y))));
-                    const float2 e = f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
-                                                      f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]),
-                                                             f2_pack(nd.z, nd.w))));
+                    const int c = 4 * c4;
+                    const uint64_t z0 = DROP ? f2_fma(rr, f2_pack(kept<W>(km, dp, c), kept<W>(km, dp, c + 1)), f2_pack(nd.x, nd.y))
+                                             : f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(nd.x, nd.y));
+                    const uint64_t z1 = DROP ? f2_fma(rr, f2_pack(kept<W>(km, dp, c + 2), kept<W>(km, dp, c + 3)), f2_pack(nd.z, nd.w))
+                                             : f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(nd.z, nd.w));
+                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[c], pv[c + 1]), z0));
+                    const float2 e = f2_unpack(f2_mul(f2_pack(pv[c + 2], pv[c + 3]), z1));
                     dp[4 * c4] = a.x;
                     dp[4 * c4 + 1] = a.y;
                     dp[4 * c4 + 2] = e.x;
@@ -632,6 +632,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                                       ((kt_first + j) * kBlockN + W * wg) >> 2,
                                       static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
                                       p.drop.seed_lo, p.drop.seed_hi, lane);
+            keep_masks(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), p.drop.thresh);
         };
         if (DROP) draw(0);
         // `ok`: as in the dK/dV kernel, a warp that gave up keeps taking part in
@@ -668,16 +669,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 tc_fence_after();
                 float dp[W];
                 tmem_ldw<W>(tDP, dp);
-                if (DROP) {
-                    // dS = P (keep dZ - D): dZ is the product's dP, taken through the keep factors
-#pragma unroll
-                    for (int c = 0; c < W; ++c)
-                        dp[c] *= col_keep<W>(*reinterpret_cast<const uint32_t(*)[W / 4]>(dw), c, p.drop);
-                }
+                // with dropout dS = P (r keep dZ - D), as in the dK/dV kernel
+                const uint32_t(&km)[W / 4] = *reinterpret_cast<const uint32_t(*)[W / 4]>(dw);
+                const uint64_t rr = f2_pack(p.drop.rscale, p.drop.rscale);
 #pragma unroll
                 for (int i = 0; i < W / 2; ++i) {
-                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]),
-                                                      f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2)));
+                    const uint64_t z = DROP ? f2_fma(rr, f2_pack(kept<W>(km, dp, 2 * i), kept<W>(km, dp, 2 * i + 1)), ndlt2)
+                                            : f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2);
+                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]), z));
                     dp[2 * i] = a.x;
                     dp[2 * i + 1] = a.y;
                 }

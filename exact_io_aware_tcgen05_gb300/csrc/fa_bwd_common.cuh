@@ -235,23 +235,21 @@ __device__ __forceinline__ void tmem_st_pk(uint32_t taddr, const float (&v)[W]) 
     }
 }
 
-// keep factor (0 or 1 / keep probability) of column c, from the row's dropout words
+// v[c] with the dropped columns cleared (m: the row's keep masks, 4 columns a word)
 template <int W>
-__device__ __forceinline__ float col_keep(const uint32_t (&dw)[W / 4], int c, const DropoutParams& d) {
-    return keep_factor(dw[c >> 2], c & 3, d.thresh, d.rscale);
+__device__ __forceinline__ float kept(const uint32_t (&m)[W / 4], const float (&v)[W], int c) {
+    return __uint_as_float(__float_as_uint(v[c]) & keep_mask32(m[c >> 2], c));
 }
 
-// tmem_st_pk of v with the dropped columns zeroed (the 1 / keep-probability factor is
+// tmem_st_pk of v with the dropped columns cleared (the 1 / keep-probability factor is
 // left to the fp32 side: the dV epilogue, the dS arithmetic)
 template <int W, int E>
 __device__ __forceinline__ void tmem_st_pk_dropped(uint32_t taddr, const float (&v)[W],
-                                                   const uint32_t (&dw)[W / 4],
-                                                   const DropoutParams& d) {
+                                                   const uint32_t (&m)[W / 4]) {
     uint32_t w[W / 2];
 #pragma unroll
     for (int i = 0; i < W / 2; ++i)
-        w[i] = pack2<E>(v[2 * i] * keep_factor(dw[i >> 1], (2 * i) & 3, d.thresh, 1.f),
-                        v[2 * i + 1] * keep_factor(dw[i >> 1], (2 * i + 1) & 3, d.thresh, 1.f));
+        w[i] = pack2<E>(v[2 * i], v[2 * i + 1]) & keep_mask_pair(m[i >> 1], 2 * i);
     if constexpr (W == 64)
         tmem_st32(taddr, w);
     else

@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
                                       ((qt_first + n % nq) * kBlockM + W * wg) >> 2, kpos >> 2,
                                       static_cast<uint32_t>(b * s.Hq + g * s.group + n / nq),
                                       p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
+            keep_masks(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), p.drop.thresh);
         };
         if (DROP) draw(0);
         bool ok = true;
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
                         if (c < clo || c > chi) pv[c] = 0.f;
                 }
                 if (DROP)
-                    tmem_st_pk_dropped<W, E>(tS, pv, *reinterpret_cast<const uint32_t(*)[W / 4]>(dw), p.drop);
+                    tmem_st_pk_dropped<W, E>(tS, pv, *reinterpret_cast<const uint32_t(*)[W / 4]>(dw));
                 else
                     tmem_st_pk<W, E>(tS, pv);
                 tmem_st_wait();
@@ -355,26 +356,27 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
                     tmem_ld32(tDP + 32 * half, raw);
                     tmem_ld_wait();
                     reg_fence(raw);
+                    // with dropout dS = P (r keep dZ - D): the dropped columns cleared by
+                    // their masks, r folded into the multiply-add
                     float dp[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dp[i] = __uint_as_float(raw[i]);
-                    if (DROP) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            dp[i] *= col_keep<W>(*reinterpret_cast<const uint32_t(*)[W / 4]>(dw), 32 * half + i,
-                                                 p.drop);
+                    for (int i = 0; i < 32; ++i) {
+                        dp[i] = __uint_as_float(raw[i]);
+                        if (DROP)
+                            dp[i] = __uint_as_float(raw[i] & keep_mask32(dw[(32 * half + i) >> 2], i));
                     }
+                    const uint64_t rr = f2_pack(p.drop.rscale, p.drop.rscale);
                     uint32_t wds[16];
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 nd = ndlt4[8 * half + c4];
                         const int c = 32 * half + 4 * c4;
-                        const float2 a = f2_unpack(f2_mul(f2_pack(pv[c], pv[c + 1]),
-                                                          f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]),
-                                                                 f2_pack(nd.x, nd.y))));
-                        const float2 e = f2_unpack(f2_mul(f2_pack(pv[c + 2], pv[c + 3]),
-                                                          f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]),
-                                                                 f2_pack(nd.z, nd.w))));
+                        const uint64_t z0 = DROP ? f2_fma(rr, f2_pack(dp[4 * c4], dp[4 * c4 + 1]), f2_pack(nd.x, nd.y))
+                                                 : f2_add(f2_pack(dp[4 * c4], dp[4 * c4 + 1]), f2_pack(nd.x, nd.y));
+                        const uint64_t z1 = DROP ? f2_fma(rr, f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]), f2_pack(nd.z, nd.w))
+                                                 : f2_add(f2_pack(dp[4 * c4 + 2], dp[4 * c4 + 3]), f2_pack(nd.z, nd.w));
+                        const float2 a = f2_unpack(f2_mul(f2_pack(pv[c], pv[c + 1]), z0));
+                        const float2 e = f2_unpack(f2_mul(f2_pack(pv[c + 2], pv[c + 3]), z1));
                         wds[2 * c4] = pack2<E>(a.x, a.y);
                         wds[2 * c4 + 1] = pack2<E>(e.x, e.y);
                     }

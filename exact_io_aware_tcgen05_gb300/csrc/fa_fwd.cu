@@ -322,15 +322,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
         // Dropout: the Philox words of a key block do not depend on the scores, so each
         // row draws those of its next block right after handing P over, while the tensor
-        // cores compute that block's scores, and parks them in shared memory (its own
-        // 128-byte row; 16-byte chunks XOR-swizzled by the row so that a warp's
-        // accesses spread over the banks).
+        // cores compute that block's scores, turns them into keep masks and parks them in
+        // shared memory (its own 128-byte row; 16-byte chunks XOR-swizzled by the row so
+        // that a warp's accesses spread over the banks).
         uint4* drop_row = reinterpret_cast<uint4*>(smem + C::kTilesBytes + C::kBarBytes) +
                           (t * kBlockM + r) * (kBlockN / 16);
         auto draw_block = [&](int jj) {
             uint32_t dw[kBlockN / 4];
             dropout_words_rows<kBlockN / 4>(dw, q >> 2, ((kv_first + jj) * kBlockN) >> 2, hs,
                                             p.drop.offset, p.drop.seed_lo, p.drop.seed_hi, lane);
+            keep_masks(dw, p.drop.thresh);
 #pragma unroll
             for (int c = 0; c < kBlockN / 16; ++c)
                 drop_row[c ^ (r & 7)] = make_uint4(dw[4 * c], dw[4 * c + 1], dw[4 * c + 2], dw[4 * c + 3]);
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 // live registers of the pass below the softmax warps' budget)
                 for (int qtr = 0; qtr < 4 && !F8; ++qtr) {
                     uint32_t pk[16];
-                    // dropout: the random bytes of keys kb + 32 qtr .. + 31 of this row;
+                    // dropout: the keep masks of keys kb + 32 qtr .. + 31 of this row;
                     // l sums the probabilities before dropout, the product takes the kept
                     // ones (the 1 / keep-probability factor is applied to O in fp32 at the
                     // end, so the 16-bit P carries no extra rounding)
@@ -436,13 +437,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
                         const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
                         rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
-                        if (DROP)
-                            pk[c] = pack2<E>(p0 * keep_factor(dw[(c >> 1) % (DROP ? 8 : 1)], (2 * c) & 3,
-                                                              p.drop.thresh, 1.f),
-                                             p1 * keep_factor(dw[(c >> 1) % (DROP ? 8 : 1)], (2 * c + 1) & 3,
-                                                              p.drop.thresh, 1.f));
-                        else
-                            pk[c] = pack2<E>(p0, p1);
+                        pk[c] = pack2<E>(p0, p1);
+                        if (DROP) pk[c] &= keep_mask_pair(dw[(c >> 1) % (DROP ? 8 : 1)], 2 * c);
                     }
                     tmem_st16(tS + 16 * qtr, pk);
                 }

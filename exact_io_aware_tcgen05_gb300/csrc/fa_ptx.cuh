@@ -668,9 +668,27 @@ __device__ __forceinline__ void dropout_words_cols(uint32_t (&words)[NB], int I0
     }
 }
 
-// keep factor of byte b of a word: rscale if kept, else 0
-__device__ __forceinline__ float keep_factor(uint32_t word, int b, uint32_t thresh, float rscale) {
-    return ((word >> (8 * b)) & 0xFFu) >= thresh ? rscale : 0.f;
+// Dropout keep masks.  keep_masks turns a row's dropout words into byte masks once
+// per step (byte k of a mask is 0xff iff byte k of the word, the random byte of the
+// column, is >= the threshold); the element-wise passes then clear dropped values
+// with a byte permute and an AND: a kept value passes unchanged, a dropped one
+// becomes +0.
+template <int N>
+__device__ __forceinline__ void keep_masks(uint32_t (&w)[N], uint32_t thresh) {
+    const uint32_t t4 = thresh * 0x01010101u;
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __vcmpgeu4(w[i], t4);
+}
+
+// all 32 bits of column c's mask byte (the AND mask of an fp32 value)
+__device__ __forceinline__ uint32_t keep_mask32(uint32_t m, int c) {
+    return __byte_perm(m, 0u, static_cast<uint32_t>(c & 3) * 0x1111u);
+}
+
+// the AND mask of a 16-bit pair, columns c (low half) and c + 1 (high half), c even
+__device__ __forceinline__ uint32_t keep_mask_pair(uint32_t m, int c) {
+    const uint32_t a = c & 3, b = (c + 1) & 3;
+    return __byte_perm(m, 0u, a | (a << 4) | (b << 8) | (b << 12));
 }
 
 }  // namespace fa
