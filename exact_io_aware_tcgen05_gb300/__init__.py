@@ -26,6 +26,7 @@ __all__ = [
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
+    "fa_debug_checks_enabled", "fa_debug_check_selftest",
     "library_path",
 ]
 
@@ -55,7 +56,8 @@ def load(path: str | None = None):
     global _lib
     if _lib is not None:
         return _lib
-    path = path or library_path
+    # FA_GB300_LIBRARY: another build of the library (e.g. the bounds-checking one)
+    path = path or os.environ.get("FA_GB300_LIBRARY") or library_path
     if not os.path.exists(path):
         raise RuntimeError(f"{path} not found: build it with exact_io_aware_tcgen05_gb300.build.build()")
     lib = ctypes.CDLL(path)
@@ -103,6 +105,10 @@ def load(path: str | None = None):
     lib.fa_set_wait_limit_cycles.restype = None
     lib.fa_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), _i]
     lib.fa_set_launch_events.restype = None
+    lib.fa_debug_checks_enabled.argtypes = []
+    lib.fa_debug_checks_enabled.restype = _i
+    lib.fa_debug_check_selftest.argtypes = [_vp]
+    lib.fa_debug_check_selftest.restype = _i
     lib.fa_last_error.argtypes = []
     lib.fa_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -271,6 +277,18 @@ def fa_set_launch_events(events) -> None:
     handles = [e if isinstance(e, int) else e.cuda_event for e in events]
     _armed_events = (ctypes.c_void_p * len(handles))(*handles)
     load().fa_set_launch_events(_armed_events, len(handles))
+
+
+def fa_debug_checks_enabled() -> bool:
+    """True for the bounds-checking build of the library."""
+    return bool(load().fa_debug_checks_enabled())
+
+
+def fa_debug_check_selftest(stream=None, check: bool = True) -> int:
+    st = load().fa_debug_check_selftest(_stream(stream))
+    if check:
+        _check(st)
+    return st
 
 
 def fa_set_wait_limit_cycles(cycles: int) -> None:

@@ -2,6 +2,7 @@
 // checks, TMA descriptor encoding, the device status word and kernel launches.
 #include "../../include/fa.h"
 #include "fa_kernels.h"
+#include "fa_ptx.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -568,6 +569,9 @@ fa_status fa_device_status(cudaStream_t stream) {
         if (e != cudaSuccess) return cuda_fail(e, "fa_device_status: clearing the status word");
         if (word == 5)
             return fail(FA_ERR_TIMEOUT, "a kernel gave up a bounded wait (device status %d)", word);
+        if (word == 7)
+            return fail(FA_ERR_CUDA, "a kernel of the bounds-checking build found a global index "
+                        "out of its tensor and skipped the access (device status %d)", word);
         return fail(FA_ERR_CUDA, "a kernel reported device status %d (misaligned shared memory)",
                     word);
     }
@@ -675,6 +679,8 @@ fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scales, int nb, int
     p.out = x8;
     p.scales = scales;
     p.heads = H;
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fp8 quantisation: cannot resolve the device status word");
     p.nb = nb;
     const cudaError_t e = launch_fp8_quant_qk(p, d, num_blocks(g, kBlockM, H), stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_qk launch");
@@ -705,6 +711,8 @@ fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_toke
     p.out = vt8;
     p.scales = scales;
     p.heads = H;
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fp8 quantisation: cannot resolve the device status word");
     p.vt_tokens = vt_tokens;
     const cudaError_t e = launch_fp8_quant_v(p, d, num_blocks(g, kBlockN, H), stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_v launch");
@@ -761,6 +769,45 @@ fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const
     if (e == cudaSuccess) e = launch_fwd(p, d, stream);
     if (e == cudaSuccess) e = record(ev, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
+    return FA_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ debug checks
+
+namespace fa {
+namespace {
+
+// One thread tests an index one past a three-element range: a build with the bounds
+// checks records kDevBadIndex; no memory is touched either way.
+__global__ void debug_check_selftest_kernel(int* status) {
+    (void)fa_index_ok(3, 3, status);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_debug_checks_enabled(void) {
+#ifdef FA_DEBUG_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+fa_status fa_debug_check_selftest(cudaStream_t stream) {
+    using namespace fa;
+    t_last_error[0] = '\0';
+    if (!fa_debug_checks_enabled())
+        return fail(FA_ERR_UNSUPPORTED, "fa_debug_check_selftest: not a bounds-checking build");
+    int* st = status_word_ptr();
+    if (!st) return fail(FA_ERR_CUDA, "fa_debug_check_selftest: cannot resolve the device status word");
+    debug_check_selftest_kernel<<<1, 1, 0, stream>>>(st);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "fa_debug_check_selftest launch");
     return FA_OK;
 }
 

@@ -90,8 +90,10 @@ __device__ __forceinline__ void kv_bound_cta(const BwdParams& p, int bi) {
     for (int i = 0; i < 8; ++i) atomicMax(&s_max[8 * sub + i], __float_as_uint(kmax[i]));
     if (sub == 0) atomicMax(&s_max[D], __float_as_uint(vmax));
     __syncthreads();
-    float* out = p.kv_bound + (static_cast<long long>(g) * kBoundSlots + slot) * (D + 1);
-    for (int i = threadIdx.x; i <= D; i += kPreThreads) out[i] = __uint_as_float(s_max[i]);
+    const long long o0 = (static_cast<long long>(g) * kBoundSlots + slot) * (D + 1);
+    for (int i = threadIdx.x; i <= D; i += kPreThreads)
+        if (fa_index_ok(o0 + i, static_cast<long long>(s.Hkv) * kBoundSlots * (D + 1), p.status))
+            p.kv_bound[o0 + i] = __uint_as_float(s_max[i]);
 }
 
 template <int D, int E>
@@ -149,8 +151,10 @@ __global__ void __launch_bounds__(kPreThreads) fa_bwd_preprocess_kernel(const __
             long long idx;
             if (s.cu_seqlens) idx = static_cast<long long>(h) * s.total_tokens + token;
             else idx = (static_cast<long long>(token / s.N) * s.Hq + h) * s.N + token % s.N;
-            p.delta[idx] = acc;
-            if (p.dq_acc) p.row_scale[idx] = fixed_point_scale(sqrtf(dsq));
+            if (fa_index_ok(idx, rows, p.status)) {
+                p.delta[idx] = acc;
+                if (p.dq_acc) p.row_scale[idx] = fixed_point_scale(sqrtf(dsq));
+            }
         }
     }
 }
@@ -320,6 +324,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             const int q = (qt_first + m % nq) * kBlockM + W * wg + (r % W);
             if (q >= len) return r < W ? -kPosInf : 0.f;
             const long long idx = row_stat_index(s, b, h, seq_start, q);
+            if (!fa_index_ok(idx, static_cast<long long>(s.total_tokens) * s.Hq, p.status)) return 0.f;
             return r < W ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
         };
         float next_stat = fetch_stat(0);
@@ -440,12 +445,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             fence_proxy_async_smem();
             named_bar_sync(kBarEpi, C::kEwThreads);
             if (warp == 4 && lane == 0) {
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_store_3d(&p.tm_dv, smem_addr(sSlots + c * C::kChunkBytes), c * 64, g,
-                                 seq_start + kb);
-                    tma_store_3d(&p.tm_dk, smem_addr(sSlots + C::kTileBytes + c * C::kChunkBytes),
-                                 c * 64, g, seq_start + kb);
-                }
+                if (fa_box_ok(seq_start + kb, kBlockN, s.total_tokens, g, s.Hkv, p.status))
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_store_3d(&p.tm_dv, smem_addr(sSlots + c * C::kChunkBytes), c * 64, g,
+                                     seq_start + kb);
+                        tma_store_3d(&p.tm_dk, smem_addr(sSlots + C::kTileBytes + c * C::kChunkBytes),
+                                     c * 64, g, seq_start + kb);
+                    }
                 bulk_commit_group();
                 bulk_wait_read_all();   // the CTA's shared memory outlives the reads
             }
@@ -454,7 +460,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
             store_acc_row<kSC, E>(t_acc, mul,
                                   static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + row + c0,
-                                  kpos < len);
+                                  kpos < len && fa_index_ok(static_cast<long long>(seq_start + kpos) * s.Hkv + g,
+                                                            static_cast<long long>(s.total_tokens) * s.Hkv, p.status));
         }
     }
     teardown_bwd_cta<D>(bars, warp);
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             uint32_t wq[kQW], wd[kQW];
 #pragma unroll
             for (int i = 0; i < kQW; ++i) wq[i] = wd[i] = 0u;
-            if (valid) {
+            if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                     static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
                 const long long off = (static_cast<long long>(seq_start + q) * s.Hq + h) * D +
                                       2 * kQW * wg;
                 const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + off);
@@ -616,7 +624,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             named_bar_arrive(kBarOperands, kOperandBar);
         }
         float lse2 = kPosInf, dlt = 0.f;
-        if (valid) {
+        if (valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
+                                 static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
             const long long idx = row_stat_index(s, b, h, seq_start, q);
             lse2 = __ldg(p.lse + idx) * kLog2eF;
             dlt = __ldg(p.delta + idx);
@@ -703,9 +712,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             fence_proxy_async_smem();
             named_bar_sync(kBarEpi, C::kEwThreads);
             if (warp == 4 && lane == 0) {
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_store_3d(&p.tm_dq, smem_addr(sSlots + c * C::kChunkBytes), c * 64, h,
-                                 seq_start + q0);
+                if (fa_box_ok(seq_start + q0, kBlockM, s.total_tokens, h, s.Hq, p.status))
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_store_3d(&p.tm_dq, smem_addr(sSlots + c * C::kChunkBytes), c * 64, h,
+                                     seq_start + q0);
                 bulk_commit_group();
                 bulk_wait_read_all();
             }
@@ -713,7 +723,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
             store_acc_row<kSC, E>(t_acc, p.scale, static_cast<uint16_t*>(p.dq) + row + kSC * wg,
-                                  valid);
+                                  valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                                       static_cast<long long>(s.total_tokens) * s.Hq,
+                                                       p.status));
         }
     }
     teardown_bwd_cta<D>(bars, warp);

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
             const int q = (qt_first + m % nq) * kBlockM + W * wg + (r % W);
             if (q >= len) return r < W ? -kPosInf : 0.f;
             const long long idx = row_stat_index(s, b, h, seq_start, q);
+            if (!fa_index_ok(idx, static_cast<long long>(s.total_tokens) * s.Hq, p.status)) return 0.f;
             return r < W ? -__ldg(p.lse + idx) * kLog2eF : -__ldg(p.delta + idx);
         };
         float next_stat = fetch_stat(0);
@@ -404,12 +405,13 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
             fence_proxy_async_smem();
             named_bar_sync(kFBarEpi, C::kEwThreads);
             if (warp == 4 && lane == 0) {
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_store_3d(&p.tm_dv, smem_addr(sSlots + c * C::kChunkBytes), c * 64, g,
-                                 seq_start + kb);
-                    tma_store_3d(&p.tm_dk, smem_addr(sSlots + C::kTileBytes + c * C::kChunkBytes),
-                                 c * 64, g, seq_start + kb);
-                }
+                if (fa_box_ok(seq_start + kb, kBlockN, s.total_tokens, g, s.Hkv, p.status))
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_store_3d(&p.tm_dv, smem_addr(sSlots + c * C::kChunkBytes), c * 64, g,
+                                     seq_start + kb);
+                        tma_store_3d(&p.tm_dk, smem_addr(sSlots + C::kTileBytes + c * C::kChunkBytes),
+                                     c * 64, g, seq_start + kb);
+                    }
                 bulk_commit_group();
                 bulk_wait_read_all();
             }
@@ -417,7 +419,8 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
             tc_fence_after();
             const long long row = (static_cast<long long>(seq_start + kpos) * s.Hkv + g) * D;
             store_acc_row<D, E>(t_acc, mul, static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + row,
-                                kpos < len);
+                                kpos < len && fa_index_ok(static_cast<long long>(seq_start + kpos) * s.Hkv + g,
+                                                          static_cast<long long>(s.total_tokens) * s.Hkv, p.status));
         }
     } else {
         regs_raise<C::kRegsDq>();
@@ -453,7 +456,8 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
 #pragma unroll
             for (int m = 0; m < (D == 128 ? 4 : 1); ++m) {
                 const int q = q0 + (D == 128 ? 32 * m + lane : ln);
-                rs[m] = q < len ? __ldg(p.row_scale + row_stat_index(s, b, h, seq_start, q)) : 0.f;
+                rs[m] = (q < len && fa_index_ok(row_stat_index(s, b, h, seq_start, q), T * s.Hq, p.status))
+                            ? __ldg(p.row_scale + row_stat_index(s, b, h, seq_start, q)) : 0.f;
             }
             float acc[NV];
             if (ok) ok = warp_wait(smem_addr(&bars->dq_full), n & 1, abort_flag, p.timeout_cycles, p.status);
@@ -474,9 +478,12 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1) fa_bwd_fused_kernel(
 #pragma unroll
                 for (int j = 0; j < NV; ++j) {
                     const float sj = __shfl_sync(0xffffffffu, rs[j / 32], j % 32);
-                    if (j < rows) red_add_s32(accg + j * 128, __float2int_rn(acc[j] * sj * fc));
+                    if (j < rows && fa_index_ok((static_cast<long long>(h) * T + seq_start + q0 + j) * 128 + ln,
+                                                T * s.Hq * 128, p.status))
+                        red_add_s32(accg + j * 128, __float2int_rn(acc[j] * sj * fc));
                 }
-            } else if (ln < rows) {
+            } else if (ln < rows && fa_index_ok(static_cast<long long>(h) * D * T + (D - 1) * T + seq_start + q0 + ln,
+                                                T * s.Hq * D, p.status)) {
                 int* accg = p.dq_acc + static_cast<long long>(h) * D * T + seq_start + q0 + ln;
 #pragma unroll
                 for (int c = 0; c < NV; ++c) red_add_s32(accg + c * T, __float2int_rn(acc[c] * rs[0] * sFc[c]));
@@ -512,7 +519,9 @@ __global__ void __launch_bounds__(kConvThreads) fa_bwd_dq_convert_kernel(const _
         for (int k = 0; k < kConvTokens * D / kConvThreads; ++k) {
             const int idx = k * kConvThreads + threadIdx.x;
             const int c = idx / kConvTokens, j = idx % kConvTokens;
-            sT[c][j] = (t0 + j < T) ? p.dq_acc[(static_cast<long long>(h) * D + c) * T + t0 + j] : 0;
+            sT[c][j] = (t0 + j < T && fa_index_ok((static_cast<long long>(h) * D + c) * T + t0 + j,
+                                                  T * s.Hq * D, p.status))
+                           ? p.dq_acc[(static_cast<long long>(h) * D + c) * T + t0 + j] : 0;
         }
     }
     __syncthreads();
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(kConvThreads) fa_bwd_dq_convert_kernel(const _
         const int idx = k * kConvThreads + threadIdx.x;
         const int j = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
         const long long t = t0 + j;
-        if (t >= T) continue;
+        if (t >= T || !fa_index_ok(t * s.Hq + h, T * s.Hq, p.status)) continue;
         int v[8];
         if constexpr (D == 128) {
             const int4* src = reinterpret_cast<const int4*>(p.dq_acc + (static_cast<long long>(h) * T + t) * D + c8);

@@ -96,14 +96,16 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quant_qk_kernel(const __gri
     uint4 v[kN];
     const float scale = block_scale(load_block<D>(static_cast<const uint16_t*>(p.x), p.heads, start,
                                                   len, h, blk, v, red));
-    if (threadIdx.x == 0)
-        p.scales[static_cast<long long>(h) * p.nb + seq_block_col(p.seq, b) + blk] = scale;
+    const long long sidx = static_cast<long long>(h) * p.nb + seq_block_col(p.seq, b) + blk;
+    if (threadIdx.x == 0 && fa_index_ok(sidx, static_cast<long long>(p.heads) * p.nb, p.status))
+        p.scales[sidx] = scale;
     const int u = threadIdx.x % kU, r0 = threadIdx.x / kU;
     uint8_t* out = static_cast<uint8_t*>(p.out);
 #pragma unroll
     for (int k = 0; k < kN; ++k) {
         const int row = blk * kBlockM + r0 + k * kRows;
-        if (row < len)
+        if (row < len && fa_index_ok(static_cast<long long>(start + row) * p.heads + h,
+                                     static_cast<long long>(p.seq.total_tokens) * p.heads, p.status))
             *reinterpret_cast<uint2*>(out + (static_cast<long long>(start + row) * p.heads + h) * D +
                                       8 * u) = quant8(v[k], scale);
     }
@@ -128,7 +130,8 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_v_amax_kernel(const __grid_
     seq_bounds(p.seq, b, start, len);
     uint4 v[kBlockM * D / 8 / kQuantThreads];
     const float m = load_block<D>(static_cast<const uint16_t*>(p.x), p.heads, start, len, h, blk, v, red);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && fa_index_ok(static_cast<long long>(h) * p.seq.B + b,
+                                        static_cast<long long>(p.heads) * p.seq.B, p.status))
         atomicMax(reinterpret_cast<int*>(p.scales + static_cast<long long>(h) * p.seq.B + b),
                   __float_as_int(m));
 }
@@ -172,7 +175,9 @@ __global__ void __launch_bounds__(128) fp8_v_quant_kernel(const __grid_constant_
             const uint32_t a2 = ch < 4 ? c[4 * q + 2].x : c[4 * q + 2].y, a3 = ch < 4 ? c[4 * q + 3].x : c[4 * q + 3].y;
             w[q] = __byte_perm(__byte_perm(a0, a1, sel), __byte_perm(a2, a3, sel), 0x5410);
         }
-        uint8_t* dst = out + (static_cast<long long>(h) * D + 8 * u + ch) * p.vt_tokens + col;
+        const long long di = (static_cast<long long>(h) * D + 8 * u + ch) * p.vt_tokens + col;
+        if (!fa_index_ok(di + kT - 1, static_cast<long long>(p.heads) * D * p.vt_tokens, p.status)) continue;
+        uint8_t* dst = out + di;
         if constexpr (kT == 16)
             *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1 % (kT / 4)], w[2 % (kT / 4)], w[3 % (kT / 4)]);
         else

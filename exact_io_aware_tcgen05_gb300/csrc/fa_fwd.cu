@@ -314,9 +314,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int blk_col = F8 ? seq_block_col(s, b) : 0;
         // (a tile wholly past the sequence end reads its last block's scale; its rows
         // are never stored)
-        const float sq = F8 ? __ldg(p.q_scale + static_cast<long long>(h) * p.nb + blk_col +
-                                    min(q0 / kBlockM + t, ceil_div(len, kBlockM) - 1))
-                            : 1.f;
+        const long long sq_idx = static_cast<long long>(h) * p.nb + blk_col +
+                                 min(q0 / kBlockM + t, ceil_div(len, kBlockM) - 1);
+        const float sq = (F8 && fa_index_ok(sq_idx, static_cast<long long>(s.Hq) * p.nb, p.status))
+                             ? __ldg(p.q_scale + sq_idx) : 1.f;
         const float* ks_row = F8 ? p.k_scale + static_cast<long long>(g) * p.nb + blk_col : nullptr;
         const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h);   // dropout counter word
 
@@ -379,7 +380,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kBlockN - 8 + i]);
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7]));
-                const float sl2b = F8 ? sl2 * sq * __ldg(ks_row + kv_first + j) : sl2;
+                const float sl2b =
+                    (F8 && fa_index_ok(static_cast<long long>(g) * p.nb + blk_col + kv_first + j,
+                                       static_cast<long long>(s.Hkv) * p.nb, p.status))
+                        ? sl2 * sq * __ldg(ks_row + kv_first + j) : sl2;
                 const float m_blk = mx * sl2b;
                 float alpha = 1.f;
                 bool rescale = false;
@@ -475,7 +479,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         // uniform over the warpgroup.
         const bool valid = q < len;
         // fp8: O carries the scale of V (per sequence and key/value head)
-        const float vs = F8 ? __ldg(p.v_scale + static_cast<long long>(g) * s.B + b) : 1.f;
+        const float vs = (F8 && fa_index_ok(static_cast<long long>(g) * s.B + b,
+                                            static_cast<long long>(s.Hkv) * s.B, p.status))
+                             ? __ldg(p.v_scale + static_cast<long long>(g) * s.B + b) : 1.f;
         const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) * vs / l : 0.f;
         if (named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
             tc_fence_after();
@@ -484,9 +490,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             fence_proxy_async_smem();
             named_bar_sync(kFwdBarEpi + t, kBlockM);
             if (quad == 0 && lane == 0) {
-                for (int c = 0; c < C::kOChunks; ++c)
-                    tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
-                                 seq_start + tile_q_first);
+                if (fa_box_ok(seq_start + tile_q_first, kBlockM, s.total_tokens, h, s.Hq, p.status))
+                    for (int c = 0; c < C::kOChunks; ++c)
+                        tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
+                                     seq_start + tile_q_first);
                 bulk_commit_group();
                 bulk_wait_read_all();   // the CTA's shared memory outlives the reads
             }
@@ -505,7 +512,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack2<EO>(__uint_as_float(orow[2 * i]) * inv_l,
                                      __uint_as_float(orow[2 * i + 1]) * inv_l);
-                if (valid) {
+                if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                         static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
                     uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -513,7 +521,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 }
             }
         }
-        if (ok && valid)
+        if (ok && valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
+                                       static_cast<long long>(s.total_tokens) * s.Hq, p.status))
             p.lse[row_stat_index(s, b, h, seq_start, q)] =
                 (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
     }

@@ -108,6 +108,7 @@ struct Fp8QuantParams {
     int heads;
     int nb;             // Q/K: columns of the scale array
     long long vt_tokens;  // V: columns of V^T
+    int* status;          // device status word (the debug build's bounds checks)
 };
 
 // Launchers (defined in the kernel translation units).  They only enqueue on

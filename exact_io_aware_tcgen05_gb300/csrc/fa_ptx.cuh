@@ -20,9 +20,31 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 __device__ __forceinline__ bool elect_lane0() { return lane_id() == 0; }
 
 // Device-wide status word, written (never read) by kernels when a bounded wait
-// gives up (kDevTimeout) or a launch finds its shared memory misaligned
-// (kDevBadSmem).  Host code reads it with fa_device_status().
-enum : int { kDevOk = 0, kDevTimeout = 5, kDevBadSmem = 6 };
+// gives up (kDevTimeout), a launch finds its shared memory misaligned
+// (kDevBadSmem), or -- in a build with FA_DEBUG_CHECKS -- a computed global index
+// or TMA store box falls outside its tensor (kDevBadIndex).  Host code reads it
+// with fa_device_status().
+enum : int { kDevOk = 0, kDevTimeout = 5, kDevBadSmem = 6, kDevBadIndex = 7 };
+
+// Bounds checks of the debug build.  With FA_DEBUG_CHECKS defined, fa_index_ok
+// tests 0 <= idx < size; a failing check records kDevBadIndex and the caller skips
+// the access (nothing traps).  Without it the checks are compiled away.
+#ifdef FA_DEBUG_CHECKS
+__device__ __forceinline__ bool fa_index_ok(long long idx, long long size, int* status) {
+    if (idx >= 0 && idx < size) return true;
+    atomicExch(status, kDevBadIndex);
+    return false;
+}
+#else
+__device__ __forceinline__ bool fa_index_ok(long long, long long, int*) { return true; }
+#endif
+
+// A TMA store box of `rows` token rows from `row` and one head: it must lie inside
+// [0, tokens) x [0, heads) (stores may not start at negative coordinates).
+__device__ __forceinline__ bool fa_box_ok(long long row, int rows, long long tokens, int head,
+                                          int heads, int* status) {
+    return fa_index_ok(row, tokens - rows + 1, status) && fa_index_ok(head, heads, status);
+}
 
 // ---------------------------------------------------------------- mbarrier
 

@@ -350,6 +350,22 @@ void fa_set_wait_limit_cycles(long long cycles);
  */
 void fa_set_launch_events(const cudaEvent_t* events, int count);
 
+/*
+ * Bounds-checking build.  The library built with FA_DEBUG_CHECKS defined
+ * (exact_io_aware_tcgen05_gb300.build.build(debug=True), libfa_gb300_debug.so)
+ * checks, inside every kernel, each computed global index and TMA store box
+ * against its tensor; a failing check skips the access and records device
+ * status 7, which fa_device_status() reports as FA_ERR_CUDA with a message.
+ * Nothing traps.  (A stand-in for a memory checker; the kernels are otherwise
+ * identical.)
+ *   fa_debug_checks_enabled: 1 in that build, 0 in the normal one.
+ *   fa_debug_check_selftest: enqueues one thread that tests an index one past
+ *     its range without touching memory, so that fa_device_status() must then
+ *     report the failed check; FA_ERR_UNSUPPORTED in the normal build.
+ */
+int fa_debug_checks_enabled(void);
+fa_status fa_debug_check_selftest(cudaStream_t stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* fa_last_error(void);
 

@@ -28,3 +28,16 @@ def fa():
     import exact_io_aware_tcgen05_gb300 as pkg
     pkg.load()          # raises if the compiled library is missing
     return pkg
+
+
+@pytest.fixture(autouse=True)
+def _device_status_after_each_test(request):
+    """With FA_GB300_CHECK_STATUS set (the bounds-checking runs), every GPU test
+    must leave the device status word clear: a kernel whose index check failed
+    records status 7 there instead of touching memory."""
+    yield
+    if not os.environ.get("FA_GB300_CHECK_STATUS") or "fa" not in request.fixturenames:
+        return
+    import exact_io_aware_tcgen05_gb300 as pkg
+    assert pkg.fa_debug_checks_enabled(), "FA_GB300_CHECK_STATUS set without the checking build"
+    pkg.fa_device_status()      # raises on a recorded failed check

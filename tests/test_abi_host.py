@@ -254,3 +254,19 @@ def test_rejected_static_workspace_call_uses_up_armed_events(lib):
     # its own argument check
     assert _fwd(fa, q=None) == fa.FA_ERR_INVALID_ARG
     assert "non-null" in fa.fa_last_error()
+
+
+def test_release_build_has_no_bounds_checks(lib):
+    fa, _ = lib
+    assert not fa.fa_debug_checks_enabled()
+    # refused before any CUDA call
+    assert fa.fa_debug_check_selftest(None, check=False) == fa.FA_ERR_UNSUPPORTED
+    assert "bounds-checking" in fa.fa_last_error()
+
+
+def test_bounds_checking_build_exports_the_same_symbols():
+    from exact_io_aware_tcgen05_gb300 import build as b
+    raw = ctypes.CDLL(b.build(debug=True))
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    assert raw.fa_debug_checks_enabled() == 1
