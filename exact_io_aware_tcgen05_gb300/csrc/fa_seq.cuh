@@ -48,22 +48,31 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // First block slot of sequence b of a packed batch for blocks of `rows` rows:
 // floor(start_b / rows) + b.  The slot ranges [first(b), first(b) + ceil(len_b /
 // rows)) are disjoint, increase with b and lie below ceil(T / rows) + B, so the
-// sequence that owns a slot is found by a binary search over cu_seqlens (O(log B)
-// loads) rather than a walk over all earlier sequences.
+// sequence that owns a slot is found by a search over cu_seqlens rather than a walk
+// over all earlier sequences.
 __device__ __forceinline__ int seq_first_slot(const SeqInfo& s, int b, int rows) {
-    int st, len;
-    seq_bounds(s, b, st, len);
-    return st / rows + b;
+    const int start = min(max(__ldg(s.cu_seqlens + b), 0), s.total_tokens);   // as seq_bounds
+    return start / rows + b;
 }
 
 // The sequence b whose slot range may hold `slot`: the last b with first(b) <= slot
-// (first() strictly increases with b).
+// (first() strictly increases with b; first(0) = 0).  A 32-way search by the whole
+// warp, which must call it converged with the same arguments: each round the lanes
+// test 32 evenly spaced candidates with one load each, and the count of those at
+// or below `slot` (a prefix of the lanes) narrows the range 32-fold.  One round of
+// loads for up to 33 sequences, two up to 1057; a binary search by one thread
+// would wait for about log2(B) dependent loads.
 __device__ __forceinline__ int seq_of_slot(const SeqInfo& s, int slot, int rows) {
-    int lo = 0, hi = s.B - 1;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = s.B - 1;   // the answer lies in [lo, hi]
     while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (seq_first_slot(s, mid, rows) <= slot) lo = mid;
-        else hi = mid - 1;
+        const int step = (hi - lo + 31) / 32;
+        const int cand = lo + (lane + 1) * step;
+        const bool below = cand <= hi && seq_first_slot(s, cand, rows) <= slot;
+        const int k = __popc(__ballot_sync(0xffffffffu, below));
+        const int nlo = lo + k * step;
+        hi = min(hi, nlo + step - 1);
+        lo = nlo;
     }
     return lo;
 }
@@ -80,7 +89,8 @@ __device__ __forceinline__ int seq_block_col(const SeqInfo& s, int b) {
 // Heads per scheduling chunk (see map_work) unless the launcher picks another.
 constexpr int kHeadChunk = 8;
 
-// Maps CTA index w to (sequence b, head h, block index blk of `rows` rows).
+// Maps CTA index w to (sequence b, head h, block index blk of `rows` rows).  Called
+// by every thread of the CTA at entry (whole warps: the packed search is per warp).
 // Heads are taken in chunks of `chunk`: all work items of a chunk are launched
 // before the next chunk's, so the CTAs in flight touch few heads and the tiles
 // they share stay in L2.  Within a chunk the order is by "level": level 0 is the
