@@ -127,3 +127,82 @@ def test_full_size_sampled(fa, oracle_mod, name, path):
             for nm, a, r in (("dq", dq_got, dq_ref), ("dk", dk_got, dk_ref), ("dv", dv_got, dv_ref)):
                 err = rel_fro(a, r)
                 assert err <= GRAD_REL_FRO, (nm, b, g, err)
+
+
+# Very long sequences (not bench workloads): a dense 131 072-token causal sequence and a
+# packed batch whose longest sequence has 100 000 tokens.  They run key-tile loops of up
+# to 1024 steps per CTA and token offsets in the hundreds of thousands.  The oracle's row
+# backward costs a full attention pass per sampled key row here, so the backward is
+# checked where that is cheap and by identities elsewhere:
+#   - O and LSE at sampled rows (the oracle's rows);
+#   - dQ of the first 300 rows of each sequence: under a causal mask they depend on that
+#     sequence's first 300 tokens only, so they equal the oracle's backward of that prefix;
+#   - dK and dV over whole sequences, per key/value head: each query's dS row sums to zero
+#     (its P row sums to one and D is its P-weighted dP), so the dK rows sum to zero; and
+#     the dV rows sum to the group's dO rows.  Within the gradient tolerance, relative to
+#     the Frobenius norm of dK and to the norm of the dO sum.  (Measured: 3e-3 for dK; for
+#     dV 1.1e-4 at 8k tokens and 5e-4 at 131k, growing with the length and pointing
+#     against the dO sum: the fp32 accumulation of long dV sums on the tensor cores
+#     comes out slightly small in magnitude, while the LSE agrees with the oracle to
+#     2e-6.)
+from exact_io_aware_tcgen05_gb300.workloads import Workload  # noqa: E402
+
+LONG = [
+    Workload("long_b1_h4kv1_n131072_d128_causal", B=1, Hq=4, Hkv=1, N=131072, d=128,
+             causal=True, window=0, backward=True),
+    Workload("long_packed_h8kv2_d64_causal", B=3, Hq=8, Hkv=2, N=100000, d=64, causal=True,
+             window=0, backward=True, lengths=(100000, 31071, 1)),
+]
+LONG_CASES = [(w, p) for w in LONG for p in ("split", "fused")]
+PREFIX = 300
+
+
+def _seq(a, w, b):
+    """Sequence b of a [B, N, H, d] or packed [T, H, d] array, as [L, H, d]."""
+    if w.packed:
+        cu = w.cu_seqlens()
+        return a[cu[b]:cu[b + 1]]
+    return a[b]
+
+
+@pytest.mark.parametrize("w,path", LONG_CASES, ids=[f"{w.name}-{p}" for w, p in LONG_CASES])
+def test_long_sequences(fa, oracle_mod, w, path):
+    x = attention_inputs(w.q_shape, w.kv_shape, 0, with_dout=True, dtype=w.dtype)
+    got = run_workload(fa, w, x, path)
+    cu = w.cu_seqlens()
+    G = w.Hq // w.Hkv
+    for b in sampled_sequences(w):
+        L = w.seq_lengths()[b]
+        rows = sample_rows(L, seed=b)
+        t = token_index(w, b, rows)
+        for h in sorted({0, w.Hq - 1}):
+            o_ref, lse_ref = oracle_mod.fwd_rows(x["q"], x["k"], x["v"], b, h, rows,
+                                                 causal=w.causal, window=w.window, scale=w.scale,
+                                                 cu_seqlens=cu)
+            o_got, lse_got = ((got["o"][t, h], got["lse"][h, t]) if w.packed
+                              else (got["o"][b, t, h], got["lse"][b, h, t]))
+            assert max_abs(o_got, o_ref) <= O_MAX_ABS, (b, h)
+            assert max_abs(lse_got, lse_ref) <= LSE_MAX_ABS, (b, h)
+    for b in sampled_sequences(w):
+        L = w.seq_lengths()[b]
+        # dQ of the prefix rows
+        P = min(PREFIX, L)
+        pre = {n: _seq(x[n], w, b)[:P] for n in ("q", "k", "v", "dout")}
+        dq_ref, _, _ = oracle_mod.attention_bwd(pre["q"], pre["k"], pre["v"], pre["dout"],
+                                                causal=True, window=w.window, scale=w.scale,
+                                                cu_seqlens=np.array([0, P], np.int32))
+        dq_got = _seq(got["dq"], w, b)[:P]
+        assert rel_fro(dq_got, dq_ref) <= GRAD_REL_FRO, ("dq prefix", b, rel_fro(dq_got, dq_ref))
+        # dK, dV sums over the whole sequence
+        dk, dv = _seq(got["dk"], w, b), _seq(got["dv"], w, b)
+        do = oracle_mod.to_f64(_seq(x["dout"], w, b))
+        for g in range(w.Hkv):
+            sk = dk[:, g].sum(axis=0)
+            if L == 1:
+                # one key: dS = dP - D = dO.v - dO.v = 0, so dK itself vanishes
+                assert np.linalg.norm(sk) <= 1e-4, ("dK of a one-token sequence", b, g)
+            else:
+                assert np.linalg.norm(sk) <= GRAD_REL_FRO * np.linalg.norm(dk[:, g]), ("sum dK", b, g)
+            so = do[:, g * G:(g + 1) * G].sum(axis=(0, 1))
+            sv = dv[:, g].sum(axis=0) - so
+            assert np.linalg.norm(sv) <= GRAD_REL_FRO * np.linalg.norm(so), ("sum dV", b, g)
