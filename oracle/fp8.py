@@ -8,8 +8,7 @@ The pages name FP8 only as a FlashAttention-3 capability ("block quantization"
 of the inputs, "incoherent processing"; "FlashAttention: How IO-Aware Tiling
 and Online Softmax Solved Transformer Memory Bottlenecks", "FlashAttention-3"
 bullets) and give no format, block size or scale rule.  The definition below is
-this library's own, stated with the C ABI's fp8 entry points; incoherent
-processing (a random orthogonal transform of Q and K) is not part of it.
+this library's own, stated with the C ABI's fp8 entry points.
 
 * e4m3 is the 8-bit float with 1 sign bit, 4 exponent bits (bias 7) and 3
   mantissa bits, no infinities, the all-ones exponent-and-mantissa pattern a
@@ -28,6 +27,20 @@ processing (a random orthogonal transform of Q and K) is not part of it.
   column 128 c_b + j, the columns past the sequence up to its next multiple of
   128 zero.
   Scales [Hkv, B].
+* Incoherent processing (optional, Q and K only): before the block
+  quantisation every row x (d channels) of Q and of K becomes
+  R x = (1/sqrt(d)) H_d diag(sigma) x, H_d the Sylvester Hadamard matrix
+  (H[i, c] = (-1)^popcount(i & c)) and sigma in {+1, -1}^d drawn from a seed.
+  R is orthogonal, so (R q) . (R k) = q . k and the forward needs no change,
+  while one large channel is spread over all d (the pages name the technique
+  without defining it; this transform is the library's reading).  sigma_c = -1
+  where bit c % 32 of word c // 32 of one Philox4x32-10 call (counter
+  (0, 2^32 - 1, 2^32 - 1, 0), key (seed mod 2^32, seed // 2^32)) is set.  The
+  arithmetic is float32 in a fixed order, so that the codes are reproducible
+  bit for bit: the signs (exact), then butterflies (a, b) -> (a + b, a - b) on
+  channel pairs (c, c + h), c & h = 0, for h = 1, 2, 4, ..., d/2 in that order,
+  each sum rounded to nearest, then one rounded product with float32(1/sqrt(d)).
+  The amax, scales and codes are taken from the rotated float32 values.
 * The fp8 forward computes, on the dequantised inputs (code value * scale),
   the same O and LSE as the bf16 forward; the kernel rounds the probabilities
   P to e4m3 for the P V product (the row sum uses them unrounded), which
@@ -38,6 +51,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import attention_fwd as _attention_fwd, to_f64
+from .dropout import philox4x32_10
 
 E4M3_MAX = 448.0
 BLOCK = 128
@@ -120,13 +134,48 @@ def _encode_scaled(x32: np.ndarray, s32) -> np.ndarray:
     return e4m3_encode(y.astype(np.float64))
 
 
+# --------------------------------------------------- incoherent processing
+
+def hadamard_signs(d: int, seed: int) -> np.ndarray:
+    """sigma (float32, +-1) of the rotation for d <= 128 channels: -1 where bit
+    c % 32 of word c // 32 of Philox4x32-10 at counter (0, 2^32-1, 2^32-1, 0), key
+    (seed mod 2^32, seed // 2^32), is set."""
+    assert 0 < d <= 128
+    seed = int(seed)
+    words = philox4x32_10(0, 0xFFFFFFFF, 0xFFFFFFFF, 0, seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    bits = np.array([(int(words[c // 32]) >> (c % 32)) & 1 for c in range(d)])
+    return np.where(bits == 1, np.float32(-1.0), np.float32(1.0)).astype(np.float32)
+
+
+def rotate(x32: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """R x = (1/sqrt(d)) H_d diag(sigma) x along the last axis, in float32 with the
+    library's order of operations: sign flips, then the butterfly stages
+    h = 1, 2, ..., d/2 (channel pair (c, c + h) with c & h = 0 becomes
+    (a + b, a - b)), then the product with float32(1/sqrt(d))."""
+    y = (np.asarray(x32, np.float32) * signs).astype(np.float32)   # exact: sign flips
+    d = y.shape[-1]
+    lead = y.shape[:-1]
+    h = 1
+    while h < d:
+        # channel c = (g * 2 + half) * h + t: the pairs are (half 0, half 1) of each g
+        y = y.reshape(*lead, d // (2 * h), 2, h)
+        a, b = y[..., 0, :], y[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(*lead, d)   # float32 adds, rounded
+        h *= 2
+    return (y * np.float32(1.0 / np.sqrt(d))).astype(np.float32)
+
+
 # --------------------------------------------------------------- quantise
 
-def quantize_qk(x, B: int, N: int, cu_seqlens=None, nb=None):
+def quantize_qk(x, B: int, N: int, cu_seqlens=None, nb=None, rotate_seed=None):
     """Block quantisation of Q or K in the library layout ([B, N, H, d] or packed
-    [T, H, d]; bf16 bit patterns or float).  Returns (codes uint8 same shape,
-    scales float32 [H, nb])."""
+    [T, H, d]; bf16 bit patterns or float).  With ``rotate_seed`` the rows are
+    first rotated by :func:`rotate` with ``hadamard_signs(d, rotate_seed)``
+    (incoherent processing).  Returns (codes uint8 same shape, scales float32
+    [H, nb])."""
     xf = to_f64(x).astype(np.float32)      # bf16 values are exact in float32
+    if rotate_seed is not None:
+        xf = rotate(xf, hadamard_signs(xf.shape[-1], rotate_seed))
     dense = cu_seqlens is None
     if dense:
         xf = xf.reshape(B * N, *xf.shape[2:])
