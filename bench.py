@@ -39,8 +39,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 from exact_io_aware_tcgen05_gb300.inputs import attention_inputs  # noqa: E402
-from exact_io_aware_tcgen05_gb300.workloads import (BENCH_DEFAULT, WORKLOADS,  # noqa: E402
-                                                    visible_pairs)
+from exact_io_aware_tcgen05_gb300.workloads import (BENCH_DEFAULT, INCOHERENT_SEED,  # noqa: E402
+                                                    WORKLOADS, visible_pairs)
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16, causal-halved) and % of GB300 dense BF16 peak"
 L2_BYTES = 129 * 1024 * 1024
@@ -299,7 +299,8 @@ def workload_config(w, l2_note):
            "causal": w.causal, "window": w.window, "packed": w.packed,
            "total_tokens": w.total_tokens, "scale": "1/sqrt(d)",
            "inputs": (f"{w.dtype} iid N(0,1), seed 0" if w.dtype != "fp8" else
-                      "bf16 iid N(0,1), seed 0, quantised to e4m3 before the timed region"),
+                      "bf16 iid N(0,1), seed 0, quantised to e4m3 before the timed region"
+                      + (" (Q, K rotated first: incoherent processing)" if w.incoherent else "")),
            "l2": l2_note}
     if w.packed:
         cfg["lengths"] = list(w.lengths)
@@ -385,8 +386,14 @@ def run_ours(args, w):
                     torch.empty((w.Hkv, w.B), dtype=torch.float32, device=dev))
 
         def quantise(q, k, v, ops, st):
-            fa.fa_fp8_quantize_qk(q, ops[0], ops[1], nb, w.B, w.Hq, w.N, w.d, cu, T, st)
-            fa.fa_fp8_quantize_qk(k, ops[2], ops[3], nb, w.B, w.Hkv, w.N, w.d, cu, T, st)
+            if w.incoherent:
+                fa.fa_fp8_quantize_qk_incoherent(q, ops[0], ops[1], nb, w.B, w.Hq, w.N, w.d, cu, T,
+                                                 INCOHERENT_SEED, st)
+                fa.fa_fp8_quantize_qk_incoherent(k, ops[2], ops[3], nb, w.B, w.Hkv, w.N, w.d, cu,
+                                                 T, INCOHERENT_SEED, st)
+            else:
+                fa.fa_fp8_quantize_qk(q, ops[0], ops[1], nb, w.B, w.Hq, w.N, w.d, cu, T, st)
+                fa.fa_fp8_quantize_qk(k, ops[2], ops[3], nb, w.B, w.Hkv, w.N, w.d, cu, T, st)
             fa.fa_fp8_quantize_v(v, ops[4], ops[5], vt_tokens, w.B, w.Hkv, w.N, w.d, cu, T, st)
 
         fp8_ops = [fp8_buffers(), fp8_buffers()]

@@ -23,6 +23,7 @@ __all__ = [
     "FA_BWD_FUSED",
     "fa_bwd_static_workspace", "FA_STATIC_WORKSPACE_BYTES", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
+    "fa_fp8_quantize_qk_incoherent",
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
@@ -94,6 +95,9 @@ def load(path: str | None = None):
     lib.fa_fp8_vt_tokens.restype = _i
     lib.fa_fp8_quantize_qk.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]
     lib.fa_fp8_quantize_qk.restype = _i
+    lib.fa_fp8_quantize_qk_incoherent.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i,
+                                                  _u64, _vp]
+    lib.fa_fp8_quantize_qk_incoherent.restype = _i
     lib.fa_fp8_quantize_v.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]
     lib.fa_fp8_quantize_v.restype = _i
     lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _i, _i,
@@ -317,6 +321,17 @@ def fa_fp8_quantize_qk(x, x8, scales, nb, B, H, N, d, cu_seqlens, total_tokens, 
     return st
 
 
+def fa_fp8_quantize_qk_incoherent(x, x8, scales, nb, B, H, N, d, cu_seqlens, total_tokens, seed,
+                                  stream=None, check: bool = True) -> int:
+    """bf16 Q or K -> rotated (incoherent processing), e4m3 codes and per-block scales."""
+    st = load().fa_fp8_quantize_qk_incoherent(_ptr(x), _ptr(x8), _ptr(scales), int(nb), B, H, N, d,
+                                              _ptr(cu_seqlens), int(total_tokens),
+                                              int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
 def fa_fp8_quantize_v(v, vt8, scales, vt_tokens, B, H, N, d, cu_seqlens, total_tokens, stream=None,
                       check: bool = True) -> int:
     """bf16 V -> transposed e4m3 codes and per-(sequence, head) scales."""
@@ -392,8 +407,11 @@ class Fp8Operands(tuple):
         return self[self._fields.index(name)]
 
 
-def quantize_fp8(q, k, v, *, cu_seqlens=None, max_seqlen=None, stream=None) -> Fp8Operands:
-    """e4m3 operands of the fp8 forward from bf16 CUDA tensors q, k, v (allocates them)."""
+def quantize_fp8(q, k, v, *, cu_seqlens=None, max_seqlen=None, stream=None,
+                 incoherent_seed=None) -> Fp8Operands:
+    """e4m3 operands of the fp8 forward from bf16 CUDA tensors q, k, v (allocates them).
+    With ``incoherent_seed`` Q and K are rotated by the same random orthogonal matrix
+    before the quantisation (incoherent processing; the forward is unchanged)."""
     import torch
     if {q.dtype, k.dtype, v.dtype} != {torch.bfloat16}:
         raise TypeError("quantize_fp8 takes bfloat16 q, k, v")
@@ -409,8 +427,14 @@ def quantize_fp8(q, k, v, *, cu_seqlens=None, max_seqlen=None, stream=None) -> F
     ks = torch.empty((Hkv, nb), dtype=torch.float32, device=dev)
     vs = torch.empty((Hkv, B), dtype=torch.float32, device=dev)
     stream = stream if stream is not None else torch.cuda.current_stream(dev)
-    fa_fp8_quantize_qk(q, q8, qs, nb, B, Hq, N, d, cu_seqlens, T, stream)
-    fa_fp8_quantize_qk(k, k8, ks, nb, B, Hkv, N, d, cu_seqlens, T, stream)
+    if incoherent_seed is None:
+        fa_fp8_quantize_qk(q, q8, qs, nb, B, Hq, N, d, cu_seqlens, T, stream)
+        fa_fp8_quantize_qk(k, k8, ks, nb, B, Hkv, N, d, cu_seqlens, T, stream)
+    else:
+        fa_fp8_quantize_qk_incoherent(q, q8, qs, nb, B, Hq, N, d, cu_seqlens, T, incoherent_seed,
+                                      stream)
+        fa_fp8_quantize_qk_incoherent(k, k8, ks, nb, B, Hkv, N, d, cu_seqlens, T, incoherent_seed,
+                                      stream)
     fa_fp8_quantize_v(v, vt8, vs, vt_tokens, B, Hkv, N, d, cu_seqlens, T, stream)
     return Fp8Operands((q8, qs, k8, ks, vt8, vs, nb, vt_tokens))
 

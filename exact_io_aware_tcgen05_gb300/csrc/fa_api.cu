@@ -641,6 +641,38 @@ fa_status fp8_geometry(int B, int H, int N, int d, const int* cu_seqlens, int to
     return check_common(B, H, H, N, d, 0, 0, cu_seqlens, total_tokens, 1.f, g);
 }
 
+fa_status fp8_quantize_qk(const char* name, bool rotate, unsigned long long seed, const void* x,
+                          void* x8, float* scales, int nb, int B, int H, int N, int d,
+                          const int* cu_seqlens, int total_tokens, cudaStream_t stream) {
+    t_last_error[0] = '\0';
+    if (!x || !x8 || !scales)
+        return fail(FA_ERR_INVALID_ARG, "%s: x, x8 and scales must be non-null", name);
+    if (!aligned16(x) || !aligned16(x8) || !aligned4(scales))
+        return fail(FA_ERR_INVALID_ARG,
+                    "%s: x and x8 must be 16-byte aligned, scales 4-byte aligned", name);
+    Geometry g;
+    fa_status st = fp8_geometry(B, H, N, d, cu_seqlens, total_tokens, name, &g);
+    if (st != FA_OK) return st;
+    if (nb < fp8_blocks(B, N, g.tokens, cu_seqlens != nullptr))
+        return fail(FA_ERR_INVALID_ARG, "%s: nb = %d below fa_fp8_scale_blocks", name, nb);
+    if (g.tokens == 0) return FA_OK;
+    Fp8QuantParams p{};
+    p.seq = g.seq;
+    p.x = x;
+    p.out = x8;
+    p.scales = scales;
+    p.heads = H;
+    p.status = status_word_ptr();
+    if (!p.status) return fail(FA_ERR_CUDA, "fp8 quantisation: cannot resolve the device status word");
+    p.nb = nb;
+    p.rotate = rotate ? 1 : 0;
+    p.seed_lo = static_cast<uint32_t>(seed);
+    p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    const cudaError_t e = launch_fp8_quant_qk(p, d, num_blocks(g, kBlockM, H), stream);
+    if (e != cudaSuccess) return fail(FA_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
+    return FA_OK;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -660,31 +692,16 @@ int fa_fp8_vt_tokens(int B, int N, int total_tokens, int packed) {
 
 fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scales, int nb, int B, int H, int N,
                              int d, const int* cu_seqlens, int total_tokens, cudaStream_t stream) {
-    using namespace fa;
-    t_last_error[0] = '\0';
-    if (!x || !x8 || !scales)
-        return fail(FA_ERR_INVALID_ARG, "fa_fp8_quantize_qk: x, x8 and scales must be non-null");
-    if (!aligned16(x) || !aligned16(x8) || !aligned4(scales))
-        return fail(FA_ERR_INVALID_ARG,
-                    "fa_fp8_quantize_qk: x and x8 must be 16-byte aligned, scales 4-byte aligned");
-    Geometry g;
-    fa_status st = fp8_geometry(B, H, N, d, cu_seqlens, total_tokens, "fa_fp8_quantize_qk", &g);
-    if (st != FA_OK) return st;
-    if (nb < fp8_blocks(B, N, g.tokens, cu_seqlens != nullptr))
-        return fail(FA_ERR_INVALID_ARG, "fa_fp8_quantize_qk: nb = %d below fa_fp8_scale_blocks", nb);
-    if (g.tokens == 0) return FA_OK;
-    Fp8QuantParams p{};
-    p.seq = g.seq;
-    p.x = x;
-    p.out = x8;
-    p.scales = scales;
-    p.heads = H;
-    p.status = status_word_ptr();
-    if (!p.status) return fail(FA_ERR_CUDA, "fp8 quantisation: cannot resolve the device status word");
-    p.nb = nb;
-    const cudaError_t e = launch_fp8_quant_qk(p, d, num_blocks(g, kBlockM, H), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "fa_fp8_quantize_qk launch");
-    return FA_OK;
+    return fa::fp8_quantize_qk("fa_fp8_quantize_qk", false, 0, x, x8, scales, nb, B, H, N, d,
+                           cu_seqlens, total_tokens, stream);
+}
+
+fa_status fa_fp8_quantize_qk_incoherent(const void* x, void* x8, float* scales, int nb, int B,
+                                        int H, int N, int d, const int* cu_seqlens,
+                                        int total_tokens, unsigned long long seed,
+                                        cudaStream_t stream) {
+    return fa::fp8_quantize_qk("fa_fp8_quantize_qk_incoherent", true, seed, x, x8, scales, nb, B, H,
+                           N, d, cu_seqlens, total_tokens, stream);
 }
 
 fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_tokens, int B, int H,

@@ -14,6 +14,16 @@
 //     from column 128 * (blocks of the sequences before b), padded with zero codes
 //     to a multiple of 128 keys, so every tile the attention kernel loads starts
 //     on a 128-byte boundary.  Scales [H, B].
+//   * Incoherent processing (Q and K, optional; the same bullets name it, again
+//     undefined): every row x becomes R x = (1/sqrt d) H_d diag(sigma) x before the
+//     block quantisation, H_d the Sylvester Hadamard matrix and sigma in {+1, -1}^d
+//     (-1 where bit c % 32 of word c / 32 of Philox4x32-10 at counter
+//     (0, 2^32 - 1, 2^32 - 1, 0), keyed by the seed, is set).  R is orthogonal, so
+//     Q K^T is unchanged, while a channel much larger than the rest is spread over
+//     all d.  The float32 arithmetic has one fixed order (sign flips; butterflies
+//     (a, b) -> (a + b, a - b) on channel pairs (c, c + h), c & h = 0, for
+//     h = 1, 2, ..., d/2, each sum rounded to nearest; one rounded product with
+//     float32(1/sqrt d)), so the codes are reproducible bit for bit.
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 #include "fa_seq.cuh"
@@ -111,6 +121,113 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quant_qk_kernel(const __gri
     }
 }
 
+// Q or K with incoherent processing: one CTA per (sequence, 128-token block, head).
+// Thread t takes the four 16-byte units u = q + kQ j (j = 0..3, q = t % kQ,
+// kQ = D / 32) of rows t / kQ + k (256 / kQ): channel c = 8 u + e is element e of
+// unit u.  Butterflies with h < 8 pair elements of one unit; h = 8 m pairs units u
+// and u ^ m, which for m < kQ sit in lanes q and q ^ m of the row's lane group and
+// otherwise in the thread's own units j and j ^ (m / kQ).  Either way the stages run
+// in the order h = 1, 2, ..., D/2, as the definition fixes.
+template <int D>
+__global__ void __launch_bounds__(kQuantThreads) fp8_quant_qk_rot_kernel(const __grid_constant__ Fp8QuantParams p) {
+    constexpr int kQ = D / 32, kRows = kQuantThreads / kQ, kN = kBlockM / kRows;
+    constexpr float kInvSqrtD = D == 64 ? 0x1p-3f : 0x1.6a09e6p-4f;   // float32(1 / sqrt D)
+    static_assert(D == 64 || D == 128, "d in {64, 128}");
+    __shared__ float red[kQuantThreads / 32];
+    int b, h, blk;
+    if (!map_work(p.seq, blockIdx.x, kBlockM, p.heads, false, b, h, blk)) return;
+    int start, len;
+    seq_bounds(p.seq, b, start, len);
+    const int q = threadIdx.x % kQ, r0 = threadIdx.x / kQ;
+    const Philox4 w = philox4x32_10(0u, 0xFFFFFFFFu, 0xFFFFFFFFu, 0u, p.seed_lo, p.seed_hi);
+    const uint16_t* x = static_cast<const uint16_t*>(p.x);
+    float f[kN][4][8];
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+        const int row = blk * kBlockM + r0 + k * kRows;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int u = q + kQ * j;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);   // rows past the sequence: zeros, no codes
+            if (row < len)
+                v = *reinterpret_cast<const uint4*>(x + (static_cast<long long>(start + row) * p.heads + h) * D +
+                                                    8 * u);
+            // sign bits of channels 8u .. 8u + 7: byte u % 4 of word u / 4 (= kQ j / 4, as q < kQ)
+            const int wi = (kQ * j) >> 2;
+            const uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+            const uint32_t sb = word >> (8 * (u & 3));
+            const uint32_t raw[8] = {v.x << 16, v.x & 0xFFFF0000u, v.y << 16, v.y & 0xFFFF0000u,
+                                     v.z << 16, v.z & 0xFFFF0000u, v.w << 16, v.w & 0xFFFF0000u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[k][j][e] = __uint_as_float(raw[e] ^ (((sb >> e) & 1u) << 31));
+#pragma unroll
+            for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if ((e & s) == 0) {
+                        const float a = f[k][j][e], c = f[k][j][e + s];
+                        f[k][j][e] = __fadd_rn(a, c);
+                        f[k][j][e + s] = __fsub_rn(a, c);
+                    }
+        }
+#pragma unroll
+        for (int mu = 1; mu < D / 8; mu <<= 1) {
+            if (mu < kQ) {
+                const bool upper = (q & mu) != 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float o = __shfl_xor_sync(0xffffffffu, f[k][j][e], mu);
+                        f[k][j][e] = upper ? __fsub_rn(o, f[k][j][e]) : __fadd_rn(f[k][j][e], o);
+                    }
+            } else {
+                const int dj = mu / kQ;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((j & dj) == 0)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float a = f[k][j][e], c = f[k][j + dj][e];
+                            f[k][j][e] = __fadd_rn(a, c);
+                            f[k][j + dj][e] = __fsub_rn(a, c);
+                        }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                f[k][j][e] = __fmul_rn(f[k][j][e], kInvSqrtD);
+                m = fmaxf(m, fabsf(f[k][j][e]));
+            }
+    }
+    const float scale = block_scale(cta_max(m, red));
+    const long long sidx = static_cast<long long>(h) * p.nb + seq_block_col(p.seq, b) + blk;
+    if (threadIdx.x == 0 && fa_index_ok(sidx, static_cast<long long>(p.heads) * p.nb, p.status))
+        p.scales[sidx] = scale;
+    uint8_t* out = static_cast<uint8_t*>(p.out);
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+        const int row = blk * kBlockM + r0 + k * kRows;
+        if (row >= len || !fa_index_ok(static_cast<long long>(start + row) * p.heads + h,
+                                       static_cast<long long>(p.seq.total_tokens) * p.heads, p.status))
+            continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float* g = f[k][j];
+            uint2 c;
+            c.x = pack4_e4m3(__fdiv_rn(g[0], scale), __fdiv_rn(g[1], scale), __fdiv_rn(g[2], scale),
+                             __fdiv_rn(g[3], scale));
+            c.y = pack4_e4m3(__fdiv_rn(g[4], scale), __fdiv_rn(g[5], scale), __fdiv_rn(g[6], scale),
+                             __fdiv_rn(g[7], scale));
+            *reinterpret_cast<uint2*>(out + (static_cast<long long>(start + row) * p.heads + h) * D +
+                                      8 * (q + kQ * j)) = c;
+        }
+    }
+}
+
 // V, in three passes over (sequence, 128-token block, head) CTAs and a fourth over
 // (sequence, head): the scale slots start at zero, take the atomic max of the
 // blocks' largest magnitudes (float bits compare like ints for non-negative
@@ -189,7 +306,10 @@ __global__ void __launch_bounds__(128) fp8_v_quant_kernel(const __grid_constant_
 
 cudaError_t launch_fp8_quant_qk(const Fp8QuantParams& p, int d, int grid, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    if (d == 128) fp8_quant_qk_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
+    if (p.rotate) {
+        if (d == 128) fp8_quant_qk_rot_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
+        else fp8_quant_qk_rot_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
+    } else if (d == 128) fp8_quant_qk_kernel<128><<<grid, kQuantThreads, 0, stream>>>(p);
     else fp8_quant_qk_kernel<64><<<grid, kQuantThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }

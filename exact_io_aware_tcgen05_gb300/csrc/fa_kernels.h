@@ -109,6 +109,8 @@ struct Fp8QuantParams {
     int nb;             // Q/K: columns of the scale array
     long long vt_tokens;  // V: columns of V^T
     int* status;          // device status word (the debug build's bounds checks)
+    int rotate;           // Q/K: incoherent processing (sign-randomised Hadamard rotation)
+    uint32_t seed_lo, seed_hi;  // its seed, the Philox key
 };
 
 // Launchers (defined in the kernel translation units).  They only enqueue on

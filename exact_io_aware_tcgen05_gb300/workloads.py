@@ -33,6 +33,7 @@ class Workload:
     dtype: str = "bf16"    # element type of the 16-bit tensors: "bf16" or "f16"; "fp8": the
                            # fp8 forward on e4m3 operands quantised from bf16 inputs
     p_drop: float = 0.0    # dropout probability of the attention probabilities (0: none)
+    incoherent: bool = False   # fp8: rotate Q and K before quantising (incoherent processing)
 
     @property
     def scale(self) -> float:
@@ -124,6 +125,8 @@ WORKLOADS = {
                  p_drop=0.1),
         Workload("fwd_b2_h16_n8192_d128_causal_fp8", 2, 16, 16, 8192, 128, True, 0, False,
                  dtype="fp8"),
+        Workload("fwd_b2_h16_n8192_d128_causal_fp8_incoherent", 2, 16, 16, 8192, 128, True, 0,
+                 False, dtype="fp8", incoherent=True),
         _varlen(128),
         _varlen(64),
         _many_short(),
@@ -132,6 +135,9 @@ WORKLOADS = {
 
 #: dropout seed and offset of the workloads with p_drop > 0
 DROPOUT_SEED, DROPOUT_OFFSET = 0x5EED, 0
+
+#: rotation seed of the fp8 workloads with incoherent processing
+INCOHERENT_SEED = 0x1C0
 
 #: the workload the benchmark times by default: long causal sequences, d = 128, fwd + bwd
 BENCH_DEFAULT = "fwdbwd_b2_h16_n8192_d128_causal"

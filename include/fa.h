@@ -251,6 +251,31 @@ fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scales, int nb, int
 fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scales, int vt_tokens, int B, int H,
                             int N, int d, const int* cu_seqlens, int total_tokens,
                             cudaStream_t stream);
+
+/*
+ * Incoherent processing, the other FP8 technique the same bullets name without
+ * defining it.  This library's reading: a random orthogonal rotation R of the
+ * head dimension applied to Q and to K before the block quantisation.  Because
+ * (R q) . (R k) = q . k, fa_fwd_fp8 needs no change (Q and K must be rotated with
+ * the same seed; V is not rotated), while a channel much larger than the rest is
+ * spread over all d, so the e4m3 rounding errors of the score terms average out.
+ *
+ *   R x = (1/sqrt d) H_d diag(sigma) x on each row x (d channels), H_d the
+ *   Sylvester Hadamard matrix, H[i][c] = (-1)^popcount(i & c); sigma_c = -1 where
+ *   bit c % 32 of word c / 32 of Philox4x32-10 (defined with the dropout entry
+ *   points) at counter (0, 0xFFFFFFFF, 0xFFFFFFFF, 0), key (seed mod 2^32,
+ *   seed / 2^32), is set, else +1.
+ *   The float32 arithmetic has one order, so the codes are reproducible bit for
+ *   bit: the sign flips; for h = 1, 2, 4, ..., d/2 in turn, every channel pair
+ *   (c, c + h) with c & h = 0 becomes (a + b, a - b), each rounded to nearest; one
+ *   product with float32(1/sqrt d), rounded to nearest.  The amax, scale and codes
+ *   of each block are then taken from those float32 values as in
+ *   fa_fp8_quantize_qk (arguments, layouts and errors as there).
+ */
+fa_status fa_fp8_quantize_qk_incoherent(const void* x, void* x8, float* scales, int nb, int B,
+                                        int H, int N, int d, const int* cu_seqlens,
+                                        int total_tokens, unsigned long long seed,
+                                        cudaStream_t stream);
 fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
                      const void* vt8, const float* v_scale, int nb, int vt_tokens, void* o,
                      float* lse, int B, int Hq, int Hkv, int N, int d, int causal, int window,

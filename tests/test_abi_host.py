@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
               "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status",
               "fa_fwd_fp8", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fp8_scale_blocks",
-              "fa_fp8_vt_tokens"):
+              "fa_fp8_vt_tokens", "fa_fp8_quantize_qk_incoherent"):
         assert n in names
 
 
@@ -206,6 +206,14 @@ def test_fp8_sizes_and_argument_checks(lib):
                                  check=False) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fp8_quantize_v(16, 16, 16, 256, 1, 1, 300, 128, None, 0, None,
                                 check=False) == fa.FA_ERR_INVALID_ARG
+    rot = fa.fa_fp8_quantize_qk_incoherent
+    assert rot(16, 16, 16, 2, 1, 1, 300, 128, None, 0, 7, None, check=False) == fa.FA_ERR_INVALID_ARG
+    assert rot(16, 16, 16, 3, 1, 1, 300, 96, None, 0, 7, None, check=False) == fa.FA_ERR_UNSUPPORTED
+    assert rot(None, 16, 16, 3, 1, 1, 300, 128, None, 0, 7, None,
+               check=False) == fa.FA_ERR_INVALID_ARG
+    assert rot(16, 8, 16, 3, 1, 1, 300, 128, None, 0, 7, None,
+               check=False) == fa.FA_ERR_INVALID_ARG                 # misaligned codes
+    assert "fa_fp8_quantize_qk_incoherent" in fa.fa_last_error()
 
 
 def _bwd(fa, **over):

@@ -153,3 +153,81 @@ def test_fp8_rejects_d64_and_short_buffers(fa):
                          0.1, check=False) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_fp8(q8, sc3, q8, sc3, vt, sc, 3, 256, o, lse, 1, 1, 1, 300, 128, 0, 0, None, 0,
                          0.1, check=False) == fa.FA_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------ incoherent processing
+#
+# fa_fp8_quantize_qk_incoherent rotates every row of Q and K by
+# (1/sqrt d) H diag(sigma) before the block quantisation.  The codes and scales must
+# equal the oracle's bit for bit (the same float32 operations in the same order), V
+# is untouched, and the unchanged fp8 forward on the rotated operands is exact
+# attention on their dequantised values within the same e4m3 bound as above.
+
+def _with_outliers(x, amp=16.0, channels=(3, 77)):
+    """The inputs incoherent processing is for: Q and K with a few channels amp times
+    the others (a power of two, so the bf16 values stay exact)."""
+    out = dict(x)
+    for name in ("q", "k"):
+        f = (x[name].astype(np.uint32) << 16).view(np.float32).copy()
+        f[..., [c % f.shape[-1] for c in channels]] *= np.float32(amp)
+        out[name] = (f.view(np.uint32) >> 16).astype(np.uint16)
+    return out
+
+
+# (B, Hq, Hkv, N, causal, window, lengths, seed); d = 128
+ROT_CASES = [
+    (1, 1, 1, 128, False, 0, None, 5),
+    (2, 4, 2, 300, True, 0, None, (3 << 32) | 17),          # both key words of the seed
+    (6, 4, 2, 513, True, 0, (1, 127, 128, 129, 300, 513), 99),
+    (4, 2, 1, 300, True, 0, (300, 0, 17, 0), 12345),          # empty sequences
+]
+
+
+def _rot_ops(fa, fp8, x, N, nb_B, seed):
+    cu = cu_dev(x["cu"])
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    ops = fa.quantize_fp8(q, k, v, cu_seqlens=cu, max_seqlen=N, incoherent_seed=seed)
+    cu_l = None if x["cu"] is None else [int(c) for c in x["cu"]]
+    ref = (*fp8.quantize_qk(x["q"], nb_B, N, cu_l, nb=ops.nb, rotate_seed=seed),
+           *fp8.quantize_qk(x["k"], nb_B, N, cu_l, nb=ops.nb, rotate_seed=seed),
+           *fp8.quantize_v(x["v"], nb_B, N, cu_l, vt_tokens=ops.vt_tokens))
+    return ops, ref, cu, cu_l
+
+
+@pytest.mark.parametrize("case", ROT_CASES, ids=lambda c: _ids(c[:7]) + f"s{c[7]}")
+def test_fp8_incoherent_quantisation_and_forward_match_oracle(fa, oracle_mod, case):
+    from oracle import fp8
+    import torch
+    B, Hq, Hkv, N, causal, window, lengths, seed = case
+    x = _with_outliers(make_case(B, Hq, Hkv, N, D, seed=41, lengths=lengths, with_dout=False))
+    Bn = B if lengths is None else len(lengths)
+    ops, ref, cu, cu_l = _rot_ops(fa, fp8, x, N, Bn, seed)
+    o, lse = fa.attention_forward_fp8(ops, causal=causal, window=window, scale=scale_of(D),
+                                      cu_seqlens=cu, max_seqlen=N)
+    fa.fa_device_status(torch.cuda.current_stream())
+    _check_quantisation(fp8, ops, ref, Bn, N, cu_l)
+    _check_forward(fp8, x, ref, o, lse, Bn, Hq, Hkv, N, causal, window, cu_l)
+
+
+@pytest.mark.parametrize("lengths", [None, (1, 200, 64, 0, 129)], ids=["dense", "packed"])
+def test_fp8_incoherent_quantisation_d64(fa, oracle_mod, lengths):
+    # the quantisers also take d = 64 (three butterfly stages between lanes, not two)
+    from oracle import fp8
+    B, H, N = 3, 2, 300
+    x = _with_outliers(make_case(B, H, H, N, 64, seed=43, lengths=lengths, with_dout=False))
+    Bn = B if lengths is None else len(lengths)
+    ops, ref, _, cu_l = _rot_ops(fa, fp8, x, N if lengths is None else max(lengths), Bn, 0xABCDEF)
+    _check_quantisation(fp8, ops, ref, Bn, N if lengths is None else max(lengths), cu_l)
+
+
+def test_fp8_incoherent_fullsize_sampled_rows(fa, oracle_mod):
+    """B2 H16 N8192 d128 causal with outlier channels: rotated codes and scales checked
+    everywhere, the forward on sampled rows of every head."""
+    from oracle import fp8
+    B, Hq, Hkv, N = 2, 16, 16, 8192
+    x = _with_outliers(make_case(B, Hq, Hkv, N, D, seed=0, with_dout=False))
+    ops, ref, cu, cu_l = _rot_ops(fa, fp8, x, N, B, 2027)
+    o, lse = fa.attention_forward_fp8(ops, causal=True, scale=scale_of(D))
+    _check_quantisation(fp8, ops, ref, B, N, cu_l)
+    rows = np.array([0, 1, 127, 128, 255, 256, 4095, 4096, 8190, 8191])
+    _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, True, 0, cu_l, rows_per_seq=rows)
