@@ -564,7 +564,8 @@ def run_ours(args, w):
         kernels = {}
         for name, times in kern_ms.items():
             mean = sum(times) / len(times)
-            entry = {"ms_mean": mean, "launches": len(times), "share": None}
+            entry = {"ms_mean": mean, "ms_median": statistics.median(times), "launches": len(times),
+                     "share": None}
             if name in KERNEL_FLOPS_PER_PAIR_D:
                 fl = KERNEL_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
                 entry["algorithmic_tflop_per_launch"] = fl / 1e12
