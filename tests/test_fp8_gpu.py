@@ -67,7 +67,8 @@ def _check_quantisation(fp8, ops, ref, B, N, cu):
     assert np.array_equal(vt8[:, :, cols], rvt8[:, :, cols])
 
 
-def _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, causal, window, cu, rows_per_seq=None):
+def _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, causal, window, cu, rows_per_seq=None,
+                   fro_max=4e-2):
     q8, qs, k8, ks, vt8, vs = ref
     qd = fp8.dequantize_qk(q8, qs, B, N, cu)
     kd = fp8.dequantize_qk(k8, ks, B, N, cu)
@@ -99,12 +100,14 @@ def _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, causal, window, cu, rows_
             err2 += float(np.sum((o_got - o_ref) ** 2))
             ref2 += float(np.sum(o_ref ** 2))
     assert worst <= 0.0, f"O outside the e4m3 bound by {worst}"
+    if fro_max is None:
+        return
     # statistical check on N(0,1) inputs.  Rounding a value spread over a binade to e4m3
     # (spacing 2^-3 of the binade's base) leaves an RMS relative error of about
     # 2^-3 ln 2 / sqrt(12) ~ 2.5%; with diffuse attention O and its error both shrink
     # like 1 / sqrt(keys seen), so the relative Frobenius error of O sits near that
     # figure.  4% leaves room for the sampling spread and catches a doubled error.
-    assert np.sqrt(err2 / ref2) <= 4e-2
+    assert np.sqrt(err2 / ref2) <= fro_max
 
 
 @pytest.mark.parametrize("case", CASES, ids=_ids)
@@ -231,3 +234,69 @@ def test_fp8_incoherent_fullsize_sampled_rows(fa, oracle_mod):
     _check_quantisation(fp8, ops, ref, B, N, cu_l)
     rows = np.array([0, 1, 127, 128, 255, 256, 4095, 4096, 8190, 8191])
     _check_forward(fp8, x, ref, o, lse, B, Hq, Hkv, N, True, 0, cu_l, rows_per_seq=rows)
+
+
+# ------------------------------------------------------------ random sweep
+#
+# Seeded random shapes through the fp8 path (d = 128): GQA group 1, 2 or 4; a dense
+# batch or a packed one mixing empty, one- and two-token and longer sequences; causal or
+# not, sometimes with a window; plain block quantisation or incoherent processing with
+# a random 63-bit seed; Q and K with two channels 1x, 4x or 16x the others.  Codes and
+# scales bit for bit, O within the per-element e4m3 bound, LSE within 1e-3 (the
+# Frobenius check above is calibrated for long N(0,1) rows and is left out here).
+
+def draw_fp8_cases(n, seed=2027):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        hkv = int(rng.choice([1, 2]))
+        hq = hkv * int(rng.choice([1, 2, 4]))
+        causal = bool(rng.random() < 0.7)
+        if rng.random() < 0.5:
+            b = int(rng.integers(1, 7))
+            pool = [0, 1, 2] + list(rng.integers(3, 640, size=6))
+            lengths = tuple(int(rng.choice(pool)) for _ in range(b))
+            if max(lengths) == 0:
+                lengths = lengths[:-1] + (int(rng.integers(1, 640)),)
+            n_max = max(lengths)
+        else:
+            b = int(rng.integers(1, 3))
+            lengths = None
+            n_max = int(rng.integers(1, 700))
+        window = int(rng.integers(1, n_max + 64)) if causal and rng.random() < 0.3 else 0
+        rot = int(rng.integers(0, 2 ** 63)) if rng.random() < 0.5 else None
+        amp = float(rng.choice([1.0, 4.0, 16.0]))
+        cases.append((b, hq, hkv, n_max, causal, window, lengths, rot, amp))
+    return cases
+
+
+FP8_CASES = draw_fp8_cases(24)
+
+
+def _fp8_id(c):
+    b, hq, hkv, n, causal, window, lengths, rot, amp = c
+    return (f"B{b}h{hq}x{hkv}n{n}c{int(causal)}w{window}{'p' if lengths else ''}"
+            f"{'r' if rot is not None else ''}a{int(amp)}")
+
+
+@pytest.mark.parametrize("idx", range(len(FP8_CASES)), ids=[_fp8_id(c) for c in FP8_CASES])
+def test_fp8_random_shapes_match_oracle(fa, oracle_mod, idx):
+    from oracle import fp8
+    import torch
+    b, hq, hkv, n, causal, window, lengths, rot, amp = FP8_CASES[idx]
+    x = make_case(b, hq, hkv, n, D, seed=3000 + idx, lengths=lengths, with_dout=False)
+    if amp != 1.0:
+        x = _with_outliers(x, amp=amp)
+    Bn = b if lengths is None else len(lengths)
+    cu = cu_dev(x["cu"])
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    ops = fa.quantize_fp8(q, k, v, cu_seqlens=cu, max_seqlen=n, incoherent_seed=rot)
+    o, lse = fa.attention_forward_fp8(ops, causal=causal, window=window, scale=scale_of(D),
+                                      cu_seqlens=cu, max_seqlen=n)
+    fa.fa_device_status(torch.cuda.current_stream())
+    cu_l = None if x["cu"] is None else [int(c) for c in x["cu"]]
+    ref = (*fp8.quantize_qk(x["q"], Bn, n, cu_l, nb=ops.nb, rotate_seed=rot),
+           *fp8.quantize_qk(x["k"], Bn, n, cu_l, nb=ops.nb, rotate_seed=rot),
+           *fp8.quantize_v(x["v"], Bn, n, cu_l, vt_tokens=ops.vt_tokens))
+    _check_quantisation(fp8, ops, ref, Bn, n, cu_l)
+    _check_forward(fp8, x, ref, o, lse, Bn, hq, hkv, n, causal, window, cu_l, fro_max=None)
