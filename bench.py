@@ -77,6 +77,9 @@ def parse_args():
     ap.add_argument("--bwd-path", choices=["auto", "split", "fused"], default="auto",
                     help="backward path (fa_bwd_set_path): auto, the library's default choice; "
                          "split (dK/dV and dQ kernels); fused (one kernel, causal masks)")
+    ap.add_argument("--dq-heads", type=int, default=0,
+                    help="query heads per dQ CTA of the split backward (fa_bwd_set_dq_heads): "
+                         "0, the library's choice; else a divisor of the GQA group")
     return ap.parse_args()
 
 
@@ -363,6 +366,7 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     fa.fa_bwd_set_path({"auto": fa.FA_BWD_AUTO, "split": fa.FA_BWD_SPLIT,
                         "fused": fa.FA_BWD_FUSED}[args.bwd_path])
+    fa.fa_bwd_set_dq_heads(args.dq_heads)
     fused = bwd and fa.fa_bwd_path(w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, T,
                                    ws_bytes) == fa.FA_BWD_FUSED
     bwd_kernels = 3
@@ -624,6 +628,8 @@ def run_ours(args, w):
             "gpu_launches": world * K * (1 + (bwd_kernels if bwd else 0)), "clocks": clocks,
             "bwd_path": ("fused" if fused else "split") if bwd else None,
         }
+        if bwd and not fused and args.dq_heads:
+            line["dq_heads"] = args.dq_heads
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

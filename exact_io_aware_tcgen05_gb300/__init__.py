@@ -23,7 +23,7 @@ __all__ = [
     "FA_BWD_FUSED",
     "fa_bwd_static_workspace", "FA_STATIC_WORKSPACE_BYTES", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
-    "fa_fp8_quantize_qk_incoherent",
+    "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads",
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
@@ -72,6 +72,8 @@ def load(path: str | None = None):
     lib.fa_bwd_workspace_size_fused.restype = _sz
     lib.fa_bwd_set_path.argtypes = [_i]
     lib.fa_bwd_set_path.restype = None
+    lib.fa_bwd_set_dq_heads.argtypes = [_i]
+    lib.fa_bwd_set_dq_heads.restype = _i
     lib.fa_bwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _sz]
     lib.fa_bwd_path.restype = _i
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -172,6 +174,12 @@ def fa_bwd_workspace_size_fused(B, Hq, Hkv, N, d, total_tokens) -> int:
 def fa_bwd_set_path(path) -> None:
     """Backward path of this thread's fa_bwd calls: FA_BWD_AUTO, FA_BWD_SPLIT or FA_BWD_FUSED."""
     load().fa_bwd_set_path(int(path))
+
+
+def fa_bwd_set_dq_heads(heads: int) -> None:
+    """Query heads per dQ CTA of the split backward on this thread (0: automatic;
+    see include/fa.h)."""
+    _check(load().fa_bwd_set_dq_heads(int(heads)))
 
 
 def fa_bwd_path(B, Hq, Hkv, N, d, causal, window, total_tokens, workspace_bytes) -> int:
@@ -460,10 +468,11 @@ _PATHS = {"auto": FA_BWD_AUTO, "split": FA_BWD_SPLIT, "fused": FA_BWD_FUSED}
 
 def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=None,
                        cu_seqlens=None, max_seqlen=None, stream=None, workspace=None,
-                       dropout=None, path="auto"):
+                       dropout=None, path="auto", dq_heads=0):
     """dQ, dK, dV for the forward above (allocates outputs and, if not given, the workspace
     that ``path`` -- "auto", "split" or "fused" -- needs; the path is this thread's
-    preference for the call)."""
+    preference for the call, and so is ``dq_heads``, the split backward's query heads per
+    dQ CTA, 0 for the library's choice)."""
     import torch
     dtype = _dtype_code(q, k, v, o, dout)
     B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
@@ -477,6 +486,7 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=N
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
     ws_given = workspace.numel() * workspace.element_size()
     fa_bwd_set_path(_PATHS[path])
+    fa_bwd_set_dq_heads(dq_heads)
     try:
         if dropout is not None:
             p_drop, seed, offset = dropout
@@ -488,4 +498,5 @@ def attention_backward(q, k, v, o, lse, dout, *, causal=False, window=0, scale=N
                          window, cu_seqlens, T, scale, workspace, ws_given, stream)
     finally:
         fa_bwd_set_path(FA_BWD_AUTO)
+        fa_bwd_set_dq_heads(0)
     return dq, dk, dv

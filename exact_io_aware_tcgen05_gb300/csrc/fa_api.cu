@@ -26,6 +26,7 @@ thread_local char t_last_error[512] = "";
 thread_local const cudaEvent_t* t_events = nullptr;  // armed by fa_set_launch_events
 thread_local int t_event_count = 0;
 thread_local int t_bwd_path = FA_BWD_AUTO;          // fa_bwd_set_path
+thread_local int t_dq_heads = 0;                     // fa_bwd_set_dq_heads (0: automatic)
 
 // Takes (and disarms) the events armed for this call, with their count.
 void take_events_any(const cudaEvent_t** out, int* count) {
@@ -209,6 +210,26 @@ int num_blocks(const Geometry& g, int rows, int heads) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Query heads per CTA of the split backward's dQ kernel.  The heads of one key/value
+// group read the same K/V tiles, so one CTA can serve several of them in turn and pay
+// its fixed costs (set-up, the first loads) once.  The largest divisor of the group
+// that still leaves at least kDqMinWaves CTAs per SM is taken (1 without GQA).
+constexpr int kDqMinWaves = 4;
+
+int dq_heads_per_cta(const Geometry& g, int Hq, int Hkv) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        sms = 152;
+    const int group = Hq / Hkv;
+    int best = 1;
+    for (int c = 2; c <= group; ++c)
+        if (group % c == 0 &&
+            static_cast<long long>(num_blocks(g, kBlockM, Hq / c)) >= static_cast<long long>(kDqMinWaves) * sms)
+            best = c;
+    return best;
+}
 
 fa_status check_dtype(fa_dtype dtype, const char* who) {
     if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
@@ -398,6 +419,13 @@ void fa_bwd_set_path(int path) {
     t_bwd_path = (path == FA_BWD_SPLIT || path == FA_BWD_FUSED) ? path : FA_BWD_AUTO;
 }
 
+fa_status fa_bwd_set_dq_heads(int heads) {
+    t_last_error[0] = '\0';
+    if (heads < 0) return fa::fail(FA_ERR_INVALID_ARG, "fa_bwd_set_dq_heads: heads = %d < 0", heads);
+    t_dq_heads = heads;
+    return FA_OK;
+}
+
 int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens,
                 size_t workspace_bytes) {
     fa::BwdWorkspace w;
@@ -486,6 +514,9 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
                     wl.full, workspace_bytes);
     const bool fused = t_bwd_path == FA_BWD_FUSED ||
                        (t_bwd_path == FA_BWD_AUTO && can_fuse && prefer_fused(d));
+    if (!fused && t_dq_heads > 0 && (Hq / Hkv) % t_dq_heads != 0)
+        return fail(FA_ERR_INVALID_ARG, "fa_bwd: %d query heads per dQ CTA (fa_bwd_set_dq_heads) do "
+                    "not divide the group of %d", t_dq_heads, Hq / Hkv);
     const int kernels = 3;
     if (ev && ev_count < kernels + 1)
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: fa_set_launch_events needs >= %d events", kernels + 1);
@@ -523,7 +554,8 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.dv = dv;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
-    p.num_work_dq = num_blocks(g, kBlockM, Hq);
+    p.dq_heads = t_dq_heads > 0 ? t_dq_heads : dq_heads_per_cta(g, Hq, Hkv);
+    p.num_work_dq = num_blocks(g, kBlockM, Hq / p.dq_heads);
     p.num_work_dkdv = num_blocks(g, kBlockN, Hkv);
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();

@@ -481,6 +481,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 // items 2j and 2j+1; V_j's slot is released after dP_j, K_j's after dQ_j.  Every
 // signal waits for its waiter's previous phase: S_{j+1} needs S_j read, dP_{j+1}
 // needs dS_j written, so no mbarrier or named barrier runs two phases ahead.
+//
+// A CTA may serve several query heads of one key/value group (p.dq_heads, chosen
+// at launch so that enough CTAs remain): their K/V tiles are the same, so the ring
+// streams them head after head without a break and the CTA's fixed costs (barrier
+// set-up, TMEM allocation, the first loads) are paid once.  Steps are counted over
+// all heads (J = t nk + j for head t), and so are the ring items and the mbarrier
+// phases.  Head t+1's Q and dO go into TMEM once acc_full has shown that every
+// product of head t is complete; its first dQ product overwrites the accumulator only
+// after all element-wise warps have passed head t's epilogue (they signal dS_0 of
+// head t+1 after it).  Only the last head's epilogue stages through the ring's shared
+// memory, which is idle by then; earlier heads store their dQ rows directly.
 
 template <int D, int E, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -495,16 +506,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     } wait_on_exit;
     if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
-    int b, h, qblk;
-    if (!map_work(s, blockIdx.x, kBlockM, s.Hq, true, b, h, qblk)) return;
+    const int hpc = p.dq_heads;   // query heads of this CTA (a divisor of the group)
+    int b, hc, qblk;
+    if (!map_work(s, blockIdx.x, kBlockM, s.Hq / hpc, true, b, hc, qblk)) return;
     int seq_start, len;
     seq_bounds(s, b, seq_start, len);
-    const int g = h / s.group;
+    const int h0 = hc * hpc;      // first query head
+    const int g = h0 / s.group;
     const int q0 = qblk * kBlockM;
     const int q_last = min(q0 + kBlockM - 1, len - 1);
     const int kt_first = max(key_lo(s, q0), 0) / kBlockN;
     const int kt_last = key_hi(s, q_last, len) / kBlockN;
     const int nk = kt_last - kt_first + 1;
+    const int steps = hpc * nk;   // key-tile steps over all heads of the CTA
 
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
     uint8_t* sSlots = smem_raw + C::kHeadBytes;
@@ -518,10 +532,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     if (warp == 0) {
         regs_lower<C::kRegsCtl>();
         if (lane == 0)
-            stream_tiles<D, R>(bars, sSlots, 2 * nk, &p.tm_k, &p.tm_v,
+            stream_tiles<D, R>(bars, sSlots, 2 * steps, &p.tm_k, &p.tm_v,
                                [&](int i, int& head, int& row) {
                                    head = g;
-                                   row = seq_start + (kt_first + i / 2) * kBlockN;
+                                   row = seq_start + (kt_first + (i / 2) % nk) * kBlockN;
                                },
                                abort_flag, p, false);
     } else if (warp == 1) {
@@ -532,42 +546,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         auto slot = [&](int i) { return smem_addr(sSlots + R::index(i) * C::kTileBytes); };
         auto free_slot = [&](int i) { mma_commit(smem_addr(&bars->slot_empty[R::index(i)])); };
         const uint32_t tQ = tmem + C::kColQ, tDO = tmem + C::kColDO, tDP = tmem + C::kColDP;
-        named_bar_sync(kBarOperands, kOperandBar);        // Q and dO are in TMEM
-        if (lane == 0) {
-            auto wait = [&](uint64_t& bar, int parity) {
-                return mbar_wait(smem_addr(&bar), parity, abort_flag, p.timeout_cycles, p.status);
-            };
-            if (wait(bars->slot_full[R::index(0)], 0) && wait(bars->slot_full[R::index(1)], 0)) {}
-            tc_fence_after();
-            issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(0));    // S_0 = Q K_0^T
-            mma_commit(smem_addr(&bars->s_full));
-            issue_ts_k<D, E>(tDP, tDO, slot(1));               // dP_0 = dO V_0^T
-            mma_commit(smem_addr(&bars->dp_full[0]));
-            free_slot(1);
-        }
-        __syncwarp();
-        for (int j = 0; j < nk; ++j) {
-            named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} landed
-            if (lane == 0 && j + 1 < nk) {
-                tc_fence_after();
-                issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * j + 2));   // S_{j+1}
-                mma_commit(smem_addr(&bars->s_full));
-            }
-            __syncwarp();
-            named_bar_sync(kBarDS0, C::kBarCount);          // dS_j written, V_{j+1} landed
+        auto wait = [&](int i) {
+            return mbar_wait(smem_addr(&bars->slot_full[R::index(i)]), R::use(i) & 1, abort_flag,
+                             p.timeout_cycles, p.status);
+        };
+        for (int t = 0; t < hpc; ++t) {
+            const int J0 = t * nk;                          // first step of head t
+            named_bar_sync(kBarOperands, kOperandBar);    // Q and dO of head t are in TMEM
             if (lane == 0) {
+                if (wait(2 * J0) && wait(2 * J0 + 1)) {}
                 tc_fence_after();
-                issue_ts<D, E>(tmem + C::kColAcc, tDP, slot(2 * j), j > 0);   // dQ += dS_j K_j
-                free_slot(2 * j);
-                if (j + 1 < nk) {
-                    issue_ts_k<D, E>(tDP, tDO, slot(2 * j + 3));   // dP_{j+1}, after dQ_j read dS_j
-                    mma_commit(smem_addr(&bars->dp_full[0]));
-                    free_slot(2 * j + 3);
-                }
+                issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * J0));    // S_0 = Q K_0^T
+                mma_commit(smem_addr(&bars->s_full));
+                issue_ts_k<D, E>(tDP, tDO, slot(2 * J0 + 1));           // dP_0 = dO V_0^T
+                mma_commit(smem_addr(&bars->dp_full[0]));
+                free_slot(2 * J0 + 1);
             }
             __syncwarp();
+            for (int j = 0; j < nk; ++j) {
+                const int J = J0 + j;
+                named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} landed
+                if (lane == 0 && j + 1 < nk) {
+                    tc_fence_after();
+                    issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * J + 2));   // S_{j+1}
+                    mma_commit(smem_addr(&bars->s_full));
+                }
+                __syncwarp();
+                named_bar_sync(kBarDS0, C::kBarCount);          // dS_j written, V_{j+1} landed
+                if (lane == 0) {
+                    tc_fence_after();
+                    issue_ts<D, E>(tmem + C::kColAcc, tDP, slot(2 * J), j > 0);   // dQ += dS_j K_j
+                    free_slot(2 * J);
+                    if (j + 1 < nk) {
+                        issue_ts_k<D, E>(tDP, tDO, slot(2 * J + 3));   // dP_{j+1}, after dQ_j read dS_j
+                        mma_commit(smem_addr(&bars->dp_full[0]));
+                        free_slot(2 * J + 3);
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0) mma_commit(smem_addr(&bars->acc_full));   // head t's products done
+            __syncwarp();
         }
-        if (lane == 0) mma_commit(smem_addr(&bars->acc_full));
     } else if (warp == 2) {
         regs_lower<C::kRegsCtl>();
         // ------------------------------------------------------ slot relay
@@ -575,11 +595,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             mbar_wait(smem_addr(&bars->slot_full[R::index(i)]), R::use(i) & 1, abort_flag,
                       p.timeout_cycles, p.status);
         };
-        for (int j = 0; j < nk; ++j) {
-            if (lane == 0 && j + 1 < nk) wait_item(2 * j + 2);   // K_{j+1}
+        for (int J = 0; J < steps; ++J) {
+            const bool more = (J % nk) + 1 < nk;                 // head J / nk has a next tile
+            if (lane == 0 && more) wait_item(2 * J + 2);         // K_{j+1}
             __syncwarp();
             named_bar_sync(kBarP, C::kBarCount);
-            if (lane == 0 && j + 1 < nk) wait_item(2 * j + 3);   // V_{j+1}
+            if (lane == 0 && more) wait_item(2 * J + 3);         // V_{j+1}
             __syncwarp();
             named_bar_sync(kBarDS0, C::kBarCount);
         }
@@ -596,136 +617,144 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
         const uint32_t tDP = tmem + lane_addr + C::kColDP + W * wg;
         const int q = q0 + r;
         const bool valid = q < len;
-        {
-            // Q and dO of row q into TMEM, two elements per 32-bit column as they lie in
-            // memory (the A-operand layout of S and dP): each warpgroup copies kQW of
-            // the D/2 columns; rows past the sequence end are zero
-            constexpr int kQW = D / 2 / C::kEwWG;   // 32 (d = 128) or 8 (d = 64)
-            uint32_t wq[kQW], wd[kQW];
-#pragma unroll
-            for (int i = 0; i < kQW; ++i) wq[i] = wd[i] = 0u;
-            if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
-                                     static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
-                const long long off = (static_cast<long long>(seq_start + q) * s.Hq + h) * D +
-                                      2 * kQW * wg;
-                const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + off);
-                const uint4* gd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
-#pragma unroll
-                for (int i = 0; i < kQW / 4; ++i) {
-                    const uint4 a = __ldg(gq + i), c = __ldg(gd + i);
-                    wq[4 * i] = a.x; wq[4 * i + 1] = a.y; wq[4 * i + 2] = a.z; wq[4 * i + 3] = a.w;
-                    wd[4 * i] = c.x; wd[4 * i + 1] = c.y; wd[4 * i + 2] = c.z; wd[4 * i + 3] = c.w;
-                }
-            }
-            tmem_st_words<kQW>(tmem + lane_addr + C::kColQ + kQW * wg, wq);
-            tmem_st_words<kQW>(tmem + lane_addr + C::kColDO + kQW * wg, wd);
-            tmem_st_wait();
-            tc_fence_before();
-            named_bar_arrive(kBarOperands, kOperandBar);
-        }
-        float lse2 = kPosInf, dlt = 0.f;
-        if (valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
-                                 static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
-            const long long idx = row_stat_index(s, b, h, seq_start, q);
-            lse2 = __ldg(p.lse + idx) * kLog2eF;
-            dlt = __ldg(p.delta + idx);
-        }
         const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
-        const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndlt2 = f2_pack(-dlt, -dlt);
         const int lo_q = key_lo(s, q), hi_q = valid ? key_hi(s, q, len) : -1;
-        // dropout bytes of this query row for the current key tile, 4 keys a word; as in
-        // the dK/dV kernel the next tile's are drawn at the end of each step
-        uint32_t dw[DROP ? W / 4 : 1];
-        auto draw = [&](int j) {
-            dropout_words_rows<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q >> 2,
-                                      ((kt_first + j) * kBlockN + W * wg) >> 2,
-                                      static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
-                                      p.drop.seed_lo, p.drop.seed_hi, lane);
-            keep_masks(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), p.drop.thresh);
-        };
-        if (DROP) draw(0);
-        // `ok`: as in the dK/dV kernel, a warp that gave up keeps taking part in
-        // every named-barrier phase
-        bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            const int kc = (kt_first + j) * kBlockN + W * wg;   // first key of my columns
-            const bool need_mask = !(kc >= lo_q && kc + W - 1 <= hi_q);
-            const int clo = lo_q - kc, chi = hi_q - kc;
-            if (ok) ok = warp_wait(smem_addr(&bars->s_full), j & 1, abort_flag, p.timeout_cycles, p.status);
-            float pv[W];
-            if (ok) {
-                tc_fence_after();
-                tmem_ldw<W>(tS, pv);
-                tc_fence_before();
-            }
-            named_bar_signal(kBarP, C::kBarCount, ok);   // S_j consumed: the next S may be issued
-            if (ok) {
-#pragma unroll
-                for (int i = 0; i < W / 2; ++i) {
-                    const float2 a = f2_unpack(f2_fma(f2_pack(pv[2 * i], pv[2 * i + 1]), sl2x2, nlse2));
-                    pv[2 * i] = ex2_approx(a.x);
-                    pv[2 * i + 1] = ex2_approx(a.y);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int c = 0; c < W; ++c)
-                        if (c < clo || c > chi) pv[c] = 0.f;
-                }
-                ok = warp_wait(smem_addr(&bars->dp_full[0]), j & 1, abort_flag, p.timeout_cycles,
-                               p.status);
-            }
-            if (ok) {
-                tc_fence_after();
-                float dp[W];
-                tmem_ldw<W>(tDP, dp);
-                // with dropout dS = P (r keep dZ - D), as in the dK/dV kernel
-                const uint32_t(&km)[W / 4] = *reinterpret_cast<const uint32_t(*)[W / 4]>(dw);
-                const uint64_t rr = f2_pack(p.drop.rscale, p.drop.rscale);
-#pragma unroll
-                for (int i = 0; i < W / 2; ++i) {
-                    const uint64_t z = DROP ? f2_fma(rr, f2_pack(kept<W>(km, dp, 2 * i), kept<W>(km, dp, 2 * i + 1)), ndlt2)
-                                            : f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2);
-                    const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]), z));
-                    dp[2 * i] = a.x;
-                    dp[2 * i + 1] = a.y;
-                }
-                tmem_st_pk<W, E>(tDP, dp);
-                tmem_st_wait();
-                tc_fence_before();
-            }
-            named_bar_signal(kBarDS0, C::kBarCount, ok);
-            if (DROP && ok && j + 1 < nk) draw(j + 1);
-        }
-        if (ok)
-            ok = warp_wait(smem_addr(&bars->acc_full), 0, abort_flag, p.timeout_cycles, p.status);
         // The warpgroups share the dQ row store: kSC (>= 32) columns each, as far as it
-        // goes.  A whole query tile leaves through shared memory and TMA stores, a tile
-        // cut by the sequence end row by row (see the dK/dV epilogue).
+        // goes.
         constexpr int kSC = (D / C::kEwWG >= 32) ? D / C::kEwWG : 32;
         const bool mine = wg * kSC < D;
         const uint32_t t_acc = tmem + lane_addr + C::kColAcc + kSC * wg;
-        if (named_bar_all(kBarEpi, C::kEwThreads, ok && q0 + kBlockM <= len)) {
-            if (mine) {
+        // `ok`: as in the dK/dV kernel, a warp that gave up keeps taking part in
+        // every named-barrier phase
+        bool ok = true;
+        for (int t = 0; t < hpc; ++t) {
+            const int h = h0 + t;
+            {
+                // Q and dO of row q into TMEM, two elements per 32-bit column as they lie
+                // in memory (the A-operand layout of S and dP): each warpgroup copies kQW
+                // of the D/2 columns; rows past the sequence end are zero.  For t > 0 the
+                // previous head's products are complete (acc_full, below).
+                constexpr int kQW = D / 2 / C::kEwWG;   // 32 (d = 128) or 8 (d = 64)
+                uint32_t wq[kQW], wd[kQW];
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) wq[i] = wd[i] = 0u;
+                if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                         static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
+                    const long long off = (static_cast<long long>(seq_start + q) * s.Hq + h) * D +
+                                          2 * kQW * wg;
+                    const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + off);
+                    const uint4* gd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
+#pragma unroll
+                    for (int i = 0; i < kQW / 4; ++i) {
+                        const uint4 a = __ldg(gq + i), c = __ldg(gd + i);
+                        wq[4 * i] = a.x; wq[4 * i + 1] = a.y; wq[4 * i + 2] = a.z; wq[4 * i + 3] = a.w;
+                        wd[4 * i] = c.x; wd[4 * i + 1] = c.y; wd[4 * i + 2] = c.z; wd[4 * i + 3] = c.w;
+                    }
+                }
+                tmem_st_words<kQW>(tmem + lane_addr + C::kColQ + kQW * wg, wq);
+                tmem_st_words<kQW>(tmem + lane_addr + C::kColDO + kQW * wg, wd);
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar_arrive(kBarOperands, kOperandBar);
+            }
+            float lse2 = kPosInf, dlt = 0.f;
+            if (valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
+                                     static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
+                const long long idx = row_stat_index(s, b, h, seq_start, q);
+                lse2 = __ldg(p.lse + idx) * kLog2eF;
+                dlt = __ldg(p.delta + idx);
+            }
+            const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndlt2 = f2_pack(-dlt, -dlt);
+            // dropout bytes of this query row for the current key tile, 4 keys a word; as
+            // in the dK/dV kernel the next tile's are drawn at the end of each step
+            uint32_t dw[DROP ? W / 4 : 1];
+            auto draw = [&](int j) {
+                dropout_words_rows<W / 4>(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), q >> 2,
+                                          ((kt_first + j) * kBlockN + W * wg) >> 2,
+                                          static_cast<uint32_t>(b * s.Hq + h), p.drop.offset,
+                                          p.drop.seed_lo, p.drop.seed_hi, lane);
+                keep_masks(*reinterpret_cast<uint32_t(*)[W / 4]>(dw), p.drop.thresh);
+            };
+            if (DROP) draw(0);
+            for (int j = 0; j < nk; ++j) {
+                const int J = t * nk + j;                               // step over all heads
+                const int kc = (kt_first + j) * kBlockN + W * wg;      // first key of my columns
+                const bool need_mask = !(kc >= lo_q && kc + W - 1 <= hi_q);
+                const int clo = lo_q - kc, chi = hi_q - kc;
+                if (ok) ok = warp_wait(smem_addr(&bars->s_full), J & 1, abort_flag, p.timeout_cycles, p.status);
+                float pv[W];
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ldw<W>(tS, pv);
+                    tc_fence_before();
+                }
+                named_bar_signal(kBarP, C::kBarCount, ok);   // S_j consumed: the next S may be issued
+                if (ok) {
+#pragma unroll
+                    for (int i = 0; i < W / 2; ++i) {
+                        const float2 a = f2_unpack(f2_fma(f2_pack(pv[2 * i], pv[2 * i + 1]), sl2x2, nlse2));
+                        pv[2 * i] = ex2_approx(a.x);
+                        pv[2 * i + 1] = ex2_approx(a.y);
+                    }
+                    if (need_mask) {
+#pragma unroll
+                        for (int c = 0; c < W; ++c)
+                            if (c < clo || c > chi) pv[c] = 0.f;
+                    }
+                    ok = warp_wait(smem_addr(&bars->dp_full[0]), J & 1, abort_flag, p.timeout_cycles,
+                                   p.status);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    float dp[W];
+                    tmem_ldw<W>(tDP, dp);
+                    // with dropout dS = P (r keep dZ - D), as in the dK/dV kernel
+                    const uint32_t(&km)[W / 4] = *reinterpret_cast<const uint32_t(*)[W / 4]>(dw);
+                    const uint64_t rr = f2_pack(p.drop.rscale, p.drop.rscale);
+#pragma unroll
+                    for (int i = 0; i < W / 2; ++i) {
+                        const uint64_t z = DROP ? f2_fma(rr, f2_pack(kept<W>(km, dp, 2 * i), kept<W>(km, dp, 2 * i + 1)), ndlt2)
+                                                : f2_add(f2_pack(dp[2 * i], dp[2 * i + 1]), ndlt2);
+                        const float2 a = f2_unpack(f2_mul(f2_pack(pv[2 * i], pv[2 * i + 1]), z));
+                        dp[2 * i] = a.x;
+                        dp[2 * i + 1] = a.y;
+                    }
+                    tmem_st_pk<W, E>(tDP, dp);
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+                named_bar_signal(kBarDS0, C::kBarCount, ok);
+                if (DROP && ok && j + 1 < nk) draw(j + 1);
+            }
+            if (ok)
+                ok = warp_wait(smem_addr(&bars->acc_full), t & 1, abort_flag, p.timeout_cycles, p.status);
+            // The last head's whole query tile leaves through shared memory (the ring is
+            // idle once every product is complete) and TMA stores; an earlier head's, while
+            // the ring streams the next head's tiles, and a tile cut by the sequence end,
+            // row by row (see the dK/dV epilogue).
+            if (t == hpc - 1 && named_bar_all(kBarEpi, C::kEwThreads, ok && q0 + kBlockM <= len)) {
+                if (mine) {
+                    tc_fence_after();
+                    stage_acc_row<kSC, E>(t_acc, p.scale, sSlots, C::kChunkBytes, r, kSC * wg);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(kBarEpi, C::kEwThreads);
+                if (warp == 4 && lane == 0) {
+                    if (fa_box_ok(seq_start + q0, kBlockM, s.total_tokens, h, s.Hq, p.status))
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_store_3d(&p.tm_dq, smem_addr(sSlots + c * C::kChunkBytes), c * 64, h,
+                                         seq_start + q0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                }
+            } else if (ok && mine) {
                 tc_fence_after();
-                stage_acc_row<kSC, E>(t_acc, p.scale, sSlots, C::kChunkBytes, r, kSC * wg);
+                const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
+                store_acc_row<kSC, E>(t_acc, p.scale, static_cast<uint16_t*>(p.dq) + row + kSC * wg,
+                                      valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                                           static_cast<long long>(s.total_tokens) * s.Hq,
+                                                           p.status));
             }
-            fence_proxy_async_smem();
-            named_bar_sync(kBarEpi, C::kEwThreads);
-            if (warp == 4 && lane == 0) {
-                if (fa_box_ok(seq_start + q0, kBlockM, s.total_tokens, h, s.Hq, p.status))
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_store_3d(&p.tm_dq, smem_addr(sSlots + c * C::kChunkBytes), c * 64, h,
-                                     seq_start + q0);
-                bulk_commit_group();
-                bulk_wait_read_all();
-            }
-        } else if (ok && mine) {
-            tc_fence_after();
-            const long long row = (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-            store_acc_row<kSC, E>(t_acc, p.scale, static_cast<uint16_t*>(p.dq) + row + kSC * wg,
-                                  valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
-                                                       static_cast<long long>(s.total_tokens) * s.Hq,
-                                                       p.status));
         }
     }
     teardown_bwd_cta<D>(bars, warp);

@@ -93,6 +93,7 @@ struct BwdParams {
     float scale;        // softmax scale
     float scale_log2;
     int num_work_dq, num_work_dkdv;
+    int dq_heads;       // query heads per dQ CTA, a divisor of the GQA group (dq_heads_per_cta)
     int elem;           // element type of every 16-bit tensor (kElemBf16Code / kElemF16Code)
     DropoutParams drop;
     long long timeout_cycles;

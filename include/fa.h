@@ -148,6 +148,19 @@ int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, in
                 size_t workspace_bytes);
 
 /*
+ * Query heads per CTA of the split backward's dQ kernel (per calling thread).  The
+ * query heads of one key/value group read the same K and V tiles, so one CTA may
+ * serve several of them in turn and pay its fixed costs (set-up, the first loads)
+ * once.  0, the default, lets fa_bwd choose: the largest divisor of the group
+ * Hq / Hkv that still leaves at least 4 CTAs per SM (1 without GQA).  A positive
+ * value forces that many; fa_bwd then fails with FA_ERR_INVALID_ARG (before any
+ * launch) if it does not divide the group.  Results do not depend on the choice:
+ * each head's products and their order are the same, so the bits are too.
+ * FA_ERR_INVALID_ARG for heads < 0.
+ */
+fa_status fa_bwd_set_dq_heads(int heads);
+
+/*
  * fa_fwd and fa_bwd for an explicit element type: `dtype` gives the type of
  * every 16-bit tensor of the call (all of them share it; "Flash Attention --
  * Fast Memory-Efficient Exact Attention", "Self-Hosting & Configuration", lists

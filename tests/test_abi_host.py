@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
               "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status",
               "fa_fwd_fp8", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fp8_scale_blocks",
-              "fa_fp8_vt_tokens", "fa_fp8_quantize_qk_incoherent"):
+              "fa_fp8_vt_tokens", "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads"):
         assert n in names
 
 
@@ -151,6 +151,21 @@ def test_backward_path_selection(lib, d):
                        None, check=False)
         assert st == fa.FA_ERR_WORKSPACE and "fused" in fa.fa_last_error()
     finally:
+        fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
+
+
+def test_dq_heads_knob_is_validated_before_any_launch(lib):
+    fa, _ = lib
+    with pytest.raises(fa.FAError):
+        fa.fa_bwd_set_dq_heads(-1)
+    need = fa.fa_bwd_workspace_size(1, 4, 1, 128, 128, 0)
+    try:
+        fa.fa_bwd_set_path(fa.FA_BWD_SPLIT)
+        fa.fa_bwd_set_dq_heads(3)                       # does not divide the group of 4
+        assert _bwd(fa, Hq=4, Hkv=1, ws_bytes=need) == fa.FA_ERR_INVALID_ARG
+        assert "fa_bwd_set_dq_heads" in fa.fa_last_error()
+    finally:
+        fa.fa_bwd_set_dq_heads(0)
         fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
 
 

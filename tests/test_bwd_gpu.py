@@ -36,7 +36,7 @@ SMALL = [
 
 
 # the two backward paths: "fused" (causal masks with the full workspace: one kernel,
-# dQ summed across CTAs in a fixed order) and "split" (the least workspace: a dK/dV
+# dQ summed across CTAs as int32 fixed point) and "split" (the least workspace: a dK/dV
 # kernel and a dQ kernel)
 PATHS = ["fused", "split"]
 
@@ -165,3 +165,45 @@ def test_many_packed_sequences(fa, oracle_mod, d):
         for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
             err = rel_fro(to_f64(g), r)
             assert err <= GRAD_REL_FRO, (path, name, err)
+
+
+# The split backward's dQ CTA may serve several query heads of one key/value group
+# (fa_bwd_set_dq_heads; the library's own choice gives more than one only on large
+# grids).  Every divisor of the group must give the same bits, and they must match the
+# oracle.  (B, Hq, Hkv, N, d, causal, window, lengths, dtype, dropout)
+DQ_HEADS_CASES = [
+    (2, 8, 2, 300, 128, True, 0, None, "bf16", None),
+    (1, 8, 1, 700, 64, True, 200, None, "bf16", None),              # MQA, window
+    (5, 4, 1, 513, 128, False, 0, (1, 127, 0, 129, 513), "f16", None),   # packed, empty seq
+    (3, 6, 2, 260, 64, True, 0, (260, 1, 131), "bf16", None),        # group of 3
+    (2, 4, 2, 384, 128, True, 0, None, "bf16", (0.1, 77, 3)),        # dropout: bits only
+]
+
+
+@pytest.mark.parametrize("case", DQ_HEADS_CASES,
+                         ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}"
+                                       f"{'p' if c[7] else ''}{c[8]}{'drop' if c[9] else ''}")
+def test_dq_heads_per_cta_give_the_same_bits(fa, oracle_mod, case):
+    import torch
+    B, Hq, Hkv, N, d, causal, window, lengths, dtype, drop = case
+    x = make_case(B, Hq, Hkv, N, d, seed=61, lengths=lengths, dtype=dtype)
+    q, k, v, do = (to_dev(x[n]) for n in ("q", "k", "v", "dout"))
+    kw = dict(causal=causal, window=window, scale=scale_of(d), cu_seqlens=cu_dev(x["cu"]),
+              max_seqlen=N)
+    o, lse = fa.attention_forward(q, k, v, dropout=drop, **kw)
+    G = Hq // Hkv
+    first = None
+    for heads in [c for c in range(1, G + 1) if G % c == 0]:
+        got = fa.attention_backward(q, k, v, o, lse, do, path="split", dq_heads=heads,
+                                    dropout=drop, **kw)
+        fa.fa_device_status(torch.cuda.current_stream())
+        if first is None:
+            first = got
+            continue
+        for name, a, b in zip(("dq", "dk", "dv"), got, first):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (heads, name)
+    if drop is None:
+        refs = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=causal,
+                                        window=window, scale=scale_of(d), cu_seqlens=x["cu"])
+        for name, g, r in zip(("dq", "dk", "dv"), first, refs):
+            assert rel_fro(to_f64(g), r) <= GRAD_REL_FRO, name
