@@ -423,19 +423,17 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     // l sums the probabilities before dropout, the product takes the kept
                     // ones (the 1 / keep-probability factor is applied to O in fp32 at the
                     // end, so the 16-bit P carries no extra rounding)
-                    uint32_t dw[DROP ? 8 : 1];
-                    if (DROP) {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const uint4 v = drop_row[(2 * qtr + c) ^ (r & 7)];
-                            dw[(4 * c) % (DROP ? 8 : 1)] = v.x;
-                            dw[(4 * c + 1) % (DROP ? 8 : 1)] = v.y;
-                            dw[(4 * c + 2) % (DROP ? 8 : 1)] = v.z;
-                            dw[(4 * c + 3) % (DROP ? 8 : 1)] = v.w;
-                        }
-                    }
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
+                        // the keep masks of these 16 keys: one 16-byte chunk of the row
+                        uint32_t dw[DROP ? 4 : 1];
+                        if (DROP) {
+                            const uint4 v = drop_row[(2 * qtr + hh) ^ (r & 7)];
+                            dw[0] = v.x;
+                            dw[1 % (DROP ? 4 : 1)] = v.y;
+                            dw[2 % (DROP ? 4 : 1)] = v.z;
+                            dw[3 % (DROP ? 4 : 1)] = v.w;
+                        }
                         uint32_t pk8[8];
 #pragma unroll
                         for (int c8 = 0; c8 < 8; ++c8) {
@@ -445,7 +443,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                             const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
                             rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
                             pk8[c8] = pack2<E>(p0, p1);
-                            if (DROP) pk8[c8] &= keep_mask_pair(dw[(c >> 1) % (DROP ? 8 : 1)], 2 * c);
+                            if (DROP) pk8[c8] &= keep_mask_pair(dw[(c8 >> 1) % (DROP ? 4 : 1)], 2 * c);
                         }
                         tmem_st8(tS + 16 * qtr + 8 * hh, pk8);
                     }
