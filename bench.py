@@ -77,6 +77,9 @@ def parse_args():
     ap.add_argument("--bwd-path", choices=["auto", "split", "fused"], default="auto",
                     help="backward path (fa_bwd_set_path): auto, the library's default choice; "
                          "split (dK/dV and dQ kernels); fused (one kernel, causal masks)")
+    ap.add_argument("--fwd-heads", type=int, default=0,
+                    help="query heads per forward CTA (fa_fwd_set_heads): 0, the library's "
+                         "choice; else a divisor of the GQA group")
     ap.add_argument("--dq-heads", type=int, default=0,
                     help="query heads per dQ CTA of the split backward (fa_bwd_set_dq_heads): "
                          "0, the library's choice; else a divisor of the GQA group")
@@ -367,6 +370,7 @@ def run_ours(args, w):
     fa.fa_bwd_set_path({"auto": fa.FA_BWD_AUTO, "split": fa.FA_BWD_SPLIT,
                         "fused": fa.FA_BWD_FUSED}[args.bwd_path])
     fa.fa_bwd_set_dq_heads(args.dq_heads)
+    fa.fa_fwd_set_heads(args.fwd_heads)
     fused = bwd and fa.fa_bwd_path(w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, T,
                                    ws_bytes) == fa.FA_BWD_FUSED
     bwd_kernels = 3
@@ -630,6 +634,8 @@ def run_ours(args, w):
         }
         if bwd and not fused and args.dq_heads:
             line["dq_heads"] = args.dq_heads
+        if args.fwd_heads:
+            line["fwd_heads"] = args.fwd_heads
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -23,7 +23,7 @@ __all__ = [
     "FA_BWD_FUSED",
     "fa_bwd_static_workspace", "FA_STATIC_WORKSPACE_BYTES", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
-    "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads",
+    "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads", "fa_fwd_set_heads",
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
@@ -74,6 +74,8 @@ def load(path: str | None = None):
     lib.fa_bwd_set_path.restype = None
     lib.fa_bwd_set_dq_heads.argtypes = [_i]
     lib.fa_bwd_set_dq_heads.restype = _i
+    lib.fa_fwd_set_heads.argtypes = [_i]
+    lib.fa_fwd_set_heads.restype = _i
     lib.fa_bwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _sz]
     lib.fa_bwd_path.restype = _i
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -174,6 +176,11 @@ def fa_bwd_workspace_size_fused(B, Hq, Hkv, N, d, total_tokens) -> int:
 def fa_bwd_set_path(path) -> None:
     """Backward path of this thread's fa_bwd calls: FA_BWD_AUTO, FA_BWD_SPLIT or FA_BWD_FUSED."""
     load().fa_bwd_set_path(int(path))
+
+
+def fa_fwd_set_heads(heads: int) -> None:
+    """Query heads per forward CTA on this thread (0: automatic; see include/fa.h)."""
+    _check(load().fa_fwd_set_heads(int(heads)))
 
 
 def fa_bwd_set_dq_heads(heads: int) -> None:
@@ -385,9 +392,10 @@ def _dtype_code(*tensors) -> int:
 
 
 def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens=None,
-                      max_seqlen=None, stream=None, dropout=None):
+                      max_seqlen=None, stream=None, dropout=None, heads=0):
     """O, LSE for CUDA tensors q, k, v (all bf16 or all fp16) in the library's layouts
-    (allocates outputs)."""
+    (allocates outputs).  ``heads``: query heads per CTA for this call (0: the library's
+    choice; see fa_fwd_set_heads)."""
     import torch
     dtype = _dtype_code(q, k, v)
     B, N, Hq, Hkv, d, T = _geometry(q, k, cu_seqlens, max_seqlen)
@@ -396,13 +404,17 @@ def attention_forward(q, k, v, *, causal=False, window=0, scale=None, cu_seqlens
     lse = torch.empty((Hq, T) if cu_seqlens is not None else (B, Hq, N), dtype=torch.float32,
                       device=q.device)
     stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    if dropout is not None:
-        p_drop, seed, offset = dropout
-        fa_fwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, B, Hq, Hkv, N, d, causal,
-                       window, cu_seqlens, T, scale, stream)
-    else:
-        fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens, T,
-                     scale, stream)
+    fa_fwd_set_heads(heads)
+    try:
+        if dropout is not None:
+            p_drop, seed, offset = dropout
+            fa_fwd_dropout(dtype, p_drop, seed, offset, q, k, v, o, lse, B, Hq, Hkv, N, d,
+                           causal, window, cu_seqlens, T, scale, stream)
+        else:
+            fa_fwd_typed(dtype, q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, cu_seqlens,
+                         T, scale, stream)
+    finally:
+        fa_fwd_set_heads(0)
     return o, lse
 
 

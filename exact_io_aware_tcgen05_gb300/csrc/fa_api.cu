@@ -27,6 +27,7 @@ thread_local const cudaEvent_t* t_events = nullptr;  // armed by fa_set_launch_e
 thread_local int t_event_count = 0;
 thread_local int t_bwd_path = FA_BWD_AUTO;          // fa_bwd_set_path
 thread_local int t_dq_heads = 0;                     // fa_bwd_set_dq_heads (0: automatic)
+thread_local int t_fwd_heads = 0;                    // fa_fwd_set_heads (0: automatic)
 
 // Takes (and disarms) the events armed for this call, with their count.
 void take_events_any(const cudaEvent_t** out, int* count) {
@@ -211,13 +212,14 @@ int num_blocks(const Geometry& g, int rows, int heads) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Query heads per CTA of the split backward's dQ kernel.  The heads of one key/value
-// group read the same K/V tiles, so one CTA can serve several of them in turn and pay
-// its fixed costs (set-up, the first loads) once.  The largest divisor of the group
-// that still leaves at least kDqMinWaves CTAs per SM is taken (1 without GQA).
-constexpr int kDqMinWaves = 4;
+// Query heads per CTA of the forward kernel and of the split backward's dQ kernel.
+// The heads of one key/value group read the same K/V tiles, so one CTA can serve
+// several of them in turn and pay its fixed costs (set-up, the first loads) once.
+// The largest divisor of the group that still leaves at least kMinWaves CTAs per SM
+// is taken (1 without GQA).
+constexpr int kMinWaves = 4;
 
-int dq_heads_per_cta(const Geometry& g, int Hq, int Hkv) {
+int heads_per_cta(const Geometry& g, int rows, int Hq, int Hkv) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
@@ -226,7 +228,7 @@ int dq_heads_per_cta(const Geometry& g, int Hq, int Hkv) {
     int best = 1;
     for (int c = 2; c <= group; ++c)
         if (group % c == 0 &&
-            static_cast<long long>(num_blocks(g, kBlockM, Hq / c)) >= static_cast<long long>(kDqMinWaves) * sms)
+            static_cast<long long>(num_blocks(g, rows, Hq / c)) >= static_cast<long long>(kMinWaves) * sms)
             best = c;
     return best;
 }
@@ -370,6 +372,9 @@ fa_status fwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     Geometry g;
     st = check_common(B, Hq, Hkv, N, d, causal, window, cu_seqlens, total_tokens, scale, &g);
     if (st != FA_OK) return st;
+    if (drop.thresh == 0 && t_fwd_heads > 0 && (Hq / Hkv) % t_fwd_heads != 0)
+        return fail(FA_ERR_INVALID_ARG, "fa_fwd: %d query heads per CTA (fa_fwd_set_heads) do not "
+                    "divide the group of %d", t_fwd_heads, Hq / Hkv);
     if (g.tokens == 0) return FA_OK;
 
     FwdParams p;
@@ -383,7 +388,10 @@ fa_status fwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.o = o;
     p.lse = lse;
     p.scale_log2 = scale * kLog2e;
-    p.num_work = num_blocks(g, kFwdQTiles * kBlockM, Hq);
+    // several query heads per CTA for the 16-bit forward without dropout
+    p.heads = drop.thresh != 0 ? 1 : t_fwd_heads > 0 ? t_fwd_heads
+                                                     : heads_per_cta(g, kFwdQTiles * kBlockM, Hq, Hkv);
+    p.num_work = num_blocks(g, kFwdQTiles * kBlockM, Hq / p.heads);
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();
     if (!p.status) return fail(FA_ERR_CUDA, "fa_fwd: cannot resolve the device status word");
@@ -417,6 +425,13 @@ size_t fa_bwd_workspace_size_fused(int B, int Hq, int Hkv, int N, int d, int tot
 
 void fa_bwd_set_path(int path) {
     t_bwd_path = (path == FA_BWD_SPLIT || path == FA_BWD_FUSED) ? path : FA_BWD_AUTO;
+}
+
+fa_status fa_fwd_set_heads(int heads) {
+    t_last_error[0] = '\0';
+    if (heads < 0) return fa::fail(FA_ERR_INVALID_ARG, "fa_fwd_set_heads: heads = %d < 0", heads);
+    t_fwd_heads = heads;
+    return FA_OK;
 }
 
 fa_status fa_bwd_set_dq_heads(int heads) {
@@ -554,7 +569,7 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.dv = dv;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
-    p.dq_heads = t_dq_heads > 0 ? t_dq_heads : dq_heads_per_cta(g, Hq, Hkv);
+    p.dq_heads = t_dq_heads > 0 ? t_dq_heads : heads_per_cta(g, kBlockM, Hq, Hkv);
     p.num_work_dq = num_blocks(g, kBlockM, Hq / p.dq_heads);
     p.num_work_dkdv = num_blocks(g, kBlockN, Hkv);
     p.timeout_cycles = g_wait_limit.load();
@@ -810,6 +825,7 @@ fa_status fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const
     p.o = o;
     p.lse = lse;
     p.scale_log2 = scale * kLog2e;
+    p.heads = 1;
     p.num_work = num_blocks(g, kFwdQTiles * kBlockM, Hq);
     p.timeout_cycles = g_wait_limit.load();
     p.status = status_word_ptr();

@@ -94,6 +94,7 @@ constexpr int kFwdBarEpi = 3;   // + t: softmax warpgroup t among itself, the ep
 
 struct FwdBars {
     uint64_t q_full;
+    uint64_t q_empty;   // heads loop: the head's last Q K^T products are complete
     uint64_t s_full[kFwdQTiles];
     uint64_t o_full;
     uint64_t kv_full[8];
@@ -107,8 +108,16 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// E: element type of q, k, v and o (kElemBf16 or kElemF16); DROP: dropout of P
-template <int D, int E, bool DROP>
+// E: element type of q, k, v and o (kElemBf16 or kElemF16); DROP: dropout of P; HL: the
+// CTA serves p.heads query heads of one key/value group in turn (16-bit, no dropout).
+// Their K/V tiles are the same, so the ring streams them head after head and the CTA's
+// fixed costs (set-up, the first loads, the exit) are paid once.  Ring items, S and O
+// phases are counted over all the CTA's heads.  Head t+1's Q tiles load once q_empty
+// shows head t's last Q K^T complete; its first P V overwrites O only after the
+// softmax warps have left head t's epilogue (they hand P of head t+1 over after it).
+// Only the last head's O tiles leave through the ring's shared memory; the earlier
+// ones are stored row by row, because the ring is then streaming the next head's tiles.
+template <int D, int E, bool DROP, bool HL>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, E>;
     constexpr bool F8 = C::kF8;
@@ -118,12 +127,16 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     // fp8: V^T tiles, K-major like K; 16-bit: V tiles read MN-major
     constexpr uint32_t kIdescPV = idesc_f32acc(kBlockM, D, false, !F8, E);
     const SeqInfo& s = p.seq;
+    static_assert(!HL || (!F8 && !DROP), "the heads loop serves the 16-bit forward without dropout");
+    const int hpc = HL ? p.heads : 1;   // query heads of this CTA (a divisor of the group)
 
-    int b, h, qblk;
-    if (!map_work(s, blockIdx.x, kFwdQTiles * kBlockM, s.Hq, true, b, h, qblk, p.head_chunk)) return;
+    int b, hc, qblk;
+    if (!map_work(s, blockIdx.x, kFwdQTiles * kBlockM, s.Hq / hpc, true, b, hc, qblk, p.head_chunk))
+        return;
     int seq_start, len;
     seq_bounds(s, b, seq_start, len);
-    const int g = h / s.group;
+    const int h0 = hc * hpc;            // first query head
+    const int g = h0 / s.group;
     const int q0 = qblk * kFwdQTiles * kBlockM;  // first query row of the CTA (in-sequence)
     const int q_last = min(q0 + kFwdQTiles * kBlockM - 1, len - 1);
     const int kv_first = max(key_lo(s, q0), 0) / kBlockN;
@@ -144,6 +157,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     if (threadIdx.x == 0) {
         bars->abort = 0;
         mbar_init(smem_addr(&bars->q_full), 1);
+        mbar_init(smem_addr(&bars->q_empty), 1);
         mbar_init(smem_addr(&bars->o_full), 1);
         for (int t = 0; t < kFwdQTiles; ++t) {
             mbar_init(smem_addr(&bars->s_full[t]), 1);
@@ -172,36 +186,46 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             tma_prefetch_desc(&p.tm_v);
             const uint64_t keep = make_l2_policy_evict_last();
             const uint32_t qbar = smem_addr(&bars->q_full);
-            mbar_arrive_expect_tx(qbar, kFwdQTiles * C::kTileBytes);
-            for (int t = 0; t < kFwdQTiles; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem_addr(sQ + t * C::kTileBytes + c * C::kChunkBytes), &p.tm_q,
-                                qbar, c * C::kChunkElems, h, seq_start + q0 + t * kBlockM);
             // fp8: V^T rows are the d dimension, columns this sequence's keys from
             // its padded start (a multiple of 128, so the TMA x coordinate is aligned)
             const int vt_col = F8 ? 128 * seq_block_col(s, b) : 0;
-            int issued = 0;
-            for (int i = 0; i < 2 * nkv; ++i) {
-                const int st = i % C::kStages, use = i / C::kStages;
-                if (use > 0 && !mbar_wait(smem_addr(&bars->kv_empty[st]), (use - 1) & 1,
-                                          abort_flag, p.timeout_cycles, p.status))
+            int issued = 0, q_issued = 0;   // ring items (over all heads), Q loads
+            bool stop = false;
+            for (int hd = 0; hd < hpc && !stop; ++hd) {
+                if (hd > 0 && !mbar_wait(smem_addr(&bars->q_empty), (hd - 1) & 1, abort_flag,
+                                         p.timeout_cycles, p.status))
                     break;
-                const uint32_t fb = smem_addr(&bars->kv_full[st]);
-                mbar_arrive_expect_tx(fb, C::kTileBytes);
-                const CUtensorMap* map = (i & 1) ? &p.tm_v : &p.tm_k;
-                const int row = seq_start + (kv_first + i / 2) * kBlockN;
-                if (F8 && (i & 1))
-                    tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes), map, fb,
-                                     vt_col + (kv_first + i / 2) * kBlockN, 0, g, keep);
-                else
+                mbar_arrive_expect_tx(qbar, kFwdQTiles * C::kTileBytes);
+                for (int t = 0; t < kFwdQTiles; ++t)
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes),
-                                         map, fb, c * C::kChunkElems, g, row, keep);
-                issued = i + 1;
+                        tma_load_3d(smem_addr(sQ + t * C::kTileBytes + c * C::kChunkBytes), &p.tm_q,
+                                    qbar, c * C::kChunkElems, h0 + hd, seq_start + q0 + t * kBlockM);
+                q_issued = hd + 1;
+                for (int i = 0; i < 2 * nkv; ++i) {
+                    const int ig = hd * 2 * nkv + i;
+                    const int st = ig % C::kStages, use = ig / C::kStages;
+                    if (use > 0 && !mbar_wait(smem_addr(&bars->kv_empty[st]), (use - 1) & 1,
+                                              abort_flag, p.timeout_cycles, p.status)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&bars->kv_full[st]);
+                    mbar_arrive_expect_tx(fb, C::kTileBytes);
+                    const CUtensorMap* map = (i & 1) ? &p.tm_v : &p.tm_k;
+                    const int row = seq_start + (kv_first + i / 2) * kBlockN;
+                    if (F8 && (i & 1))
+                        tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes), map, fb,
+                                         vt_col + (kv_first + i / 2) * kBlockN, 0, g, keep);
+                    else
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes),
+                                             map, fb, c * C::kChunkElems, g, row, keep);
+                    issued = ig + 1;
+                }
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA exits
-                mbar_wait_drain(qbar, 0, kDrainCycles);
+                if (q_issued > 0) mbar_wait_drain(qbar, (q_issued - 1) & 1, kDrainCycles);
                 for (int i = max(0, issued - C::kStages); i < issued; ++i)
                     mbar_wait_drain(smem_addr(&bars->kv_full[i % C::kStages]),
                                     (i / C::kStages) & 1, kDrainCycles);
@@ -250,47 +274,60 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 }
             }
         };
-        if (lane == 0) {
-            if (mbar_wait(smem_addr(&bars->q_full), 0, abort_flag, p.timeout_cycles, p.status))
-                mbar_wait(smem_addr(&bars->kv_full[0]), 0, abort_flag, p.timeout_cycles, p.status);
-            tc_fence_after();
-            for (int t = 0; t < kFwdQTiles; ++t) {
-                issue_qk(t, kv_stage(0));
-                mma_commit(smem_addr(&bars->s_full[t]));
-            }
-            mma_commit(smem_addr(&bars->kv_empty[kv_stage(0)]));
-        }
-        __syncwarp();
-        for (int j = 0; j < nkv; ++j) {
-            const int iv = 2 * j + 1, ik = 2 * j + 2;
-            for (int t = 0; t < kFwdQTiles; ++t) {
-                named_bar_sync(kFwdBarP + t, kFwdBarCount);   // P_t(j) written (V_j, K_{j+1} landed)
-                if (lane == 0) {
-                    tc_fence_after();
-                    issue_pv(t, kv_stage(iv), j > 0);
-                    if (j + 1 < nkv) {
-                        issue_qk(t, kv_stage(ik));
-                        mma_commit(smem_addr(&bars->s_full[t]));
-                        if (t == kFwdQTiles - 1) mma_commit(smem_addr(&bars->kv_empty[kv_stage(ik)]));
-                    }
+        for (int hd = 0; hd < hpc; ++hd) {
+            const int base = hd * 2 * nkv;   // ring item of this head's K_0
+            if (lane == 0) {
+                if (mbar_wait(smem_addr(&bars->q_full), hd & 1, abort_flag, p.timeout_cycles, p.status))
+                    mbar_wait(smem_addr(&bars->kv_full[kv_stage(base)]), (base / C::kStages) & 1,
+                              abort_flag, p.timeout_cycles, p.status);
+                tc_fence_after();
+                for (int t = 0; t < kFwdQTiles; ++t) {
+                    issue_qk(t, kv_stage(base));
+                    mma_commit(smem_addr(&bars->s_full[t]));
                 }
-                __syncwarp();
+                mma_commit(smem_addr(&bars->kv_empty[kv_stage(base)]));
+                if (HL && nkv == 1) mma_commit(smem_addr(&bars->q_empty));   // Q is free
             }
-            if (lane == 0) mma_commit(smem_addr(&bars->kv_empty[kv_stage(iv)]));
+            __syncwarp();
+            for (int j = 0; j < nkv; ++j) {
+                const int iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+                for (int t = 0; t < kFwdQTiles; ++t) {
+                    named_bar_sync(kFwdBarP + t, kFwdBarCount);   // P_t(j) written (V_j, K_{j+1} landed)
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_pv(t, kv_stage(iv), j > 0);
+                        if (j + 1 < nkv) {
+                            issue_qk(t, kv_stage(ik));
+                            mma_commit(smem_addr(&bars->s_full[t]));
+                            if (t == kFwdQTiles - 1) {
+                                mma_commit(smem_addr(&bars->kv_empty[kv_stage(ik)]));
+                                if (HL && j + 2 == nkv) mma_commit(smem_addr(&bars->q_empty));
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) mma_commit(smem_addr(&bars->kv_empty[kv_stage(iv)]));
+            }
+            // o_full: head hd's products are complete (and, for the last head, tells the
+            // teardown that no MMA is still running)
+            if (lane == 0) mma_commit(smem_addr(&bars->o_full));
         }
-        // o_full also tells the teardown that no MMA is still running.
-        if (lane == 0) mma_commit(smem_addr(&bars->o_full));
     } else if (warp == 2) {
         // ------------------------------------------------------ K/V relay
         regs_lower<kFwdRegsCtl>();
-        for (int j = 0; j < nkv; ++j) {
-            if (lane == 0) {
-                for (int i = 2 * j + 1; i <= 2 * j + 2 && i < 2 * nkv; ++i)
-                    mbar_wait(smem_addr(&bars->kv_full[i % C::kStages]), (i / C::kStages) & 1,
-                              abort_flag, p.timeout_cycles, p.status);
+        for (int hd = 0; hd < hpc; ++hd) {
+            const int base = hd * 2 * nkv;
+            for (int j = 0; j < nkv; ++j) {
+                if (lane == 0) {
+                    for (int i = 2 * j + 1; i <= 2 * j + 2 && i < 2 * nkv; ++i)
+                        mbar_wait(smem_addr(&bars->kv_full[(base + i) % C::kStages]),
+                                  ((base + i) / C::kStages) & 1, abort_flag, p.timeout_cycles,
+                                  p.status);
+                }
+                __syncwarp();
+                for (int t = 0; t < kFwdQTiles; ++t) named_bar_sync(kFwdBarP + t, kFwdBarCount);
             }
-            __syncwarp();
-            for (int t = 0; t < kFwdQTiles; ++t) named_bar_sync(kFwdBarP + t, kFwdBarCount);
         }
     } else if (warp == 3) {
         regs_lower<kFwdRegsCtl>();   // idle; its warpgroup gives registers away
@@ -314,12 +351,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         const int blk_col = F8 ? seq_block_col(s, b) : 0;
         // (a tile wholly past the sequence end reads its last block's scale; its rows
         // are never stored)
-        const long long sq_idx = static_cast<long long>(h) * p.nb + blk_col +
+        const long long sq_idx = static_cast<long long>(h0) * p.nb + blk_col +
                                  min(q0 / kBlockM + t, ceil_div(len, kBlockM) - 1);
         const float sq = (F8 && fa_index_ok(sq_idx, static_cast<long long>(s.Hq) * p.nb, p.status))
                              ? __ldg(p.q_scale + sq_idx) : 1.f;
         const float* ks_row = F8 ? p.k_scale + static_cast<long long>(g) * p.nb + blk_col : nullptr;
-        const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h);   // dropout counter word
+        const uint32_t hs = static_cast<uint32_t>(b * s.Hq + h0);   // dropout counter word
 
         // Dropout: the Philox words of a key block do not depend on the scores, so each
         // row draws those of its next block right after handing P over, while the tensor
@@ -339,200 +376,204 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         };
         if (DROP) draw_block(0);
 
-        float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
-        float l = 0.f;
         // `ok` turns false (warp-uniformly: the TMEM accesses are warp-collective)
         // when a wait gives up; the warp then skips the work but keeps taking part
         // in every named-barrier phase, blocking instead of arriving.
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (ok)
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full[t]), j & 1, abort_flag,
-                                                       p.timeout_cycles, p.status));
-            if (ok) {
-                tc_fence_after();
-                uint32_t sr[kBlockN];
+        for (int hd = 0; hd < hpc; ++hd) {
+            const int h = h0 + hd;
+            float m_ref = kNegInf;  // exponent reference (log2 units), shared by O and l
+            float l = 0.f;
+            for (int j = 0; j < nkv; ++j) {
+                if (ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->s_full[t]), (hd * nkv + j) & 1,
+                                                           abort_flag, p.timeout_cycles, p.status));
+                if (ok) {
+                    tc_fence_after();
+                    uint32_t sr[kBlockN];
 #pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c)
-                    tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-                tmem_ld_wait();
-                reg_fence(sr);
-                float sv[kBlockN];
+                    for (int c = 0; c < kBlockN / 32; ++c)
+                        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                    tmem_ld_wait();
+                    reg_fence(sr);
+                    float sv[kBlockN];
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) sv[c] = __uint_as_float(sr[c]);
-                const int kb = (kv_first + j) * kBlockN;
-                if (!(kb >= full_lo && kb + kBlockN - 1 <= full_hi)) {
-                    const int clo = lo_q - kb, chi = hi_q - kb;
+                    for (int c = 0; c < kBlockN; ++c) sv[c] = __uint_as_float(sr[c]);
+                    const int kb = (kv_first + j) * kBlockN;
+                    if (!(kb >= full_lo && kb + kBlockN - 1 <= full_hi)) {
+                        const int clo = lo_q - kb, chi = hi_q - kb;
 #pragma unroll
-                    for (int c = 0; c < kBlockN; ++c)
-                        if (c < clo || c > chi) sv[c] = kNegInf;
-                }
-                // row max in 8 independent chains (short latency) of three-input maxima
-                // (half the instructions of two-input ones)
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-                for (int c = 8; c + 16 <= kBlockN; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kBlockN - 8 + i]);
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
-                const float sl2b =
-                    (F8 && fa_index_ok(static_cast<long long>(g) * p.nb + blk_col + kv_first + j,
-                                       static_cast<long long>(s.Hkv) * p.nb, p.status))
-                        ? sl2 * sq * __ldg(ks_row + kv_first + j) : sl2;
-                const float m_blk = mx * sl2b;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (m_blk > m_ref + kRescaleThreshold) {
-                    alpha = ex2_approx(m_ref - m_blk);  // 0 on the first visible block
-                    rescale = (j > 0);
-                    m_ref = m_blk;
-                    l *= alpha;
-                }
-                const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
-                const uint64_t sl2x2 = f2_pack(sl2b, sl2b), nref2 = f2_pack(neg_ref, neg_ref);
-                uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-                // P (16-bit pairs) goes to the first 64 columns of S_t in two halves; every
-                // S value is already in registers, so the overwrite is safe.  fp8: P as
-                // e4m3, four keys per column, the first 32 columns.
-#pragma unroll
-                for (int half = 0; half < 2 && F8; ++half) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int kc = 64 * half + 4 * c;
-                        const float2 a = f2_unpack(f2_fma(f2_pack(sv[kc], sv[kc + 1]), sl2x2, nref2));
-                        const float2 e = f2_unpack(f2_fma(f2_pack(sv[kc + 2], sv[kc + 3]), sl2x2, nref2));
-                        const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-                        const float p2 = ex2_approx(e.x), p3 = ex2_approx(e.y);
-                        rs2[c & 1] = f2_add(rs2[c & 1], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
-                        pk[c] = pack4_e4m3(p0, p1, p2, p3);
+                        for (int c = 0; c < kBlockN; ++c)
+                            if (c < clo || c > chi) sv[c] = kNegInf;
                     }
-                    tmem_st16(tS + 16 * half, pk);
-                }
+                    // row max in 8 independent chains (short latency) of three-input maxima
+                    // (half the instructions of two-input ones)
+                    float mx8[8];
 #pragma unroll
-                // (an eighth of the row per TMEM store, 16 keys in 8 packed words, and two
-                // row-sum chains keep the live registers of the pass within the 168 the
-                // compiler allocates to every warp: no spills in the 16-bit instances)
-                for (int qtr = 0; qtr < 4 && !F8; ++qtr) {
-                    // dropout: the keep masks of keys kb + 32 qtr .. + 31 of this row;
-                    // l sums the probabilities before dropout, the product takes the kept
-                    // ones (the 1 / keep-probability factor is applied to O in fp32 at the
-                    // end, so the 16-bit P carries no extra rounding)
+                    for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        // the keep masks of these 16 keys: one 16-byte chunk of the row
-                        uint32_t dw[DROP ? 4 : 1];
-                        if (DROP) {
-                            const uint4 v = drop_row[(2 * qtr + hh) ^ (r & 7)];
-                            dw[0] = v.x;
-                            dw[1 % (DROP ? 4 : 1)] = v.y;
-                            dw[2 % (DROP ? 4 : 1)] = v.z;
-                            dw[3 % (DROP ? 4 : 1)] = v.w;
-                        }
-                        uint32_t pk8[8];
+                    for (int c = 8; c + 16 <= kBlockN; c += 16)
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            const int c = 8 * hh + c8;
-                            const int k = 32 * qtr + 2 * c;
-                            const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kBlockN - 8 + i]);
+                    const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                           fmaxf(mx8[6], mx8[7]));
+                    const float sl2b =
+                        (F8 && fa_index_ok(static_cast<long long>(g) * p.nb + blk_col + kv_first + j,
+                                           static_cast<long long>(s.Hkv) * p.nb, p.status))
+                            ? sl2 * sq * __ldg(ks_row + kv_first + j) : sl2;
+                    const float m_blk = mx * sl2b;
+                    float alpha = 1.f;
+                    bool rescale = false;
+                    if (m_blk > m_ref + kRescaleThreshold) {
+                        alpha = ex2_approx(m_ref - m_blk);  // 0 on the first visible block
+                        rescale = (j > 0);
+                        m_ref = m_blk;
+                        l *= alpha;
+                    }
+                    const float neg_ref = (m_ref == kNegInf) ? 0.f : -m_ref;
+                    const uint64_t sl2x2 = f2_pack(sl2b, sl2b), nref2 = f2_pack(neg_ref, neg_ref);
+                    uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+                    // P (16-bit pairs) goes to the first 64 columns of S_t in two halves; every
+                    // S value is already in registers, so the overwrite is safe.  fp8: P as
+                    // e4m3, four keys per column, the first 32 columns.
+#pragma unroll
+                    for (int half = 0; half < 2 && F8; ++half) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int kc = 64 * half + 4 * c;
+                            const float2 a = f2_unpack(f2_fma(f2_pack(sv[kc], sv[kc + 1]), sl2x2, nref2));
+                            const float2 e = f2_unpack(f2_fma(f2_pack(sv[kc + 2], sv[kc + 3]), sl2x2, nref2));
                             const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-                            rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
-                            pk8[c8] = pack2<E>(p0, p1);
-                            if (DROP) pk8[c8] &= keep_mask_pair(dw[(c8 >> 1) % (DROP ? 4 : 1)], 2 * c);
+                            const float p2 = ex2_approx(e.x), p3 = ex2_approx(e.y);
+                            rs2[c & 1] = f2_add(rs2[c & 1], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+                            pk[c] = pack4_e4m3(p0, p1, p2, p3);
                         }
-                        tmem_st8(tS + 16 * qtr + 8 * hh, pk8);
+                        tmem_st16(tS + 16 * half, pk);
+                    }
+#pragma unroll
+                    // (an eighth of the row per TMEM store, 16 keys in 8 packed words, and two
+                    // row-sum chains keep the live registers of the pass within the 168 the
+                    // compiler allocates to every warp: no spills in the 16-bit instances)
+                    for (int qtr = 0; qtr < 4 && !F8; ++qtr) {
+                        // dropout: the keep masks of keys kb + 32 qtr .. + 31 of this row;
+                        // l sums the probabilities before dropout, the product takes the kept
+                        // ones (the 1 / keep-probability factor is applied to O in fp32 at the
+                        // end, so the 16-bit P carries no extra rounding)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            // the keep masks of these 16 keys: one 16-byte chunk of the row
+                            uint32_t dw[DROP ? 4 : 1];
+                            if (DROP) {
+                                const uint4 v = drop_row[(2 * qtr + hh) ^ (r & 7)];
+                                dw[0] = v.x;
+                                dw[1 % (DROP ? 4 : 1)] = v.y;
+                                dw[2 % (DROP ? 4 : 1)] = v.z;
+                                dw[3 % (DROP ? 4 : 1)] = v.w;
+                            }
+                            uint32_t pk8[8];
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const int c = 8 * hh + c8;
+                                const int k = 32 * qtr + 2 * c;
+                                const float2 a = f2_unpack(f2_fma(f2_pack(sv[k], sv[k + 1]), sl2x2, nref2));
+                                const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                                rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
+                                pk8[c8] = pack2<E>(p0, p1);
+                                if (DROP) pk8[c8] &= keep_mask_pair(dw[(c8 >> 1) % (DROP ? 4 : 1)], 2 * c);
+                            }
+                            tmem_st8(tS + 16 * qtr + 8 * hh, pk8);
+                        }
+                    }
+                    const float2 rsum = f2_unpack(f2_add(rs2[0], rs2[1]));
+                    l += rsum.x + rsum.y;
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
+                        // signalled; scale it in place before the next product accumulates.
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t orow[32];
+                            tmem_ld32(tO + c * 32, orow);
+                            tmem_ld_wait();
+                            reg_fence(orow);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                            tmem_st32(tO + c * 32, orow);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+                named_bar_signal(kFwdBarP + t, kFwdBarCount, ok);
+                if (DROP && ok && j + 1 < nkv) draw_block(j + 1);
+            }
+            // ------------------------------------------------------------ epilogue
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->o_full), hd & 1, abort_flag,
+                                                       p.timeout_cycles, p.status));
+            // A tile of 128 query rows inside the sequence leaves through shared memory
+            // (its K/V stage, idle by now) and TMA stores, coalesced and asynchronous; a
+            // tile cut by the sequence end, and any head but the CTA's last (the ring is
+            // streaming the next head's tiles), row by row.  The choice is made uniform over
+            // the warpgroup.
+            const bool valid = q < len;
+            // fp8: O carries the scale of V (per sequence and key/value head)
+            const float vs = (F8 && fa_index_ok(static_cast<long long>(g) * s.B + b,
+                                                static_cast<long long>(s.Hkv) * s.B, p.status))
+                                 ? __ldg(p.v_scale + static_cast<long long>(g) * s.B + b) : 1.f;
+            const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) * vs / l : 0.f;
+            if (hd == hpc - 1 && named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
+                tc_fence_after();
+                uint8_t* stage = sKV + t * C::kOTileBytes;
+                stage_acc_row<D, EO>(tO, inv_l, stage, C::kChunkBytes, r, 0);
+                fence_proxy_async_smem();
+                named_bar_sync(kFwdBarEpi + t, kBlockM);
+                if (quad == 0 && lane == 0) {
+                    if (fa_box_ok(seq_start + tile_q_first, kBlockM, s.total_tokens, h, s.Hq, p.status))
+                        for (int c = 0; c < C::kOChunks; ++c)
+                            tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
+                                         seq_start + tile_q_first);
+                    bulk_commit_group();
+                    bulk_wait_read_all();   // the CTA's shared memory outlives the reads
+                }
+            } else if (ok) {
+                tc_fence_after();
+                uint16_t* orow_g = static_cast<uint16_t*>(p.o) +
+                                   (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orow[32];
+                    tmem_ld32(tO + c * 32, orow);
+                    tmem_ld_wait();
+                    reg_fence(orow);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<EO>(__uint_as_float(orow[2 * i]) * inv_l,
+                                         __uint_as_float(orow[2 * i + 1]) * inv_l);
+                    if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
+                                             static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
                 }
-                const float2 rsum = f2_unpack(f2_add(rs2[0], rs2[1]));
-                l += rsum.x + rsum.y;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O_t was last written by O_t += P V_{j-1}, complete before S_t(j) was
-                    // signalled; scale it in place before the next product accumulates.
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t orow[32];
-                        tmem_ld32(tO + c * 32, orow);
-                        tmem_ld_wait();
-                        reg_fence(orow);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                        tmem_st32(tO + c * 32, orow);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
             }
-            named_bar_signal(kFwdBarP + t, kFwdBarCount, ok);
-            if (DROP && ok && j + 1 < nkv) draw_block(j + 1);
+            if (ok && valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
+                                           static_cast<long long>(s.total_tokens) * s.Hq, p.status))
+                p.lse[row_stat_index(s, b, h, seq_start, q)] =
+                    (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
         }
-        // ------------------------------------------------------------ epilogue
-        if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bars->o_full), 0, abort_flag,
-                                                   p.timeout_cycles, p.status));
-        // A tile of 128 query rows inside the sequence leaves through shared memory
-        // (its K/V stage, idle by now) and TMA stores, coalesced and asynchronous; a
-        // tile cut by the sequence end is stored row by row.  The choice is made
-        // uniform over the warpgroup.
-        const bool valid = q < len;
-        // fp8: O carries the scale of V (per sequence and key/value head)
-        const float vs = (F8 && fa_index_ok(static_cast<long long>(g) * s.B + b,
-                                            static_cast<long long>(s.Hkv) * s.B, p.status))
-                             ? __ldg(p.v_scale + static_cast<long long>(g) * s.B + b) : 1.f;
-        const float inv_l = (l > 0.f) ? (DROP ? p.drop.rscale : 1.f) * vs / l : 0.f;
-        if (named_bar_all(kFwdBarEpi + t, kBlockM, ok && tile_q_first + kBlockM <= len)) {
-            tc_fence_after();
-            uint8_t* stage = sKV + t * C::kOTileBytes;
-            stage_acc_row<D, EO>(tO, inv_l, stage, C::kChunkBytes, r, 0);
-            fence_proxy_async_smem();
-            named_bar_sync(kFwdBarEpi + t, kBlockM);
-            if (quad == 0 && lane == 0) {
-                if (fa_box_ok(seq_start + tile_q_first, kBlockM, s.total_tokens, h, s.Hq, p.status))
-                    for (int c = 0; c < C::kOChunks; ++c)
-                        tma_store_3d(&p.tm_o, smem_addr(stage + c * C::kChunkBytes), c * 64, h,
-                                     seq_start + tile_q_first);
-                bulk_commit_group();
-                bulk_wait_read_all();   // the CTA's shared memory outlives the reads
-            }
-        } else if (ok) {
-            tc_fence_after();
-            uint16_t* orow_g = static_cast<uint16_t*>(p.o) +
-                               (static_cast<long long>(seq_start + q) * s.Hq + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t orow[32];
-                tmem_ld32(tO + c * 32, orow);
-                tmem_ld_wait();
-                reg_fence(orow);
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<EO>(__uint_as_float(orow[2 * i]) * inv_l,
-                                     __uint_as_float(orow[2 * i + 1]) * inv_l);
-                if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
-                                         static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                }
-            }
-        }
-        if (ok && valid && fa_index_ok(row_stat_index(s, b, h, seq_start, q),
-                                       static_cast<long long>(s.total_tokens) * s.Hq, p.status))
-            p.lse[row_stat_index(s, b, h, seq_start, q)] =
-                (l > 0.f) ? m_ref * kLn2 + logf(l) : kNegInf;
     }
 
     // ------------------------------------------------------------ teardown
     if (*abort_flag && warp == 1 && lane == 0) {
         // o_full was committed last: once it fires no tcgen05 op still uses TMEM
-        mbar_wait_drain(smem_addr(&bars->o_full), 0, kDrainCycles);
+        mbar_wait_drain(smem_addr(&bars->o_full), (hpc - 1) & 1, kDrainCycles);
     }
     tc_fence_before();
     __syncthreads();
@@ -553,12 +594,12 @@ int fwd_head_chunk(int n_keys, int d, int elem_bytes) {
     return static_cast<int>(fit < kHeadChunk ? kHeadChunk : fit > 4096 ? 4096 : fit);
 }
 
-template <int D, int E, bool DROP>
+template <int D, int E, bool DROP, bool HL = false>
 cudaError_t launch_fwd_d(const FwdParams& params, cudaStream_t stream) {
     using C = FwdCfg<D, E>;
     FwdParams p = params;
     p.head_chunk = fwd_head_chunk(p.seq.N, D, C::kElemBytes);
-    auto kern = fa_fwd_kernel<D, E, DROP>;
+    auto kern = fa_fwd_kernel<D, E, DROP, HL>;
     // the register split needs the launch's full 168 registers per thread: a
     // build that gave the kernel fewer would make the softmax warps wait forever
     static const cudaError_t regs_ok = [&] {
@@ -584,6 +625,10 @@ cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
     if (drop) {
         if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, true>(p, stream) : launch_fwd_d<64, kElemF16, true>(p, stream);
         return d == 128 ? launch_fwd_d<128, kElemBf16, true>(p, stream) : launch_fwd_d<64, kElemBf16, true>(p, stream);
+    }
+    if (p.heads > 1) {   // several query heads per CTA (16-bit, no dropout)
+        if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, false, true>(p, stream) : launch_fwd_d<64, kElemF16, false, true>(p, stream);
+        return d == 128 ? launch_fwd_d<128, kElemBf16, false, true>(p, stream) : launch_fwd_d<64, kElemBf16, false, true>(p, stream);
     }
     if (f16) return d == 128 ? launch_fwd_d<128, kElemF16, false>(p, stream) : launch_fwd_d<64, kElemF16, false>(p, stream);
     return d == 128 ? launch_fwd_d<128, kElemBf16, false>(p, stream) : launch_fwd_d<64, kElemBf16, false>(p, stream);

@@ -52,6 +52,7 @@ struct FwdParams {
     float scale_log2;   // softmax scale * log2(e)
     int num_work;       // launched CTAs (upper bound on work items)
     int head_chunk;     // heads per scheduling chunk (map_work); set by launch_fwd
+    int heads;          // query heads per CTA, a divisor of the GQA group (1: fp8, dropout)
     int elem;           // element type of q, k, v, o (kElemBf16Code / kElemF16Code), or
                         // kElemFp8Code: e4m3 q, k and transposed v (tm_v over [Hkv, d,
                         // vt_tokens]), bf16 o

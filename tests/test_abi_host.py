@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     for n in ("fa_fwd", "fa_bwd", "fa_fwd_typed", "fa_bwd_typed", "fa_fwd_dropout",
               "fa_bwd_dropout", "fa_bwd_workspace_size", "fa_last_error", "fa_device_status",
               "fa_fwd_fp8", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fp8_scale_blocks",
-              "fa_fp8_vt_tokens", "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads"):
+              "fa_fp8_vt_tokens", "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads",
+              "fa_fwd_set_heads"):
         assert n in names
 
 
@@ -167,6 +168,18 @@ def test_dq_heads_knob_is_validated_before_any_launch(lib):
     finally:
         fa.fa_bwd_set_dq_heads(0)
         fa.fa_bwd_set_path(fa.FA_BWD_AUTO)
+
+
+def test_fwd_heads_knob_is_validated_before_any_launch(lib):
+    fa, _ = lib
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_set_heads(-2)
+    try:
+        fa.fa_fwd_set_heads(3)                          # does not divide the group of 4
+        assert _fwd(fa, Hq=4, Hkv=1) == fa.FA_ERR_INVALID_ARG
+        assert "fa_fwd_set_heads" in fa.fa_last_error()
+    finally:
+        fa.fa_fwd_set_heads(0)
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -84,3 +84,42 @@ def test_forward_large_scores(fa, oracle_mod):
     assert np.isfinite(to_f64(o)).all()
     assert max_abs(to_f64(o), o_ref) <= O_MAX_ABS
     assert max_abs(lse.cpu().numpy().astype(np.float64), lse_ref) <= LSE_MAX_ABS
+
+
+# A forward CTA may serve several query heads of one key/value group (fa_fwd_set_heads;
+# the library's own choice gives more than one only on large grids).  Every divisor of
+# the group must give the same bits, and they must match the oracle.
+# (B, Hq, Hkv, N, d, causal, window, lengths, dtype)
+HEADS_CASES = [
+    (2, 8, 2, 300, 128, True, 0, None, "bf16"),
+    (1, 8, 1, 700, 64, True, 200, None, "bf16"),                    # MQA, window
+    (5, 4, 1, 513, 128, False, 0, (1, 127, 0, 129, 513), "f16"),     # packed, empty seq
+    (3, 6, 2, 260, 64, True, 0, (260, 1, 131), "bf16"),              # group of 3
+    (1, 4, 1, 100, 128, True, 0, None, "bf16"),                      # one key block per CTA
+]
+
+
+@pytest.mark.parametrize("case", HEADS_CASES,
+                         ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}"
+                                       f"{'p' if c[7] else ''}{c[8]}")
+def test_heads_per_cta_give_the_same_bits(fa, oracle_mod, case):
+    import torch
+    B, Hq, Hkv, N, d, causal, window, lengths, dtype = case
+    x = make_case(B, Hq, Hkv, N, d, seed=62, lengths=lengths, dtype=dtype, with_dout=False)
+    q, k, v = (to_dev(x[n]) for n in ("q", "k", "v"))
+    kw = dict(causal=causal, window=window, scale=scale_of(d), cu_seqlens=cu_dev(x["cu"]),
+              max_seqlen=N)
+    G = Hq // Hkv
+    first = None
+    for heads in [c for c in range(1, G + 1) if G % c == 0]:
+        o, lse = fa.attention_forward(q, k, v, heads=heads, **kw)
+        fa.fa_device_status(torch.cuda.current_stream())
+        if first is None:
+            first = (o, lse)
+            continue
+        assert torch.equal(o.view(torch.int16), first[0].view(torch.int16)), heads
+        assert torch.equal(lse, first[1]), heads
+    o_ref, lse_ref = oracle_mod.attention_fwd(x["q"], x["k"], x["v"], causal=causal, window=window,
+                                              scale=scale_of(d), cu_seqlens=x["cu"])
+    assert max_abs(to_f64(first[0]), o_ref) <= O_MAX_ABS
+    assert max_abs(first[1].cpu().numpy().astype(np.float64), lse_ref) <= LSE_MAX_ABS
