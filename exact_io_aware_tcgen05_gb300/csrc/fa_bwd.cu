@@ -536,6 +536,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                                [&](int i, int& head, int& row) {
                                    head = g;
                                    row = seq_start + (kt_first + (i / 2) % nk) * kBlockN;
+                                   // with head t's first K tile, head t+1's Q and dO tiles
+                                   // into L2: the element-wise warps read them at that
+                                   // head's start
+                                   const int t = i / (2 * nk);
+                                   if (i == 2 * nk * t && t + 1 < hpc)
+                                       for (int c = 0; c < C::kChunks; ++c) {
+                                           tma_prefetch_l2_3d(&p.tm_q, c * 64, h0 + t + 1, seq_start + q0);
+                                           tma_prefetch_l2_3d(&p.tm_do, c * 64, h0 + t + 1, seq_start + q0);
+                                       }
                                },
                                abort_flag, p, false);
     } else if (warp == 1) {
