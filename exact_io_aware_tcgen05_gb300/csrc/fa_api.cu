@@ -529,7 +529,7 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
                     wl.full, workspace_bytes);
     const bool fused = t_bwd_path == FA_BWD_FUSED ||
                        (t_bwd_path == FA_BWD_AUTO && can_fuse && prefer_fused(d));
-    if (!fused && t_dq_heads > 0 && (Hq / Hkv) % t_dq_heads != 0)
+    if (!fused && drop.thresh == 0 && t_dq_heads > 0 && (Hq / Hkv) % t_dq_heads != 0)
         return fail(FA_ERR_INVALID_ARG, "fa_bwd: %d query heads per dQ CTA (fa_bwd_set_dq_heads) do "
                     "not divide the group of %d", t_dq_heads, Hq / Hkv);
     const int kernels = 3;
@@ -569,7 +569,8 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
     p.dv = dv;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
-    p.dq_heads = t_dq_heads > 0 ? t_dq_heads : heads_per_cta(g, kBlockM, Hq, Hkv);
+    // several query heads per dQ CTA for the backward without dropout
+    p.dq_heads = drop.thresh != 0 ? 1 : t_dq_heads > 0 ? t_dq_heads : heads_per_cta(g, kBlockM, Hq, Hkv);
     p.num_work_dq = num_blocks(g, kBlockM, Hq / p.dq_heads);
     p.num_work_dkdv = num_blocks(g, kBlockN, Hkv);
     p.timeout_cycles = g_wait_limit.load();

@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 // head t+1 after it).  Only the last head's epilogue stages through the ring's shared
 // memory, which is idle by then; earlier heads store their dQ rows directly.
 
-template <int D, int E, bool DROP>
+template <int D, int E, bool DROP, bool HL>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     using R = Ring<C::kSlotsDq, C::kSlotsOddDq>;   // K_j (even) and V_j (odd)
@@ -506,7 +506,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     } wait_on_exit;
     if (!smem_base_ok(smem_raw, p.status)) return;
     const SeqInfo& s = p.seq;
-    const int hpc = p.dq_heads;   // query heads of this CTA (a divisor of the group)
+    // query heads of this CTA (a divisor of the group); the instances without the heads
+    // loop fix it at one at compile time
+    static_assert(!(HL && DROP), "the heads loop serves the backward without dropout");
+    const int hpc = HL ? p.dq_heads : 1;
     int b, hc, qblk;
     if (!map_work(s, blockIdx.x, kBlockM, s.Hq / hpc, true, b, hc, qblk)) return;
     int seq_start, len;
@@ -595,7 +598,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                 __syncwarp();
             }
             if (lane == 0) mma_commit(smem_addr(&bars->acc_full));   // head t's products done
-            __syncwarp();
         }
     } else if (warp == 2) {
         regs_lower<C::kRegsCtl>();
@@ -833,17 +835,19 @@ cudaError_t launch_dependent(K kern, int grid, int threads, int smem, const BwdP
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int D, int E, bool DROP>
+template <int D, int E, bool DROP, bool HL>
 cudaError_t launch_bwd_dq_d(const BwdParams& p, cudaStream_t stream) {
-    static const cudaError_t regs_ok = check_regs(fa_bwd_dq_kernel<D, E, DROP>, BwdCfg<D>::kRegsLaunch);
+    static const cudaError_t regs_ok = check_regs(fa_bwd_dq_kernel<D, E, DROP, HL>, BwdCfg<D>::kRegsLaunch);
     if (regs_ok != cudaSuccess) return regs_ok;
-    return launch_dependent(fa_bwd_dq_kernel<D, E, DROP>, p.num_work_dq, BwdCfg<D>::kThreads,
+    return launch_dependent(fa_bwd_dq_kernel<D, E, DROP, HL>, p.num_work_dq, BwdCfg<D>::kThreads,
                             BwdCfg<D>::kSmemBytes, p, stream);
 }
 
 template <int D, int E>
 cudaError_t launch_bwd_dq_de(const BwdParams& p, cudaStream_t stream) {
-    return p.drop.thresh ? launch_bwd_dq_d<D, E, true>(p, stream) : launch_bwd_dq_d<D, E, false>(p, stream);
+    if (p.drop.thresh) return launch_bwd_dq_d<D, E, true, false>(p, stream);
+    return p.dq_heads > 1 ? launch_bwd_dq_d<D, E, false, true>(p, stream)
+                          : launch_bwd_dq_d<D, E, false, false>(p, stream);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {

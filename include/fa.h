@@ -167,9 +167,10 @@ int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, in
  * once.  0, the default, lets fa_bwd choose: the largest divisor of the group
  * Hq / Hkv that still leaves at least 4 CTAs per SM (1 without GQA).  A positive
  * value forces that many; fa_bwd then fails with FA_ERR_INVALID_ARG (before any
- * launch) if it does not divide the group.  Results do not depend on the choice:
- * each head's products and their order are the same, so the bits are too.
- * FA_ERR_INVALID_ARG for heads < 0.
+ * launch) if it does not divide the group.  The backward with dropout always serves
+ * one head per dQ CTA.  Results do not depend on the choice: each head's products
+ * and their order are the same, so the bits are too.  FA_ERR_INVALID_ARG for
+ * heads < 0.
  */
 fa_status fa_bwd_set_dq_heads(int heads);
 

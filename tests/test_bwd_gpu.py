@@ -176,7 +176,7 @@ DQ_HEADS_CASES = [
     (1, 8, 1, 700, 64, True, 200, None, "bf16", None),              # MQA, window
     (5, 4, 1, 513, 128, False, 0, (1, 127, 0, 129, 513), "f16", None),   # packed, empty seq
     (3, 6, 2, 260, 64, True, 0, (260, 1, 131), "bf16", None),        # group of 3
-    (2, 4, 2, 384, 128, True, 0, None, "bf16", (0.1, 77, 3)),        # dropout: bits only
+    (2, 4, 2, 384, 128, True, 0, None, "bf16", (0.1, 77, 3)),        # dropout: one head per CTA whatever is asked
 ]
 
 
