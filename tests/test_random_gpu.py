@@ -6,7 +6,9 @@ Each case draws: the head dimension (64 or 128); key/value heads and a GQA group
 one- and two-token and longer sequences; a causal mask or none, and under a causal
 mask sometimes a sliding window (from one key to wider than the sequence); bf16 or fp16
 operands.  The backward runs the library's default path and, under causal masks, the
-fused path as well.  Tolerances are those of the other parity tests.
+fused path as well.  Tolerances are those of the other parity tests.  For a GQA group of
+more than one head the forward and the split backward also run with the whole group per
+CTA (fa_fwd_set_heads, fa_bwd_set_dq_heads), which must give the same bits.
 """
 import numpy as np
 import pytest
@@ -71,3 +73,12 @@ def test_random_shapes_match_oracle(fa, oracle_mod, idx):
         fa.fa_device_status(torch.cuda.current_stream())
         for name, g, r in zip(("dq", "dk", "dv"), got, grads):
             assert rel_fro(to_f64(g), r) <= GRAD_REL_FRO, (path, name)
+    G = hq // hkv
+    if G > 1:
+        o2, lse2 = fa.attention_forward(q, k, v, heads=G, **kw)
+        split = fa.attention_backward(q, k, v, o, lse, do, path="split", **kw)
+        grouped = fa.attention_backward(q, k, v, o, lse, do, path="split", dq_heads=G, **kw)
+        fa.fa_device_status(torch.cuda.current_stream())
+        assert torch.equal(o2.view(torch.int16), o.view(torch.int16)) and torch.equal(lse2, lse)
+        for name, a, b in zip(("dq", "dk", "dv"), grouped, split):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
