@@ -36,10 +36,10 @@ struct BwdCfg {
     // kSlotsOddDq.
     static constexpr int kSlotsDq = kSlots + 2;
     static constexpr int kSlotsOddDq = (D == 128) ? 2 : 3;
-    // element-wise warpgroups, each owning kEwCols of the 128 tile columns: d = 64 has
-    // half the tensor work per tile of d = 128 and the same element-wise work, so it
-    // gets twice the element-wise warps
-    static constexpr int kEwWG = (D == 64) ? 4 : 2;
+    // element-wise warpgroups, each owning kEwCols of the 128 tile columns.  Two at
+    // both head dimensions: four of 32 columns at d = 64 (640 threads, 96 registers at
+    // launch) spilled in the dK/dV kernel and measured slower than two of 64
+    static constexpr int kEwWG = 2;
     static constexpr int kEwCols = 128 / kEwWG;
     static constexpr int kEwThreads = 128 * kEwWG;
     static constexpr int kThreads = 128 + kEwThreads;   // warp 0 TMA, warp 1 MMA, warp 2 relay, warps 4.. element-wise
@@ -48,8 +48,8 @@ struct BwdCfg {
     // per SM); the warpgroup of warps 0..3 then drops to kRegsCtl and the
     // element-wise warpgroups rise to kRegsEw (setmaxnreg)
     static constexpr int kRegsLaunch = (65536 / kThreads) & ~7;
-    static constexpr int kRegsCtl = (D == 128) ? 152 : 64;
-    static constexpr int kRegsEw = (D == 128) ? 176 : 104;
+    static constexpr int kRegsCtl = 152;
+    static constexpr int kRegsEw = 176;
     static_assert(128 * kRegsCtl + kEwThreads * kRegsEw <= kThreads * kRegsLaunch,
                   "register split exceeds the launch's registers");
     static constexpr int kTmemCols = 512;
