@@ -109,9 +109,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // E: element type of q, k, v and o (kElemBf16 or kElemF16); DROP: dropout of P; HL: the
-// CTA serves p.heads query heads of one key/value group in turn (16-bit, no dropout).
-// Their K/V tiles are the same, so the ring streams them head after head and the CTA's
-// fixed costs (set-up, the first loads, the exit) are paid once.  Ring items, S and O
+// CTA serves p.heads consecutive query heads in turn (16-bit, no dropout).  The ring
+// streams each head's K/V tiles after the previous head's (the same tiles, read again
+// from L2, for the heads of one key/value group) and the CTA's fixed costs (set-up, the
+// first loads, the exit) are paid once.  Ring items, S and O
 // phases are counted over all the CTA's heads.  Head t+1's Q tiles load once q_empty
 // shows head t's last Q K^T complete; its first P V overwrites O only after the
 // softmax warps have left head t's epilogue (they hand P of head t+1 over after it).
@@ -213,13 +214,14 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                     mbar_arrive_expect_tx(fb, C::kTileBytes);
                     const CUtensorMap* map = (i & 1) ? &p.tm_v : &p.tm_k;
                     const int row = seq_start + (kv_first + i / 2) * kBlockN;
+                    const int gh = (h0 + hd) / s.group;   // this head's key/value head
                     if (F8 && (i & 1))
                         tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes), map, fb,
-                                         vt_col + (kv_first + i / 2) * kBlockN, 0, g, keep);
+                                         vt_col + (kv_first + i / 2) * kBlockN, 0, gh, keep);
                     else
                         for (int c = 0; c < C::kChunks; ++c)
                             tma_load_3d_hint(smem_addr(sKV + st * C::kTileBytes + c * C::kChunkBytes),
-                                             map, fb, c * C::kChunkElems, g, row, keep);
+                                             map, fb, c * C::kChunkElems, gh, row, keep);
                     issued = ig + 1;
                 }
             }

@@ -86,9 +86,9 @@ def test_forward_large_scores(fa, oracle_mod):
     assert max_abs(lse.cpu().numpy().astype(np.float64), lse_ref) <= LSE_MAX_ABS
 
 
-# A forward CTA may serve several query heads of one key/value group (fa_fwd_set_heads;
-# the library's own choice gives more than one only on large grids).  Every divisor of
-# the group must give the same bits, and they must match the oracle.
+# A forward CTA may serve several consecutive query heads (fa_fwd_set_heads; those of
+# one key/value group share its K/V tiles).  Every divisor of Hq, including counts that
+# span several groups, must give the same bits, and they must match the oracle.
 # (B, Hq, Hkv, N, d, causal, window, lengths, dtype)
 HEADS_CASES = [
     (2, 8, 2, 300, 128, True, 0, None, "bf16"),
@@ -96,6 +96,8 @@ HEADS_CASES = [
     (5, 4, 1, 513, 128, False, 0, (1, 127, 0, 129, 513), "f16"),     # packed, empty seq
     (3, 6, 2, 260, 64, True, 0, (260, 1, 131), "bf16"),              # group of 3
     (1, 4, 1, 100, 128, True, 0, None, "bf16"),                      # one key block per CTA
+    (2, 8, 8, 300, 128, True, 0, None, "bf16"),                      # MHA
+    (4, 4, 4, 300, 64, False, 0, (300, 1, 0, 129), "f16"),           # MHA, packed
 ]
 
 
@@ -109,9 +111,8 @@ def test_heads_per_cta_give_the_same_bits(fa, oracle_mod, case):
     q, k, v = (to_dev(x[n]) for n in ("q", "k", "v"))
     kw = dict(causal=causal, window=window, scale=scale_of(d), cu_seqlens=cu_dev(x["cu"]),
               max_seqlen=N)
-    G = Hq // Hkv
     first = None
-    for heads in [c for c in range(1, G + 1) if G % c == 0]:
+    for heads in [c for c in range(1, Hq + 1) if Hq % c == 0]:
         o, lse = fa.attention_forward(q, k, v, heads=heads, **kw)
         fa.fa_device_status(torch.cuda.current_stream())
         if first is None:
