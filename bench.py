@@ -52,6 +52,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel performs four and the dQ kernel contributes dQ (its second S and dP
 # are recomputation and not counted).
 KERNEL_FLOPS_PER_PAIR_D = {"fa_fwd": 4, "fa_bwd_fused": 10, "fa_bwd_dkdv": 8, "fa_bwd_dq": 2}
+# the products each kernel issues, per visible pair and unit of d (the dQ kernel rebuilds
+# S and dP before dQ = dS K: 3 products; the others issue exactly what they are credited)
+KERNEL_EXECUTED_FLOPS_PER_PAIR_D = {"fa_fwd": 4, "fa_bwd_fused": 10, "fa_bwd_dkdv": 8, "fa_bwd_dq": 6}
 HBM_KERNELS = ("fa_bwd_preprocess", "fa_bwd_dq_convert")
 KERNEL_SOURCES = {"fa_fwd": ("fa_fwd.cu",), "fa_bwd_fused": ("fa_bwd_fused.cu", "fa_bwd_common.cuh"),
                   "fa_bwd_dkdv": ("fa_bwd.cu", "fa_bwd_common.cuh"),
@@ -578,6 +581,9 @@ def run_ours(args, w):
                 fl = KERNEL_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
                 entry["algorithmic_tflop_per_launch"] = fl / 1e12
                 entry["tflops"] = fl / (mean / 1e3) / 1e12
+                ex = KERNEL_EXECUTED_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
+                entry["executed_tflop_per_launch"] = ex / 1e12
+                entry["executed_tflops"] = ex / (mean / 1e3) / 1e12
                 if name == "fa_fwd":
                     entry["algorithmic_bytes_per_launch"] = w.fwd_io_bytes()
                     entry["gbs"] = w.fwd_io_bytes() / (mean / 1e3) / 1e9

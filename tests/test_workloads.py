@@ -69,3 +69,16 @@ def test_io_bytes_are_the_tensors_read_and_written_once(name):
     else:
         assert w.fwd_io_bytes() == 2 * (q + 2 * kv) + 2 * q + 4 * lse
         assert w.bwd_io_bytes() == 2 * (3 * q + 2 * kv) + 4 * lse + 2 * (q + 2 * kv)
+
+
+def test_kernel_flop_credits_add_up():
+    """The kernels' credited FLOPs per pair and unit of d add up to the step's
+    algorithmic count on both backward paths (forward 4, backward 10), and the executed
+    count differs only for the dQ kernel, which also rebuilds S and dP (3 products)."""
+    import bench
+    cr, ex = bench.KERNEL_FLOPS_PER_PAIR_D, bench.KERNEL_EXECUTED_FLOPS_PER_PAIR_D
+    assert cr["fa_fwd"] == 4
+    assert cr["fa_bwd_dkdv"] + cr["fa_bwd_dq"] == 10 and cr["fa_bwd_fused"] == 10
+    assert set(cr) == set(ex)
+    assert {k for k in cr if cr[k] != ex[k]} == {"fa_bwd_dq"}
+    assert ex["fa_bwd_dq"] == 3 * 2
