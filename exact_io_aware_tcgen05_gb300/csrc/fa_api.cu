@@ -238,15 +238,15 @@ int heads_per_cta(const Geometry& g, int rows, int Hq, int Hkv) {
     return best;
 }
 
-// The forward's choice.  With GQA, heads_per_cta.  Without it there is no K/V to share,
-// only the fixed costs: short sequences (at most 2048 tokens, 16 key blocks per query
-// tile) take 2 heads per CTA while at least 1.5 CTAs per SM remain.  Measured on GB300:
-// B4 H16 N2048 causal 0.0783 -> 0.0758 ms with 2 heads, 0.116 ms with 4 (128 CTAs); at
-// N = 8192 (items 4x longer) 2 heads were 2.6% slower.
+// The forward's choice: heads_per_cta (GQA groups on large grids), and where that gives
+// one head, the fixed costs alone decide: short sequences (at most 2048 tokens, 16 key
+// blocks per query tile) take 2 heads per CTA while at least 1.5 CTAs per SM remain.
+// Measured on GB300 without GQA: B4 H16 N2048 causal 0.0783 -> 0.0758 ms with 2 heads,
+// 0.116 ms with 4 (128 CTAs); at N = 8192 (items 4x longer) 2 heads were 2.6% slower.
 int fwd_heads_per_cta(const Geometry& g, int Hq, int Hkv) {
     constexpr int rows = kFwdQTiles * kBlockM;
-    if (Hq != Hkv) return heads_per_cta(g, rows, Hq, Hkv);
-    if (g.seq.N > 2048 || Hq % 2 != 0) return 1;
+    const int c = heads_per_cta(g, rows, Hq, Hkv);
+    if (c > 1 || g.seq.N > 2048 || Hq % 2 != 0) return c;
     return 2LL * num_blocks(g, rows, Hq / 2) >= 3LL * sm_count() ? 2 : 1;
 }
 

@@ -105,9 +105,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * Query heads per CTA of the forward (per calling thread).  One CTA may serve several
  * consecutive query heads in turn and pay its fixed costs (set-up, the first loads,
  * the exit) once; the heads of one key/value group also read the same K and V tiles.
- * 0, the default, lets fa_fwd choose: with GQA the largest divisor of the group
- * Hq / Hkv that still leaves at least 4 CTAs per SM; without it 2 when no sequence is
- * longer than 2048 tokens and at least 1.5 CTAs per SM remain, else 1.  A positive
+ * 0, the default, lets fa_fwd choose: the largest divisor of the group Hq / Hkv that
+ * still leaves at least 4 CTAs per SM; where that is 1 (always without GQA), 2 when no
+ * sequence is longer than 2048 tokens and at least 1.5 CTAs per SM remain.  A positive
  * value forces that many; fa_fwd then fails with FA_ERR_INVALID_ARG (before any launch)
  * if it does not divide Hq.  The forward with dropout and the fp8 forward always serve
  * one head per CTA.  Results do not depend on the choice (each head's products, their
