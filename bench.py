@@ -79,7 +79,7 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--bwd-path", choices=["auto", "split", "fused"], default="auto",
                     help="backward path (fa_bwd_set_path): auto, the library's default choice; "
-                         "split (dK/dV and dQ kernels); fused (one kernel, causal masks)")
+                         "split (dK/dV and dQ kernels); fused (one kernel)")
     ap.add_argument("--fwd-heads", type=int, default=0,
                     help="query heads per forward CTA (fa_fwd_set_heads): 0, the library's "
                          "choice; else a divisor of the GQA group")

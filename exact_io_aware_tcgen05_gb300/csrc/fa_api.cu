@@ -318,8 +318,8 @@ bool bwd_workspace(int B, int Hq, int Hkv, int N, int d, int total_tokens, BwdWo
     return true;
 }
 
-// The backward fa_bwd runs by default for head dimension d when the mask and the
-// workspace allow the fused one (the path measured faster on GB300).
+// The backward fa_bwd runs by default for head dimension d when the workspace allows
+// the fused one (the path measured faster on GB300, with and without a causal mask).
 bool prefer_fused(int d) { return d == 64; }
 
 }  // namespace fa
@@ -462,8 +462,9 @@ int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, in
     fa::BwdWorkspace w;
     if (!fa::bwd_workspace(B, Hq, Hkv, N, d, total_tokens, &w) || workspace_bytes < w.delta)
         return -1;
+    (void)causal;
     (void)window;
-    const bool can_fuse = causal && workspace_bytes >= w.full;
+    const bool can_fuse = workspace_bytes >= w.full;
     if (t_bwd_path == FA_BWD_SPLIT) return FA_BWD_SPLIT;
     if (t_bwd_path == FA_BWD_FUSED) return can_fuse ? FA_BWD_FUSED : -1;
     return (can_fuse && fa::prefer_fused(d)) ? FA_BWD_FUSED : FA_BWD_SPLIT;
@@ -534,12 +535,10 @@ fa_status bwd_impl(fa_dtype dtype, const DropoutParams& drop, const void* q, con
                     workspace ? "" : " (null)");
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(FA_ERR_WORKSPACE, "fa_bwd: workspace must be 256-byte aligned");
-    // the fused backward (one tensor-core kernel) for causal masks when the workspace
-    // holds its dQ accumulator and the thread's preference allows it; otherwise the
-    // split backward (dK/dV, then dQ)
-    const bool can_fuse = causal && workspace_bytes >= wl.full;
-    if (t_bwd_path == FA_BWD_FUSED && !causal)
-        return fail(FA_ERR_UNSUPPORTED, "fa_bwd: the fused backward serves causal masks only");
+    // the fused backward (one tensor-core kernel, any mask) when the workspace holds
+    // its dQ accumulator and the thread's preference allows it; otherwise the split
+    // backward (dK/dV, then dQ)
+    const bool can_fuse = workspace_bytes >= wl.full;
     if (t_bwd_path == FA_BWD_FUSED && !can_fuse)
         return fail(FA_ERR_WORKSPACE, "fa_bwd: the fused backward needs a workspace of %zu bytes, got %zu",
                     wl.full, workspace_bytes);

@@ -9,8 +9,9 @@
 // forms each tile's dQ contribution, dQ_i += scale sum_j dS_ij k_j.
 //
 // One CTA per (sequence, key/value head, 128-key tile), looping over the query
-// heads of the group and the query tiles that see the key tile (causal masks,
-// with or without a sliding window).  Per step n the issuer runs
+// heads of the group and the query tiles that see the key tile (all of them
+// without a causal mask; under one, those from the key tile's diagonal on, up to
+// the window's end).  Per step n the issuer runs
 //   dV += P^T_n dO_n | S^T_{n+1} = K Q_{n+1}^T      (after P^T_n is written)
 //   dQ_n = (dS_n K)  | dK += dS^T_n Q_n              (after dS_n is written)
 //   dP^T_{n+1} = V dO_{n+1}^T                        (after dQ_n has been read out)

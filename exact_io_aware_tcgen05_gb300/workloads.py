@@ -130,6 +130,8 @@ WORKLOADS = {
         _varlen(128),
         _varlen(64),
         _many_short(),
+        # without a causal mask: 8 x 2048 tokens, 32 heads of 64 channels (width 2048)
+        Workload("fwdbwd_b8_h32_n2048_d64", 8, 32, 32, 2048, 64, False, 0, True),
     ]
 }
 

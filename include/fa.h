@@ -119,8 +119,8 @@ fa_status fa_fwd_set_heads(int heads);
  * Backward paths.  fa_bwd runs one of two:
  *   split  the row statistics D_i = sum_c dO_ic O_ic, a dK/dV kernel, then a dQ
  *          kernel that rebuilds S and dP a second time (any mask);
- *   fused  causal masks only: D_i and the fixed-point scales, ONE kernel that
- *          forms dQ, dK and dV from a single rebuild of each score tile, then a
+ *   fused  (any mask) D_i and the fixed-point scales, ONE kernel that forms
+ *          dQ, dK and dV from a single rebuild of each score tile, then a
  *          kernel that converts the dQ sums.  Several CTAs add into each dQ row;
  *          each contribution is rounded to fixed point (an int32 multiple of
  *          2^-F for an F chosen per row and channel from ||dO_i||_2, max_j ||v_j||_2
@@ -142,12 +142,12 @@ fa_status fa_fwd_set_heads(int heads);
  *   fa_bwd_workspace_size        what the default choice below needs for this d.
  *
  * Choice (per calling thread, fa_bwd_set_path): FA_BWD_AUTO, the default, runs
- * the fused backward where it measured faster on GB300 (d = 64), given a causal
- * mask and at least fa_bwd_workspace_size_fused bytes, and the split one
- * otherwise; FA_BWD_SPLIT always runs the split one; FA_BWD_FUSED always runs
- * the fused one and fails (FA_ERR_UNSUPPORTED without a causal mask,
- * FA_ERR_WORKSPACE with a smaller workspace).  fa_bwd_path tells which one
- * fa_bwd would run on the calling thread (-1: it would fail).
+ * the fused backward where it measured faster on GB300 (d = 64, with or without a
+ * causal mask), given at least fa_bwd_workspace_size_fused bytes, and the split
+ * one otherwise; FA_BWD_SPLIT always runs the split one; FA_BWD_FUSED always runs
+ * the fused one and fails with FA_ERR_WORKSPACE given a smaller workspace.
+ * fa_bwd_path tells which one fa_bwd would run on the calling thread (-1: it
+ * would fail).
  */
 typedef enum fa_bwd_path_kind {
     FA_BWD_AUTO = -1,

@@ -122,9 +122,9 @@ def test_workspace_size(lib):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_backward_path_selection(lib, d):
-    """Default: the fused backward for causal masks (with or without a window) at
-    d = 64 when the workspace holds it, the split one otherwise; a thread can force
-    either, and a forced fused call without its mask or workspace would fail."""
+    """Default: the fused backward at d = 64 (any mask) when the workspace holds it,
+    the split one otherwise; a thread can force either, and a forced fused call
+    without its workspace would fail."""
     fa, _ = lib
     args = (2, 4, 2, 300, d)
     full = fa.fa_bwd_workspace_size_fused(*args, 0)
@@ -135,7 +135,8 @@ def test_backward_path_selection(lib, d):
         assert fa.fa_bwd_path(*args, 1, 0, 0, full) == auto_fused
         assert fa.fa_bwd_path(*args, 1, 100, 0, full) == auto_fused
         assert fa.fa_bwd_path(*args, 1, 0, 0, full - 1) == fa.FA_BWD_SPLIT
-        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == fa.FA_BWD_SPLIT
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == auto_fused
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full - 1) == fa.FA_BWD_SPLIT
         assert fa.fa_bwd_path(*args, 1, 0, 0, least - 1) == -1
         assert fa.fa_bwd_path(2, 4, 2, 300, 96, 1, 0, 0, full) == -1
         fa.fa_bwd_set_path(fa.FA_BWD_SPLIT)
@@ -143,11 +144,9 @@ def test_backward_path_selection(lib, d):
         fa.fa_bwd_set_path(fa.FA_BWD_FUSED)
         assert fa.fa_bwd_path(*args, 1, 0, 0, full) == fa.FA_BWD_FUSED
         assert fa.fa_bwd_path(*args, 1, 0, 0, full - 1) == -1
-        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == -1
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full) == fa.FA_BWD_FUSED
+        assert fa.fa_bwd_path(*args, 0, 0, 0, full - 1) == -1
         # and fa_bwd itself refuses, before touching the GPU
-        st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, *args, 0, 0, None, 0, 0.1, 256, full,
-                       None, check=False)
-        assert st == fa.FA_ERR_UNSUPPORTED and "causal" in fa.fa_last_error()
         st = fa.fa_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, *args, 1, 0, None, 0, 0.1, 256, least,
                        None, check=False)
         assert st == fa.FA_ERR_WORKSPACE and "fused" in fa.fa_last_error()

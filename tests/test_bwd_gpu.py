@@ -18,6 +18,9 @@ SMALL = [
     (6, 4, 2, 513, 128, True, 0, (1, 127, 128, 129, 300, 513)),   # packed batch
     (6, 4, 2, 513, 64, True, 0, (1, 127, 128, 129, 300, 513)),
     (3, 2, 1, 900, 128, False, 0, (900, 5, 256)),
+    # without a causal mask at d = 64 (the default there is the fused backward)
+    (2, 4, 2, 300, 64, False, 0, None),
+    (4, 4, 1, 700, 64, False, 0, (700, 33, 256, 1)),
     (4, 4, 1, 700, 128, True, 100, (700, 33, 256, 1)),
     # the backward's work order takes heads in chunks of 8: 18 query-head pairs (dQ:
     # 8 + 8 + 2) and 9 key/value-head pairs (dK/dV: 8 + 1); packed, 12 query heads
@@ -35,9 +38,9 @@ SMALL = [
 ]
 
 
-# the two backward paths: "fused" (causal masks with the full workspace: one kernel,
-# dQ summed across CTAs as int32 fixed point) and "split" (the least workspace: a dK/dV
-# kernel and a dQ kernel)
+# the two backward paths: "fused" (the full workspace: one kernel, dQ summed across
+# CTAs as int32 fixed point) and "split" (the least workspace: a dK/dV kernel and a dQ
+# kernel)
 PATHS = ["fused", "split"]
 
 
@@ -81,8 +84,6 @@ def oracle_grads(oracle_mod, x, case):
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}{'p' if c[7] else ''}")
 def test_backward_matches_oracle(fa, oracle_mod, case, path):
     B, Hq, Hkv, N, d, causal, window, lengths = case
-    if path == "fused" and not causal:
-        pytest.skip("the fused backward serves causal masks; others run the split one")
     assert expected_path(fa, case, path) == (fa.FA_BWD_FUSED if path == "fused" else fa.FA_BWD_SPLIT)
     x = make_case(B, Hq, Hkv, N, d, seed=5, lengths=lengths)
     dq, dk, dv = run_fwd_bwd(fa, x, N, d, causal, window, path)
@@ -93,18 +94,19 @@ def test_backward_matches_oracle(fa, oracle_mod, case, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("case", [(1, 8, 2, 1100, 128, None), (3, 8, 2, 1100, 64, (1100, 7, 640))],
-                         ids=["d128", "d64packed"])
+@pytest.mark.parametrize("case", [(1, 8, 2, 1100, 128, True, None), (3, 8, 2, 1100, 64, True, (1100, 7, 640)),
+                                  (2, 4, 2, 1100, 64, False, None)],
+                         ids=["d128", "d64packed", "d64noncausal"])
 def test_backward_is_deterministic(fa, case, path):
     """Two runs give the same bits.  Split: every gradient row is summed by one CTA in
     a fixed order.  Fused: dK and dV as in the split path; dQ is summed across CTAs
     as fixed-point integers, whose sum does not depend on the order of the additions
     (both head dimensions; their accumulator layouts differ)."""
     import torch
-    B, Hq, Hkv, N, d, lengths = case
+    B, Hq, Hkv, N, d, causal, lengths = case
     x = make_case(B, Hq, Hkv, N, d, seed=9, lengths=lengths)
-    a = run_fwd_bwd(fa, x, N, d, True, 0, path)
-    b = run_fwd_bwd(fa, x, N, d, True, 0, path)
+    a = run_fwd_bwd(fa, x, N, d, causal, 0, path)
+    b = run_fwd_bwd(fa, x, N, d, causal, 0, path)
     for ga, gb in zip(a, b):
         assert torch.equal(ga.view(torch.int16), gb.view(torch.int16))
 
@@ -113,11 +115,12 @@ def test_backward_is_deterministic(fa, case, path):
     (2, 16, 2, 1500, 128, True, 0, None),          # GQA 8:1, 12 key tiles: chains of up to 12
     (1, 4, 4, 2100, 64, True, 300, None),          # window: chains of 4 over 17 tiles
     (5, 8, 4, 900, 128, True, 0, (900, 1, 385, 0, 640)),   # packed, unaligned starts, empty
-], ids=["gqa8_chain12", "d64_window300", "packed_mixed"])
+    (1, 8, 2, 2100, 64, False, 0, None),          # no mask: every row gets all 17 tiles
+], ids=["gqa8_chain12", "d64_window300", "packed_mixed", "d64_noncausal17"])
 def test_fused_backward_longer_chains(fa, oracle_mod, case):
     """The fused backward on cases whose dQ rows collect many contributions (long
     causal chains, a window, GQA 8:1, a packed batch with unaligned starts and an
-    empty sequence), against the oracle."""
+    empty sequence, no mask over 17 key tiles), against the oracle."""
     B, Hq, Hkv, N, d, causal, window, lengths = case
     assert expected_path(fa, case, "fused") == fa.FA_BWD_FUSED
     x = make_case(B, Hq, Hkv, N, d, seed=17, lengths=lengths)

@@ -99,14 +99,16 @@ CASES = [
     (1, 4, 4, 513, 64, True, 0, None),
     (1, 8, 1, 700, 128, True, 200, None),
     (2, 2, 2, 200, 128, False, 0, None),
+    (2, 4, 2, 300, 64, False, 0, None),
     (6, 4, 2, 513, 128, True, 0, (1, 127, 128, 129, 300, 513)),
     (6, 4, 2, 513, 64, True, 0, (1, 127, 128, 129, 300, 513)),
 ]
 
 
+@pytest.mark.parametrize("path", ["fused", "split"])
 @pytest.mark.parametrize("p_drop", [0.1, 0.3])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}h{c[1]}x{c[2]}n{c[3]}d{c[4]}c{int(c[5])}w{c[6]}{'p' if c[7] else ''}")
-def test_dropout_matches_oracle(fa, drop, case, p_drop):
+def test_dropout_matches_oracle(fa, drop, case, p_drop, path):
     import torch
     B, Hq, Hkv, N, d, causal, window, lengths = case
     x = make_case(B, Hq, Hkv, N, d, seed=31, lengths=lengths)
@@ -115,7 +117,7 @@ def test_dropout_matches_oracle(fa, drop, case, p_drop):
               max_seqlen=N, dropout=(p_drop, seed, off))
     q, k, v, do = (to_dev(x[n]) for n in ("q", "k", "v", "dout"))
     o, lse = fa.attention_forward(q, k, v, **kw)
-    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, **kw)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, path=path, **kw)
     fa.fa_device_status(torch.cuda.current_stream())
     okw = dict(causal=causal, window=window, scale=scale_of(d), p_drop=p_drop, seed=seed,
                offset=off, cu_seqlens=x["cu"])

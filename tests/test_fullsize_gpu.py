@@ -81,7 +81,7 @@ def token_index(w, b, rows):
 # dropout workloads are checked against the dropout oracle at smaller sizes
 # (tests/test_dropout_gpu.py): its dense per-head matrices do not scale to these;
 # the fp8 workload against the fp8 oracle (tests/test_fp8_gpu.py, same shape)
-# backward workloads run both backward paths (all of them have causal masks)
+# backward workloads run both backward paths
 CASES = [(n, p) for n, w in sorted(WORKLOADS.items()) if w.p_drop == 0 and w.dtype != "fp8"
          for p in (("split", "fused") if w.backward else ("split",))]
 

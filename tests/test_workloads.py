@@ -54,6 +54,7 @@ def test_closed_forms_of_the_dense_workloads():
     assert WORKLOADS["fwdbwd_b1_h32kv8_n16384_d128_causal_w4096"].visible_pairs_per_head() == \
         4096 * 4097 // 2 + (16384 - 4096) * 4096
     assert WORKLOADS["fwd_b1_h1_n128_d64"].visible_pairs_per_head() == 128 * 128
+    assert WORKLOADS["fwdbwd_b8_h32_n2048_d64"].visible_pairs_per_head() == 8 * 2048 * 2048
 
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
