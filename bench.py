@@ -9,11 +9,12 @@ inputs already resident in HBM).  Prints ONE JSON line on rank 0:
   e2e          the same metric through the C ABI with pinned HOST buffers: each
                step copies Q, K, V, dO in and O, LSE, dQ, dK, dV out (two device
                buffer sets; copies of neighbouring steps overlap the kernels)
-  roofline     the dominant kernel (largest device time): algorithmic FLOPs per
-               launch / its mean launch time, from a second timed region of K
-               steps in which the library records CUDA events around each of
-               its launches on the launching stream, against the measured bf16
-               tensor peak
+  roofline     the dominant kernel (largest device time): algorithmic FLOPs (or
+               bytes) per launch / its mean launch time, from a second timed
+               region of K steps in which the library records CUDA events around
+               each of its launches on the launching stream, against the measured
+               bf16 tensor peak (or HBM copy rate): whichever of the two gives the
+               kernel's algorithmic work the longer time is its bound
   cpu_baseline the fp64 oracle timed on the host cores on a bounded sample
   clocks       SM clocks and throttle reasons sampled during the timed region
 
@@ -110,6 +111,12 @@ def job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> fl
     """Whole-job throughput of `world` replicas, each doing flops_per_rank_step per step,
     when the slowest rank takes ms_per_step per step."""
     return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
+
+
+def binding_roof(tflop: float, nbytes: float, peak_tflops: float, peak_gbs: float) -> str:
+    """The roof that binds a kernel: "tensor" if its algorithmic FLOPs need at least as
+    long at the tensor peak as its algorithmic bytes need at the HBM rate, else "hbm"."""
+    return "tensor" if tflop / peak_tflops >= nbytes / 1e9 / peak_gbs else "hbm"
 
 
 def measured_peaks():
@@ -569,6 +576,7 @@ def run_ours(args, w):
     # e4m3 products: the measured bf16 figure times the nominal fp8 / bf16 ratio (4.5 / 2.25)
     peak_mult = 2.0 if fp8 else 1.0
     peak_tf *= peak_mult
+    peak_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     kernels, roof, fwd_tf, bwd_tf = None, None, None, None
     if not args.no_kernel_events:
         pairs_heads = w.visible_pairs_per_head() * w.Hq
@@ -584,31 +592,26 @@ def run_ours(args, w):
                 ex = KERNEL_EXECUTED_FLOPS_PER_PAIR_D[name] * w.d * pairs_heads
                 entry["executed_tflop_per_launch"] = ex / 1e12
                 entry["executed_tflops"] = ex / (mean / 1e3) / 1e12
-                if name == "fa_fwd":
-                    entry["algorithmic_bytes_per_launch"] = w.fwd_io_bytes()
-                    entry["gbs"] = w.fwd_io_bytes() / (mean / 1e3) / 1e9
-            else:
-                T_, Hq_, Hkv_, d_ = w.total_tokens, w.Hq, w.Hkv, w.d
-                if name == "fa_bwd_dq_convert":
-                    # int32 sums and row scales in, dQ out
-                    by = 4 * T_ * Hq_ * d_ + 4 * T_ * Hq_ + 2 * T_ * Hq_ * d_
-                else:
-                    # O and dO in, D out; fused: also the row scales out, the int32 sums
-                    # zeroed and K, V read for their bounds
-                    by = 2 * T_ * Hq_ * d_ * 2 + 4 * T_ * Hq_
-                    if fused:
-                        by += 4 * T_ * Hq_ + 4 * T_ * Hq_ * d_ + 2 * T_ * Hkv_ * d_ * 2
-                entry["algorithmic_bytes_per_launch"] = by
-                entry["gbs"] = by / (mean / 1e3) / 1e9
+            by = w.kernel_io_bytes(name, fused)
+            entry["algorithmic_bytes_per_launch"] = by
+            entry["gbs"] = by / (mean / 1e3) / 1e9
+            entry["bound"] = binding_roof(entry.get("algorithmic_tflop_per_launch", 0.0), by,
+                                          peak_tf, peak_gbs)
             kernels[name] = entry
         tot = sum(k["ms_mean"] for k in kernels.values())
         for k in kernels.values():
             k["share"] = k["ms_mean"] / tot
-        dom = max((n for n in kernels if n in KERNEL_FLOPS_PER_PAIR_D), key=lambda n: kernels[n]["ms_mean"])
-        roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_tf,
-                "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (nominal fp8 / bf16)" if fp8 else "") + (" of measured" if peak_src == "measured" else " of fallback"),
-                "traffic": recorded_traffic(dom, w.name)}
+        dom = max(kernels, key=lambda n: kernels[n]["ms_mean"])
+        of = " of measured" if peak_src == "measured" else " of fallback"
+        if kernels[dom]["bound"] == "tensor":
+            roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_tf,
+                    "peak_source": f"{peak_src} bf16_tflops (burst)" + (" x 2 (nominal fp8 / bf16)" if fp8 else "") + of}
+        else:
+            roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak_gbs,
+                    "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak_gbs,
+                    "peak_source": f"{peak_src} hbm_gbs (copy)" + of}
+        roof["traffic"] = recorded_traffic(dom, w.name)
         fwd_tf = fwd_flops / (kernels["fa_fwd"]["ms_mean"] / 1e3) / 1e12
         bwd_tf = None
         if bwd:

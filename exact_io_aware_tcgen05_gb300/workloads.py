@@ -89,6 +89,29 @@ class Workload:
                 + 4 * T * self.Hq                                     # LSE
                 + 2 * T * self.d * (self.Hq + 2 * self.Hkv))          # dQ, dK, dV
 
+    def kernel_io_bytes(self, kernel: str, fused: bool = False) -> int:
+        """Algorithmic HBM bytes of one launch of a library kernel: each tensor the kernel
+        must read or write, once (16-bit Q, K, V, O, dO and gradients; fp32 LSE, D and row
+        scales; the fused backward's int32 dQ sums).  ``fused``: the preprocess of the
+        fused backward, which also writes the row scales, zeroes the dQ sums and reads K
+        and V for their bounds."""
+        T, d = self.total_tokens, self.d
+        q, kv, rows = T * self.Hq * d, T * self.Hkv * d, T * self.Hq
+        e = 2
+        if kernel == "fa_fwd":
+            return self.fwd_io_bytes()
+        if kernel == "fa_bwd_preprocess":            # O, dO in; D out
+            return 2 * e * q + 4 * rows + ((4 * rows + 4 * q + 2 * e * kv) if fused else 0)
+        if kernel == "fa_bwd_dkdv":                  # Q, dO, K, V, LSE, D in; dK, dV out
+            return e * (2 * q + 2 * kv) + 8 * rows + 2 * e * kv
+        if kernel == "fa_bwd_dq":                    # Q, dO, K, V, LSE, D in; dQ out
+            return e * (2 * q + 2 * kv) + 8 * rows + e * q
+        if kernel == "fa_bwd_fused":                 # + row scales in; dK, dV, int32 dQ sums out
+            return e * (2 * q + 2 * kv) + 12 * rows + 2 * e * kv + 4 * q
+        if kernel == "fa_bwd_dq_convert":            # int32 sums and row scales in, dQ out
+            return 4 * q + 4 * rows + e * q
+        raise KeyError(kernel)
+
 
 def visible_pairs(L: int, causal: bool, window: int) -> int:
     """Number of (query, key) pairs with key visible to query in one sequence of length L."""

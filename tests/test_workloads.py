@@ -83,3 +83,39 @@ def test_kernel_flop_credits_add_up():
     assert set(cr) == set(ex)
     assert {k for k in cr if cr[k] != ex[k]} == {"fa_bwd_dq"}
     assert ex["fa_bwd_dq"] == 3 * 2
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_kernel_io_bytes_are_the_tensors_each_kernel_moves(name):
+    """Per-kernel algorithmic bytes, from the tensor shapes: the dK/dV and dQ kernels
+    each read Q, dO, K, V, LSE and D and write their own gradients; the fused backward
+    writes dK, dV and the int32 dQ sums; the preprocess reads O and dO and writes D."""
+    w = WORKLOADS[name]
+    n = lambda shape: int(np.prod(shape))
+    q, kv, rows = n(w.q_shape), n(w.kv_shape), n(w.lse_shape)
+    assert w.kernel_io_bytes("fa_fwd") == w.fwd_io_bytes()
+    reads = 2 * (2 * q + 2 * kv) + 4 * rows + 4 * rows
+    assert w.kernel_io_bytes("fa_bwd_dkdv") == reads + 2 * (2 * kv)
+    assert w.kernel_io_bytes("fa_bwd_dq") == reads + 2 * q
+    assert w.kernel_io_bytes("fa_bwd_fused") == reads + 4 * rows + 2 * (2 * kv) + 4 * q
+    assert w.kernel_io_bytes("fa_bwd_preprocess") == 2 * 2 * q + 4 * rows
+    assert w.kernel_io_bytes("fa_bwd_dq_convert") == 4 * q + 4 * rows + 2 * q
+
+
+def test_roofline_bound_follows_arithmetic_intensity():
+    """The kernels of the long-sequence workloads are tensor-bound at the measured peaks
+    (1875 TFLOP/s, 6788 GB/s: a ridge near 276 FLOP/B); those of 1024 sequences of
+    64-512 tokens and the single 128-token tile are HBM-bound."""
+    import bench
+    def bound(name, kernel):
+        w = WORKLOADS[name]
+        fl = bench.KERNEL_FLOPS_PER_PAIR_D[kernel] * w.d * w.visible_pairs_per_head() * w.Hq
+        return bench.binding_roof(fl / 1e12, w.kernel_io_bytes(kernel), 1875.4, 6788.3)
+    # the rule itself: equal times go to the tensor roof
+    assert bench.binding_roof(1.0, 1e9 * 6788.3 / 1875.4, 1875.4, 6788.3) == "tensor"
+    assert bench.binding_roof(1.0, 1.01e9 * 6788.3 / 1875.4, 1875.4, 6788.3) == "hbm"
+    for k in ("fa_fwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_fused"):
+        assert bound("fwdbwd_b2_h16_n8192_d128_causal", k) == "tensor"
+        assert bound("fwdbwd_varlen1024_h32kv8_d128_causal", k) == "hbm"
+    assert bound("fwd_b4_h16_n2048_d128_causal", "fa_fwd") == "tensor"
+    assert bound("fwd_b1_h1_n128_d64", "fa_fwd") == "hbm"
