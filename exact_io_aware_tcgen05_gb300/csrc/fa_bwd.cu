@@ -469,16 +469,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 
 // ---------------------------------------------------------------------- dQ
 //
-// Q and dO of the CTA's query tile live in TMEM, copied there row by row by the
-// element-wise warps at the start, as the A operands of S_j = Q K_j^T and dP_j =
-// dO V_j^T; shared memory holds only the K/V slot ring (7 slots at d = 128: 5 for
-// K_j, 2 for V_j; K_j is held from S_j to dQ_j, about one and a half steps, and
-// the deeper ring lets its load start well before it is needed).  Per key tile j:
+// Q and dO of the CTA's query tile live in TMEM, as the A operands of S_j = Q K_j^T
+// and dP_j = dO V_j^T.  Shared memory holds one slot ring (7 slots at d = 128: 5 for
+// even items, 2 for odd ones); per query head it streams Q and dO (items 0 and 1,
+// whole tiles by TMA), then K_j and V_j as items 2 + 2j and 3 + 2j.  The element-wise
+// warps copy their rows of Q and dO from the ring into TMEM (whole-tile loads, then
+// conflict-free reads of the swizzled rows: a warp-wide load of 32 scattered rows from
+// global memory took about 3 us per tile) and the issuer hands the two slots back.
+// K_j is held from S_j to dQ_j, about one and a half steps, and the deeper even ring
+// lets its load start well before it is needed.  Per key tile j:
 // as soon as the element-wise warps have read S_j into registers the issuer runs
 // S_{j+1}; when dS_j is back in TMEM (over dP_j) it runs dQ += dS_j K_j and then
 // dP_{j+1} into the same columns (tcgen05 ops of one thread execute in issue
-// order, so dQ_j has read dS_j first).  K_j and V_j stream through the ring as
-// items 2j and 2j+1; V_j's slot is released after dP_j, K_j's after dQ_j.  Every
+// order, so dQ_j has read dS_j first).  V_j's slot is released after dP_j, K_j's
+// after dQ_j.  Every
 // signal waits for its waiter's previous phase: S_{j+1} needs S_j read, dP_{j+1}
 // needs dS_j written, so no mbarrier or named barrier runs two phases ahead.
 //
@@ -486,8 +490,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 // at launch so that enough CTAs remain): their K/V tiles are the same, so the ring
 // streams them head after head without a break and the CTA's fixed costs (barrier
 // set-up, TMEM allocation, the first loads) are paid once.  Steps are counted over
-// all heads (J = t nk + j for head t), and so are the ring items and the mbarrier
-// phases.  Head t+1's Q and dO go into TMEM once acc_full has shown that every
+// all heads (J = t nk + j for head t), ring items too (2 nk + 2 per head), and so are
+// the mbarrier phases.  Head t+1's Q and dO go into TMEM once acc_full has shown that every
 // product of head t is complete; its first dQ product overwrites the accumulator only
 // after all element-wise warps have passed head t's epilogue (they signal dS_0 of
 // head t+1 after it).  Only the last head's epilogue stages through the ring's shared
@@ -522,6 +526,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     const int kt_last = key_hi(s, q_last, len) / kBlockN;
     const int nk = kt_last - kt_first + 1;
     const int steps = hpc * nk;   // key-tile steps over all heads of the CTA
+    // ring items per head: Q, dO, then K_j, V_j; K_j of head t is item k_item(t, j)
+    const int P = 2 * nk + 2;
+    auto k_item = [&](int t, int j) { return t * P + 2 + 2 * j; };
 
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw);
     uint8_t* sSlots = smem_raw + C::kHeadBytes;
@@ -535,19 +542,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
     if (warp == 0) {
         regs_lower<C::kRegsCtl>();
         if (lane == 0)
-            stream_tiles<D, R>(bars, sSlots, 2 * steps, &p.tm_k, &p.tm_v,
-                               [&](int i, int& head, int& row) {
+            stream_tiles<D, R>(bars, sSlots, P * hpc, &p.tm_k, &p.tm_v,
+                               [&](int i, int& head, int& row) -> const CUtensorMap* {
+                                   const int t = i / P, k = i % P;
+                                   if (k < 2) {            // Q and dO of query head t
+                                       head = h0 + t;
+                                       row = seq_start + q0;
+                                       return k == 0 ? &p.tm_q : &p.tm_do;
+                                   }
                                    head = g;
-                                   row = seq_start + (kt_first + (i / 2) % nk) * kBlockN;
+                                   row = seq_start + (kt_first + (k - 2) / 2) * kBlockN;
                                    // with head t's first K tile, head t+1's Q and dO tiles
-                                   // into L2: the element-wise warps read them at that
-                                   // head's start
-                                   const int t = i / (2 * nk);
-                                   if (i == 2 * nk * t && t + 1 < hpc)
+                                   // into L2, so that their ring loads are short
+                                   if (k == 2 && t + 1 < hpc)
                                        for (int c = 0; c < C::kChunks; ++c) {
                                            tma_prefetch_l2_3d(&p.tm_q, c * 64, h0 + t + 1, seq_start + q0);
                                            tma_prefetch_l2_3d(&p.tm_do, c * 64, h0 + t + 1, seq_start + q0);
                                        }
+                                   return nullptr;         // K_j (even) or V_j (odd)
                                },
                                abort_flag, p, false);
     } else if (warp == 1) {
@@ -563,36 +575,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                              p.timeout_cycles, p.status);
         };
         for (int t = 0; t < hpc; ++t) {
-            const int J0 = t * nk;                          // first step of head t
             named_bar_sync(kBarOperands, kOperandBar);    // Q and dO of head t are in TMEM
             if (lane == 0) {
-                if (wait(2 * J0) && wait(2 * J0 + 1)) {}
+                // the element-wise warps read Q and dO from their slots before the
+                // barrier: the slots go back to the producer
+                mbar_arrive(smem_addr(&bars->slot_empty[R::index(t * P)]));
+                mbar_arrive(smem_addr(&bars->slot_empty[R::index(t * P + 1)]));
+                const int k0 = k_item(t, 0);
+                if (wait(k0) && wait(k0 + 1)) {}
                 tc_fence_after();
-                issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * J0));    // S_0 = Q K_0^T
+                issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(k0));        // S_0 = Q K_0^T
                 mma_commit(smem_addr(&bars->s_full));
-                issue_ts_k<D, E>(tDP, tDO, slot(2 * J0 + 1));           // dP_0 = dO V_0^T
+                issue_ts_k<D, E>(tDP, tDO, slot(k0 + 1));               // dP_0 = dO V_0^T
                 mma_commit(smem_addr(&bars->dp_full[0]));
-                free_slot(2 * J0 + 1);
+                free_slot(k0 + 1);
             }
             __syncwarp();
             for (int j = 0; j < nk; ++j) {
-                const int J = J0 + j;
+                const int kj = k_item(t, j);                    // K_j; V_j is kj + 1
                 named_bar_sync(kBarP, C::kBarCount);            // S_j read, K_{j+1} landed
                 if (lane == 0 && j + 1 < nk) {
                     tc_fence_after();
-                    issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(2 * J + 2));   // S_{j+1}
+                    issue_ts_k<D, E>(tmem + C::kColS, tQ, slot(kj + 2));   // S_{j+1}
                     mma_commit(smem_addr(&bars->s_full));
                 }
                 __syncwarp();
                 named_bar_sync(kBarDS0, C::kBarCount);          // dS_j written, V_{j+1} landed
                 if (lane == 0) {
                     tc_fence_after();
-                    issue_ts<D, E>(tmem + C::kColAcc, tDP, slot(2 * J), j > 0);   // dQ += dS_j K_j
-                    free_slot(2 * J);
+                    issue_ts<D, E>(tmem + C::kColAcc, tDP, slot(kj), j > 0);   // dQ += dS_j K_j
+                    free_slot(kj);
                     if (j + 1 < nk) {
-                        issue_ts_k<D, E>(tDP, tDO, slot(2 * J + 3));   // dP_{j+1}, after dQ_j read dS_j
+                        issue_ts_k<D, E>(tDP, tDO, slot(kj + 3));   // dP_{j+1}, after dQ_j read dS_j
                         mma_commit(smem_addr(&bars->dp_full[0]));
-                        free_slot(2 * J + 3);
+                        free_slot(kj + 3);
                     }
                 }
                 __syncwarp();
@@ -607,11 +623,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
                       p.timeout_cycles, p.status);
         };
         for (int J = 0; J < steps; ++J) {
-            const bool more = (J % nk) + 1 < nk;                 // head J / nk has a next tile
-            if (lane == 0 && more) wait_item(2 * J + 2);         // K_{j+1}
+            const int t = J / nk, j = J % nk;
+            const bool more = j + 1 < nk;                        // head t has a next tile
+            if (lane == 0 && more) wait_item(k_item(t, j + 1));      // K_{j+1}
             __syncwarp();
             named_bar_sync(kBarP, C::kBarCount);
-            if (lane == 0 && more) wait_item(2 * J + 3);         // V_{j+1}
+            if (lane == 0 && more) wait_item(k_item(t, j + 1) + 1);  // V_{j+1}
             __syncwarp();
             named_bar_sync(kBarDS0, C::kBarCount);
         }
@@ -642,22 +659,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const
             const int h = h0 + t;
             {
                 // Q and dO of row q into TMEM, two elements per 32-bit column as they lie
-                // in memory (the A-operand layout of S and dP): each warpgroup copies kQW
-                // of the D/2 columns; rows past the sequence end are zero.  For t > 0 the
-                // previous head's products are complete (acc_full, below).
-                constexpr int kQW = D / 2 / C::kEwWG;   // 32 (d = 128) or 8 (d = 64)
+                // in memory (the A-operand layout of S and dP), from their ring slots: each
+                // warpgroup copies kQW of the D/2 columns, whole 16-byte units of the
+                // 128-byte-swizzled row; rows past the sequence end are zero.  For t > 0
+                // the previous head's products are complete (acc_full, below).
+                constexpr int kQW = D / 2 / C::kEwWG;   // 32 (d = 128) or 16 (d = 64)
+                static_assert(kQW % 4 == 0 && 4 * kQW <= 128, "whole units of one 64-column chunk");
                 uint32_t wq[kQW], wd[kQW];
 #pragma unroll
                 for (int i = 0; i < kQW; ++i) wq[i] = wd[i] = 0u;
-                if (valid && fa_index_ok(static_cast<long long>(seq_start + q) * s.Hq + h,
-                                         static_cast<long long>(s.total_tokens) * s.Hq, p.status)) {
-                    const long long off = (static_cast<long long>(seq_start + q) * s.Hq + h) * D +
-                                          2 * kQW * wg;
-                    const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + off);
-                    const uint4* gd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + off);
+                const int qi = t * P;                   // Q's item; dO's is qi + 1
+                if (ok) ok = warp_wait(smem_addr(&bars->slot_full[R::index(qi)]), R::use(qi) & 1,
+                                       abort_flag, p.timeout_cycles, p.status);
+                if (ok) ok = warp_wait(smem_addr(&bars->slot_full[R::index(qi + 1)]), R::use(qi + 1) & 1,
+                                       abort_flag, p.timeout_cycles, p.status);
+                if (ok && valid) {
+                    const int byte0 = 4 * kQW * wg;     // this warpgroup's first byte of the row
+                    const int off = (byte0 / 128) * C::kChunkBytes;
+                    const int u0 = (byte0 % 128) / 16;
+                    uint8_t* tq = sSlots + R::index(qi) * C::kTileBytes + off;
+                    uint8_t* td = sSlots + R::index(qi + 1) * C::kTileBytes + off;
 #pragma unroll
                     for (int i = 0; i < kQW / 4; ++i) {
-                        const uint4 a = __ldg(gq + i), c = __ldg(gd + i);
+                        const uint4 a = *swizzled_unit(tq, r, u0 + i), c = *swizzled_unit(td, r, u0 + i);
                         wq[4 * i] = a.x; wq[4 * i + 1] = a.y; wq[4 * i + 2] = a.z; wq[4 * i + 3] = a.w;
                         wd[4 * i] = c.x; wd[4 * i + 1] = c.y; wd[4 * i + 2] = c.z; wd[4 * i + 3] = c.w;
                     }

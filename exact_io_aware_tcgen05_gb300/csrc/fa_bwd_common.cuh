@@ -11,6 +11,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 namespace fa {
 namespace {
 
@@ -331,10 +333,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit, status));
 }
 
-// Producer loop shared by both kernels: streams `items` tiles through the slot
+// Producer loop shared by the kernels: streams `items` tiles through the slot
 // ring R (item i from map (i & 1) ? odd : even); `coords(i, head, row)` gives the
-// head and token row of item i.  `resident`: the CTA also loaded a resident pair
-// on res_full, which an abort has to wait for too.
+// head and token row of item i and may return another tensor map for it (void or
+// nullptr: the one its parity names).  `resident`: the CTA also loaded a resident
+// pair on res_full, which an abort has to wait for too.
 template <int D, typename R, typename Coords>
 __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int items,
                                              const CUtensorMap* even, const CUtensorMap* odd,
@@ -351,8 +354,13 @@ __device__ __forceinline__ void stream_tiles(BwdBars* bars, uint8_t* slots, int 
         const uint32_t fb = smem_addr(&bars->slot_full[sl]);
         mbar_arrive_expect_tx(fb, C::kTileBytes);
         int head, row;
-        coords(i, head, row);
         const CUtensorMap* map = (i & 1) ? odd : even;
+        if constexpr (std::is_void_v<decltype(coords(i, head, row))>) {
+            coords(i, head, row);
+        } else {
+            const CUtensorMap* m = coords(i, head, row);
+            if (m) map = m;
+        }
         for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d_hint(smem_addr(slots + sl * C::kTileBytes + c * C::kChunkBytes), map, fb,
                              c * 64, head, row, keep);
