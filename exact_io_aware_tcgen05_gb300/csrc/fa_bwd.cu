@@ -471,36 +471,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dkdv_kernel(con
 //
 // Q and dO of the CTA's query tile live in TMEM, as the A operands of S_j = Q K_j^T
 // and dP_j = dO V_j^T.  Shared memory holds one slot ring (7 slots at d = 128: 5 for
-// even items, 2 for odd ones); per query head it streams Q and dO (items 0 and 1,
-// whole tiles by TMA), then K_j and V_j as items 2 + 2j and 3 + 2j.  The element-wise
-// warps copy their rows of Q and dO from the ring into TMEM (whole-tile loads, then
-// conflict-free reads of the swizzled rows: a warp-wide load of 32 scattered rows from
-// global memory took about 3 us per tile) and the issuer hands the two slots back.
-// K_j is held from S_j to dQ_j, about one and a half steps, and the deeper even ring
-// lets its load start well before it is needed.  Per key tile j:
-// as soon as the element-wise warps have read S_j into registers the issuer runs
-// S_{j+1}; when dS_j is back in TMEM (over dP_j) it runs dQ += dS_j K_j and then
-// dP_{j+1} into the same columns (tcgen05 ops of one thread execute in issue
+// even items, 2 for odd ones; 10 at d = 64: 7 and 3).  Per query head it streams Q
+// and dO (items 0 and 1, whole tiles by TMA), then K_j and V_j as items 2 + 2j and
+// 3 + 2j.  The element-wise warps copy their rows of Q and dO from the ring into TMEM
+// (whole-tile loads, then conflict-free reads of the swizzled rows: a warp-wide load
+// of 32 scattered rows from global memory took about 3 us per tile) and the issuer
+// hands the two slots back.  K_j is held from S_j to dQ_j, about one and a half
+// steps, and the deeper even ring lets its load start well before it is needed.
+//
+// Per key tile j: as soon as the element-wise warps have read S_j into registers the
+// issuer runs S_{j+1}; when dS_j is back in TMEM (over dP_j) it runs dQ += dS_j K_j
+// and then dP_{j+1} into the same columns (tcgen05 ops of one thread execute in issue
 // order, so dQ_j has read dS_j first).  V_j's slot is released after dP_j, K_j's
-// after dQ_j.  Every
-// signal waits for its waiter's previous phase: S_{j+1} needs S_j read, dP_{j+1}
-// needs dS_j written, so no mbarrier or named barrier runs two phases ahead.
+// after dQ_j.  Every signal waits for its waiter's previous phase: S_{j+1} needs S_j
+// read, dP_{j+1} needs dS_j written, so no mbarrier or named barrier runs two phases
+// ahead.
 //
 // A CTA may serve several query heads of one key/value group (p.dq_heads, chosen
 // at launch so that enough CTAs remain): their K/V tiles are the same, so the ring
 // streams them head after head without a break and the CTA's fixed costs (barrier
 // set-up, TMEM allocation, the first loads) are paid once.  Steps are counted over
 // all heads (J = t nk + j for head t), ring items too (2 nk + 2 per head), and so are
-// the mbarrier phases.  Head t+1's Q and dO go into TMEM once acc_full has shown that every
-// product of head t is complete; its first dQ product overwrites the accumulator only
-// after all element-wise warps have passed head t's epilogue (they signal dS_0 of
-// head t+1 after it).  Only the last head's epilogue stages through the ring's shared
-// memory, which is idle by then; earlier heads store their dQ rows directly.
+// the mbarrier phases.  Head t+1's Q and dO go into TMEM once acc_full has shown that
+// every product of head t is complete; its first dQ product overwrites the
+// accumulator only after all element-wise warps have passed head t's epilogue (they
+// signal dS_0 of head t+1 after it).  Only the last head's epilogue stages through the
+// ring's shared memory, which is idle by then; earlier heads store their dQ rows
+// directly.
 
 template <int D, int E, bool DROP, bool HL>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
-    using R = Ring<C::kSlotsDq, C::kSlotsOddDq>;   // K_j (even) and V_j (odd)
+    using R = Ring<C::kSlotsDq, C::kSlotsOddDq>;   // Q and K_j (even), dO and V_j (odd)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Launched as a programmatic dependent of the dK/dV kernel: it may start while
     // that grid finishes.  Before exiting, every CTA waits for that grid, so the

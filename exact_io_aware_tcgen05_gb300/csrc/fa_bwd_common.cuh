@@ -34,8 +34,8 @@ struct BwdCfg {
     // kind a prefetch distance of its own.
     static constexpr int kSlotsOdd = (D == 128) ? 2 : 3;
     // The dQ kernel keeps Q and dO in TMEM (below), so every tile of shared memory
-    // belongs to its ring: 7 (d = 128) or 10 (d = 64) slots, of which V_j takes
-    // kSlotsOddDq.
+    // belongs to its ring: 7 (d = 128) or 10 (d = 64) slots, of which the odd items
+    // (each head's dO, then its V_j) take kSlotsOddDq and the even ones (Q, K_j) the rest.
     static constexpr int kSlotsDq = kSlots + 2;
     static constexpr int kSlotsOddDq = (D == 128) ? 2 : 3;
     // element-wise warpgroups, each owning kEwCols of the 128 tile columns.  Two at
