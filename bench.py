@@ -310,6 +310,17 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def served_heads(w, fp8: bool, bwd: bool, fused: bool):
+    """(forward, dQ) query heads per CTA of a run on this thread's settings; dQ is None
+    without a split backward."""
+    import exact_io_aware_tcgen05_gb300 as fa
+    q = (w.B, w.Hq, w.Hkv, w.N, w.d, int(w.causal), w.window, w.total_tokens if w.packed else 0)
+    one = fp8 or w.p_drop > 0
+    fwd = 1 if one else fa.fa_fwd_heads(*q)
+    dq = None if (not bwd or fused) else (1 if w.p_drop > 0 else fa.fa_bwd_dq_heads(*q))
+    return fwd, dq
+
+
 def workload_config(w, l2_note):
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
            "causal": w.causal, "window": w.window, "packed": w.packed,
@@ -641,10 +652,9 @@ def run_ours(args, w):
             "gpu_launches": world * K * (1 + (bwd_kernels if bwd else 0)), "clocks": clocks,
             "bwd_path": ("fused" if fused else "split") if bwd else None,
         }
-        if bwd and not fused and args.dq_heads:
-            line["dq_heads"] = args.dq_heads
-        if args.fwd_heads:
-            line["fwd_heads"] = args.fwd_heads
+        # query heads per CTA the kernels served: the library's choice, or the count the
+        # options above forced (dropout and fp8 forwards serve one head per CTA)
+        line["fwd_heads"], line["dq_heads"] = served_heads(w, fp8, bwd, fused)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -23,7 +23,8 @@ __all__ = [
     "FA_BWD_FUSED",
     "fa_bwd_static_workspace", "FA_STATIC_WORKSPACE_BYTES", "FA_DTYPE_BF16", "FA_DTYPE_F16",
     "fa_fp8_scale_blocks", "fa_fp8_vt_tokens", "fa_fp8_quantize_qk", "fa_fp8_quantize_v",
-    "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads", "fa_fwd_set_heads",
+    "fa_fp8_quantize_qk_incoherent", "fa_bwd_set_dq_heads", "fa_fwd_set_heads", "fa_fwd_heads",
+    "fa_bwd_dq_heads",
     "fa_fwd_fp8", "Fp8Operands", "quantize_fp8", "attention_forward_fp8",
     "fa_device_status",
     "fa_set_wait_limit_cycles", "fa_set_launch_events", "fa_last_error", "attention_forward", "attention_backward",
@@ -78,6 +79,9 @@ def load(path: str | None = None):
     lib.fa_fwd_set_heads.restype = _i
     lib.fa_bwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _sz]
     lib.fa_bwd_path.restype = _i
+    for name in ("fa_fwd_heads", "fa_bwd_dq_heads"):
+        getattr(lib, name).argtypes = [_i] * 8
+        getattr(lib, name).restype = _i
     lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                            _vp, _i, _f, _vp, _sz, _vp]
     lib.fa_bwd.restype = _i
@@ -187,6 +191,20 @@ def fa_bwd_set_dq_heads(heads: int) -> None:
     """Query heads per dQ CTA of the split backward on this thread (0: automatic;
     see include/fa.h)."""
     _check(load().fa_bwd_set_dq_heads(int(heads)))
+
+
+def fa_fwd_heads(B, Hq, Hkv, N, d, causal, window, total_tokens) -> int:
+    """Query heads per CTA fa_fwd would serve on this thread for these sizes (total_tokens:
+    T for a packed batch, 0 for a dense one; -1: fa_fwd would fail)."""
+    return int(load().fa_fwd_heads(B, Hq, Hkv, N, d, int(bool(causal)), int(window),
+                                   int(total_tokens)))
+
+
+def fa_bwd_dq_heads(B, Hq, Hkv, N, d, causal, window, total_tokens) -> int:
+    """Query heads per dQ CTA the split backward would serve on this thread (as
+    fa_fwd_heads)."""
+    return int(load().fa_bwd_dq_heads(B, Hq, Hkv, N, d, int(bool(causal)), int(window),
+                                      int(total_tokens)))
 
 
 def fa_bwd_path(B, Hq, Hkv, N, d, causal, window, total_tokens, workspace_bytes) -> int:

@@ -457,6 +457,27 @@ fa_status fa_bwd_set_dq_heads(int heads) {
     return FA_OK;
 }
 
+int fa_fwd_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens) {
+    // the block count of a packed batch needs only T and B: a non-null stand-in marks it
+    static const int kPacked = 0;
+    fa::Geometry g;
+    if (fa::check_common(B, Hq, Hkv, N, d, causal, window, total_tokens > 0 ? &kPacked : nullptr,
+                         total_tokens, 1.f, &g) != FA_OK)
+        return -1;
+    if (t_fwd_heads > 0) return Hq % t_fwd_heads == 0 ? t_fwd_heads : -1;
+    return fa::fwd_heads_per_cta(g, Hq, Hkv);
+}
+
+int fa_bwd_dq_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens) {
+    static const int kPacked = 0;
+    fa::Geometry g;
+    if (fa::check_common(B, Hq, Hkv, N, d, causal, window, total_tokens > 0 ? &kPacked : nullptr,
+                         total_tokens, 1.f, &g) != FA_OK)
+        return -1;
+    if (t_dq_heads > 0) return (Hq / Hkv) % t_dq_heads == 0 ? t_dq_heads : -1;
+    return fa::heads_per_cta(g, kBlockM, Hq, Hkv);
+}
+
 int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens,
                 size_t workspace_bytes) {
     fa::BwdWorkspace w;

@@ -116,6 +116,16 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_set_heads(int heads);
 
 /*
+ * How many query heads per CTA fa_fwd (16-bit, no dropout) would serve on the calling
+ * thread for these sizes: the fa_fwd_set_heads value if one is set, else the library's
+ * choice above.  total_tokens: T for a packed batch, 0 for a dense one (the choice needs
+ * only the token and sequence counts, not cu_seqlens).  The SM count is the current
+ * device's, 152 (GB300) when none can be queried.  -1 for invalid sizes or a set value
+ * that does not divide Hq (fa_fwd would fail).  No device work.
+ */
+int fa_fwd_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens);
+
+/*
  * Backward paths.  fa_bwd runs one of two:
  *   split  the row statistics D_i = sum_c dO_ic O_ic, a dK/dV kernel, then a dQ
  *          kernel that rebuilds S and dP a second time (any mask);
@@ -174,6 +184,14 @@ int fa_bwd_path(int B, int Hq, int Hkv, int N, int d, int causal, int window, in
  * heads < 0.
  */
 fa_status fa_bwd_set_dq_heads(int heads);
+
+/*
+ * How many query heads per dQ CTA the split backward (no dropout) would serve on the
+ * calling thread for these sizes: the fa_bwd_set_dq_heads value if one is set, else the
+ * library's choice above.  Arguments as for fa_fwd_heads; -1 for invalid sizes or a set
+ * value that does not divide the group (fa_bwd would fail).  No device work.
+ */
+int fa_bwd_dq_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens);
 
 /*
  * fa_fwd and fa_bwd for an explicit element type: `dtype` gives the type of

@@ -181,6 +181,45 @@ def test_fwd_heads_knob_is_validated_before_any_launch(lib):
         fa.fa_fwd_set_heads(0)
 
 
+def test_heads_per_cta_choices_on_the_measured_workloads(lib):
+    """The library's heads-per-CTA choices (with no device to query, the 152 SMs of a
+    GB300), each the one measured fastest on GB300: one head per CTA on B2 H16 N8192; two
+    per forward CTA on B4 H16 N2048 (short MHA sequences); on the GQA workloads (group of
+    4) two per forward CTA and the whole group per dQ CTA at N = 16384 with a 4096-key
+    window, and the whole group for both on 16 packed sequences and on 1024 short ones."""
+    from exact_io_aware_tcgen05_gb300.workloads import WORKLOADS
+    fa, _ = lib
+    want = {"fwdbwd_b2_h16_n8192_d128_causal": (1, 1), "fwd_b4_h16_n2048_d128_causal": (2, 1),
+            "fwdbwd_b1_h32kv8_n16384_d128_causal_w4096": (2, 4),
+            "fwdbwd_varlen16_h32kv8_d128_causal": (4, 4),
+            "fwdbwd_varlen1024_h32kv8_d128_causal": (4, 4)}
+    for name, (f, q) in want.items():
+        w = WORKLOADS[name]
+        T = w.total_tokens if w.packed else 0
+        args = (w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, w.window, T)
+        assert (fa.fa_fwd_heads(*args), fa.fa_bwd_dq_heads(*args)) == (f, q), name
+
+
+def test_heads_queries_follow_the_thread_knobs(lib):
+    """A set count is reported as long as it divides Hq (forward) or the group (dQ);
+    otherwise, and for invalid sizes, the queries answer -1 as the calls would fail."""
+    fa, _ = lib
+    args = (1, 32, 8, 16384, 128, 1, 4096, 0)
+    try:
+        fa.fa_fwd_set_heads(8)
+        fa.fa_bwd_set_dq_heads(2)
+        assert fa.fa_fwd_heads(*args) == 8 and fa.fa_bwd_dq_heads(*args) == 2
+        fa.fa_fwd_set_heads(3)
+        fa.fa_bwd_set_dq_heads(8)                          # divides Hq, not the group of 4
+        assert fa.fa_fwd_heads(*args) == -1 and fa.fa_bwd_dq_heads(*args) == -1
+    finally:
+        fa.fa_fwd_set_heads(0)
+        fa.fa_bwd_set_dq_heads(0)
+    assert fa.fa_fwd_heads(1, 32, 8, 16384, 96, 1, 0, 0) == -1      # head dimension
+    assert fa.fa_bwd_dq_heads(1, 6, 4, 128, 64, 1, 0, 0) == -1       # Hq % Hkv != 0
+    assert fa.fa_fwd_heads(1, 32, 8, 16384, 128, 1, 4096, 0) == 2    # knobs were reset
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import exact_io_aware_tcgen05_gb300 as fa
     saved = fa._lib

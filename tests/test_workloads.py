@@ -119,3 +119,13 @@ def test_roofline_bound_follows_arithmetic_intensity():
         assert bound("fwdbwd_varlen1024_h32kv8_d128_causal", k) == "hbm"
     assert bound("fwd_b4_h16_n2048_d128_causal", "fa_fwd") == "tensor"
     assert bound("fwd_b1_h1_n128_d64", "fa_fwd") == "hbm"
+
+
+def test_bench_reports_the_heads_the_kernels_serve():
+    """The bench line's heads per CTA: the library's choice for 16-bit calls without
+    dropout, one for dropout and fp8 forwards, and no dQ count without a split backward."""
+    import bench
+    assert bench.served_heads(WORKLOADS["fwdbwd_b1_h32kv8_n16384_d128_causal_w4096"], False, True, False) == (2, 4)
+    assert bench.served_heads(WORKLOADS["fwdbwd_b2_h16_n8192_d128_causal_dropout10"], False, True, False) == (1, 1)
+    assert bench.served_heads(WORKLOADS["fwd_b2_h16_n8192_d128_causal_fp8"], True, False, False) == (1, None)
+    assert bench.served_heads(WORKLOADS["fwdbwd_varlen16_h32kv8_d64_causal"], False, True, True) == (4, None)
