@@ -250,6 +250,16 @@ int fwd_heads_per_cta(const Geometry& g, int Hq, int Hkv) {
     return 2LL * num_blocks(g, rows, Hq / 2) >= 3LL * sm_count() ? 2 : 1;
 }
 
+// The geometry of a query about sizes alone (no tensors): total_tokens > 0 marks a packed
+// batch, whose block counts need only T and B, so a non-null stand-in takes cu_seqlens'
+// place.  False where the sizes are invalid (the calls would fail).
+bool query_geometry(int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                    int total_tokens, Geometry* g) {
+    static const int kPacked = 0;
+    return check_common(B, Hq, Hkv, N, d, causal, window, total_tokens > 0 ? &kPacked : nullptr,
+                        total_tokens, 1.f, g) == FA_OK;
+}
+
 fa_status check_dtype(fa_dtype dtype, const char* who) {
     if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16)
         return fail(FA_ERR_UNSUPPORTED, "%s: element type %d is neither FA_DTYPE_BF16 nor FA_DTYPE_F16",
@@ -458,22 +468,15 @@ fa_status fa_bwd_set_dq_heads(int heads) {
 }
 
 int fa_fwd_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens) {
-    // the block count of a packed batch needs only T and B: a non-null stand-in marks it
-    static const int kPacked = 0;
     fa::Geometry g;
-    if (fa::check_common(B, Hq, Hkv, N, d, causal, window, total_tokens > 0 ? &kPacked : nullptr,
-                         total_tokens, 1.f, &g) != FA_OK)
-        return -1;
+    if (!fa::query_geometry(B, Hq, Hkv, N, d, causal, window, total_tokens, &g)) return -1;
     if (t_fwd_heads > 0) return Hq % t_fwd_heads == 0 ? t_fwd_heads : -1;
     return fa::fwd_heads_per_cta(g, Hq, Hkv);
 }
 
 int fa_bwd_dq_heads(int B, int Hq, int Hkv, int N, int d, int causal, int window, int total_tokens) {
-    static const int kPacked = 0;
     fa::Geometry g;
-    if (fa::check_common(B, Hq, Hkv, N, d, causal, window, total_tokens > 0 ? &kPacked : nullptr,
-                         total_tokens, 1.f, &g) != FA_OK)
-        return -1;
+    if (!fa::query_geometry(B, Hq, Hkv, N, d, causal, window, total_tokens, &g)) return -1;
     if (t_dq_heads > 0) return (Hq / Hkv) % t_dq_heads == 0 ? t_dq_heads : -1;
     return fa::heads_per_cta(g, kBlockM, Hq, Hkv);
 }
