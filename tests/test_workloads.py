@@ -129,3 +129,27 @@ def test_bench_reports_the_heads_the_kernels_serve():
     assert bench.served_heads(WORKLOADS["fwdbwd_b2_h16_n8192_d128_causal_dropout10"], False, True, False) == (1, 1)
     assert bench.served_heads(WORKLOADS["fwd_b2_h16_n8192_d128_causal_fp8"], True, False, False) == (1, None)
     assert bench.served_heads(WORKLOADS["fwdbwd_varlen16_h32kv8_d64_causal"], False, True, True) == (4, None)
+
+
+def test_traffic_records_follow_the_kernel_sources(tmp_path, monkeypatch):
+    """bench.py reports a kernel's recorded DRAM bytes only while the hash of its source
+    files (which exist, one entry per kernel) is the one stored with the record."""
+    import json
+    import os
+    import bench
+    csrc = os.path.join(bench.ROOT, "exact_io_aware_tcgen05_gb300", "csrc")
+    kernels = set(bench.KERNEL_FLOPS_PER_PAIR_D) | {"fa_bwd_preprocess", "fa_bwd_dq_convert"}
+    assert set(bench.KERNEL_SOURCES) == kernels
+    for k, files in bench.KERNEL_SOURCES.items():
+        for f in files + tuple(bench.SHARED_SOURCES):
+            assert os.path.exists(os.path.join(csrc, f)), (k, f)
+        assert len(bench.source_sha(k)) == 16
+    (tmp_path / "profiles").mkdir()
+    rec = {"about": "test", "w": {"fa_fwd": {"dram_bytes_per_launch": 123, "source_sha": "a" * 16},
+                                  "fa_bwd_dkdv": {"dram_bytes_per_launch": 456, "source_sha": "b" * 16}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_sha", lambda k: "a" * 16)
+    assert bench.recorded_traffic("fa_fwd", "w") == 123
+    assert bench.recorded_traffic("fa_bwd_dkdv", "w") is None      # source changed since
+    assert bench.recorded_traffic("fa_fwd", "other") is None        # never captured
