@@ -180,6 +180,10 @@ DQ_HEADS_CASES = [
     (5, 4, 1, 513, 128, False, 0, (1, 127, 0, 129, 513), "f16", None),   # packed, empty seq
     (3, 6, 2, 260, 64, True, 0, (260, 1, 131), "bf16", None),        # group of 3
     (2, 4, 2, 384, 128, True, 0, None, "bf16", (0.1, 77, 3)),        # dropout: one head per CTA whatever is asked
+    # 9 key tiles per head: Q, dO and the K/V tiles of up to 4 heads wrap the dQ kernel's
+    # slot ring many times (items counted over all heads)
+    (1, 8, 2, 1100, 64, False, 0, None, "bf16", None),
+    (1, 8, 2, 1100, 128, True, 0, None, "bf16", None),
 ]
 
 
